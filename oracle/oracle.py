@@ -1,0 +1,275 @@
+"""ctypes binding of the C oracle (``nvfp4moe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the checker the CUDA path is compared against.
+Arrays are numpy; every function returns fresh numpy arrays.  The math lives
+in the C file; this module only marshals arguments.
+"""
+import ctypes as C
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        _lib = C.CDLL(path)
+        _declare(_lib)
+    return _lib
+
+
+_P = C.c_void_p
+_I64 = C.c_int64
+
+
+def _declare(L):
+    L.orc_e2m1_value.restype = C.c_double
+    L.orc_e2m1_value.argtypes = [C.c_int]
+    L.orc_e4m3_value.restype = C.c_double
+    L.orc_e4m3_value.argtypes = [C.c_int]
+    L.orc_e4m3_encode.restype = C.c_int
+    L.orc_e4m3_encode.argtypes = [C.c_float]
+    L.orc_e2m1_encode.restype = C.c_int
+    L.orc_e2m1_encode.argtypes = [C.c_float]
+    L.orc_round_bf16.restype = C.c_float
+    L.orc_round_bf16.argtypes = [C.c_float]
+    L.orc_tensor_scale.restype = C.c_float
+    L.orc_tensor_scale.argtypes = [_P, _I64, _I64, _I64]
+    L.orc_quantize_block.restype = None
+    L.orc_quantize_block.argtypes = [_P, C.c_float, _P, _P]
+    L.orc_quantize.restype = None
+    L.orc_quantize.argtypes = [_P, _I64, _I64, _I64, C.c_int, _P, _P, _P]
+    L.orc_dequantize.restype = None
+    L.orc_dequantize.argtypes = [_P, _P, C.c_float, _I64, _I64, _P]
+    L.orc_route.restype = None
+    L.orc_route.argtypes = [_P, C.c_int, C.c_int, C.c_int, _P, _P]
+    L.orc_permute.restype = None
+    L.orc_permute.argtypes = [_P, C.c_int, C.c_int, C.c_int, _P, _P, _P]
+    L.orc_grouped_gemm_w4a4.restype = None
+    L.orc_grouped_gemm_w4a4.argtypes = [_P, _P, C.c_float, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, _P]
+    L.orc_grouped_gemm_w4a16.restype = None
+    L.orc_grouped_gemm_w4a16.argtypes = [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, _P]
+    L.orc_swiglu.restype = None
+    L.orc_swiglu.argtypes = [_P, _I64, _I64, _P]
+    L.orc_combine.restype = None
+    L.orc_combine.argtypes = [_P, _P, _P, C.c_int, C.c_int, _I64, _P]
+    layer_args = [C.c_int, _P, _P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                  _P, _P, _P, _P, _P, _P, C.c_float, _P]
+    L.orc_moe_layer.restype = None
+    L.orc_moe_layer.argtypes = layer_args + [_P] * 9
+    L.orc_moe_layer_naive.restype = None
+    L.orc_moe_layer_naive.argtypes = layer_args
+    L.orc_num_threads.restype = C.c_int
+    L.orc_num_threads.argtypes = []
+
+
+def _c(a, dtype):
+    """Contiguous array of the given dtype (copy only if needed)."""
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+# --------------------------------------------------------------------------
+# scalar format helpers
+# --------------------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return lib().orc_e2m1_value(int(code))
+
+
+def e4m3_value(code: int) -> float:
+    return lib().orc_e4m3_value(int(code))
+
+
+def e4m3_encode(b: float) -> int:
+    return lib().orc_e4m3_encode(float(np.float32(b)))
+
+
+def e2m1_encode(q: float) -> int:
+    return lib().orc_e2m1_encode(float(np.float32(q)))
+
+
+def round_bf16(v: float) -> float:
+    return float(lib().orc_round_bf16(float(np.float32(v))))
+
+
+def num_threads() -> int:
+    return lib().orc_num_threads()
+
+
+# --------------------------------------------------------------------------
+# array functions
+# --------------------------------------------------------------------------
+
+def tensor_scale(x) -> np.float32:
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    return np.float32(lib().orc_tensor_scale(_p(x), rows, cols, cols))
+
+
+def quantize(x, S=None):
+    """NVFP4-quantise x [rows, cols]. S=None: dynamic (S = amax/2688).
+    Returns (codes uint8 [rows, cols/2], scales uint8 [rows, cols/16], S)."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 16), np.uint8)
+    s = np.zeros(1, np.float32)
+    if S is not None:
+        s[0] = np.float32(S)
+    lib().orc_quantize(_p(x), rows, cols, cols, 0 if S is not None else 1, _p(s), _p(codes), _p(scales))
+    return codes, scales, np.float32(s[0])
+
+
+def quantize_block(xb, S):
+    xb = _c(xb, np.float32)
+    assert xb.shape == (16,)
+    sc = np.zeros(1, np.uint8)
+    ec = np.zeros(16, np.uint8)
+    lib().orc_quantize_block(_p(xb), float(np.float32(S)), _p(sc), _p(ec))
+    return int(sc[0]), ec
+
+
+def dequantize(codes, scales, S, cols):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    rows = codes.shape[0]
+    out = np.zeros((rows, cols), np.float64)
+    lib().orc_dequantize(_p(codes), _p(scales), float(np.float32(S)), rows, cols, _p(out))
+    return out
+
+
+def route(logits, k):
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    lib().orc_route(_p(logits), T, E, k, _p(ids), _p(w))
+    return ids, w
+
+
+def permute(ids, E):
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    offsets = np.zeros(E + 1, np.int32)
+    perm = np.zeros(T * k, np.int32)
+    inv = np.zeros(T * k, np.int32)
+    lib().orc_permute(_p(ids), T, E, k, _p(offsets), _p(perm), _p(inv))
+    return offsets, perm, inv
+
+
+def grouped_gemm_w4a4(a_codes, a_scales, S_a, w_codes, w_scales, w_S, offsets):
+    a_codes = _c(a_codes, np.uint8)
+    a_scales = _c(a_scales, np.uint8)
+    w_codes = _c(w_codes, np.uint8)
+    w_scales = _c(w_scales, np.uint8)
+    w_S = _c(w_S, np.float32)
+    offsets = _c(offsets, np.int32)
+    E, N, Kh = w_codes.shape
+    K = 2 * Kh
+    R = int(offsets[E])
+    out = np.zeros((R, N), np.float64)
+    lib().orc_grouped_gemm_w4a4(_p(a_codes), _p(a_scales), float(np.float32(S_a)), _p(w_codes), _p(w_scales),
+                                _p(w_S), _p(offsets), E, N, K, _p(out))
+    return out
+
+
+def grouped_gemm_w4a16(a, w_codes, w_scales, w_S, offsets):
+    a = _c(a, np.float32)
+    w_codes = _c(w_codes, np.uint8)
+    w_scales = _c(w_scales, np.uint8)
+    w_S = _c(w_S, np.float32)
+    offsets = _c(offsets, np.int32)
+    E, N, Kh = w_codes.shape
+    K = 2 * Kh
+    R = int(offsets[E])
+    out = np.zeros((R, N), np.float64)
+    lib().orc_grouped_gemm_w4a16(_p(a), _p(w_codes), _p(w_scales), _p(w_S), _p(offsets), E, N, K, _p(out))
+    return out
+
+
+def swiglu(G):
+    G = _c(G, np.float32)
+    R, I2 = G.shape
+    h = np.zeros((R, I2 // 2), np.float64)
+    lib().orc_swiglu(_p(G), R, I2 // 2, _p(h))
+    return h
+
+
+def combine(Y, inv, w):
+    Y = _c(Y, np.float32)
+    w = _c(w, np.float64)
+    inv = _c(inv, np.int32)
+    T, k = w.shape
+    H = Y.shape[1]
+    out = np.zeros((T, H), np.float64)
+    lib().orc_combine(_p(Y), _p(inv), _p(w), T, k, H, _p(out))
+    return out
+
+
+def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False):
+    """Full layer.  mode: 'w4a4' | 'w4a16'.  w13 / w2: (codes, scales, S[E]).
+    Returns out fp64 [T, H] (and a dict of intermediates if asked)."""
+    x = _c(x, np.float32)
+    logits = _c(logits, np.float32)
+    T, H = x.shape
+    E = logits.shape[1]
+    c13, s13, S13 = (_c(w13[0], np.uint8), _c(w13[1], np.uint8), _c(w13[2], np.float32))
+    c2, s2, S2 = (_c(w2[0], np.uint8), _c(w2[1], np.uint8), _c(w2[2], np.float32))
+    I = c2.shape[2] * 2
+    R = T * k
+    out = np.zeros((T, H), np.float64)
+    m = 0 if mode == "w4a4" else 1
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    offsets = np.zeros(E + 1, np.int32)
+    perm = np.zeros(R, np.int32)
+    inv = np.zeros(R, np.int32)
+    S_x = np.zeros(1, np.float32)
+    hq_c = np.zeros((R, I // 2), np.uint8)
+    hq_s = np.zeros((R, I // 16), np.uint8)
+    h32 = np.zeros((R, I), np.float32)
+    lib().orc_moe_layer(m, _p(x), _p(logits), T, H, I, E, k, _p(c13), _p(s13), _p(S13), _p(c2), _p(s2), _p(S2),
+                        float(np.float32(S_h)), _p(out), _p(ids), _p(w), _p(offsets), _p(perm), _p(inv), _p(S_x),
+                        _p(hq_c), _p(hq_s), _p(h32))
+    if not intermediates:
+        return out
+    return out, dict(ids=ids, w=w, offsets=offsets, perm=perm, inv=inv, S_x=np.float32(S_x[0]),
+                     hq_codes=hq_c, hq_scales=hq_s, h32=h32)
+
+
+def moe_layer_naive(mode, x, logits, k, w13, w2, S_h):
+    x = _c(x, np.float32)
+    logits = _c(logits, np.float32)
+    T, H = x.shape
+    E = logits.shape[1]
+    c13, s13, S13 = (_c(w13[0], np.uint8), _c(w13[1], np.uint8), _c(w13[2], np.float32))
+    c2, s2, S2 = (_c(w2[0], np.uint8), _c(w2[1], np.uint8), _c(w2[2], np.float32))
+    I = c2.shape[2] * 2
+    out = np.zeros((T, H), np.float64)
+    m = 0 if mode == "w4a4" else 1
+    lib().orc_moe_layer_naive(m, _p(x), _p(logits), T, H, I, E, k, _p(c13), _p(s13), _p(S13), _p(c2), _p(s2),
+                              _p(S2), float(np.float32(S_h)), _p(out))
+    return out
+
+
+def quantize_experts(w):
+    """Quantise a stack of expert weight matrices w [E, N, K] one expert at a
+    time, each with its own dynamic per-tensor scale.  Returns (codes
+    [E, N, K/2], scales [E, N, K/16], S [E])."""
+    w = np.asarray(w, np.float32)
+    E, N, K = w.shape
+    codes = np.zeros((E, N, K // 2), np.uint8)
+    scales = np.zeros((E, N, K // 16), np.uint8)
+    S = np.zeros(E, np.float32)
+    for e in range(E):
+        codes[e], scales[e], S[e] = quantize(w[e])
+    return codes, scales, S
