@@ -368,11 +368,14 @@ void orc_combine(const float* Y, const int32_t* inv, const double* w, int T, int
  *   (W4A4: requantise h with the static S_h | W4A16: round h to bf16) ->
  *   down grouped GEMM (Y stored fp32) -> weighted combine (out fp64).
  * mode 0 = W4A4, 1 = W4A16.  x is [T, H] (bf16 values widened to fp32).
+ * S_x_in: NULL = the dynamic per-tensor scale of these T rows; otherwise the
+ * scale of a larger tensor these rows were taken from (to check a sample of
+ * tokens of a big batch, the scale must be the whole batch's).
  * Optional intermediate outputs may be NULL. */
 void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, int I, int E, int k,
                    const uint8_t* w13_codes, const uint8_t* w13_scales, const float* w13_S,
                    const uint8_t* w2_codes, const uint8_t* w2_scales, const float* w2_S, float S_h,
-                   double* out, int32_t* ids_o, double* w_o, int32_t* offsets_o, int32_t* perm_o,
+                   const float* S_x_in, double* out, int32_t* ids_o, double* w_o, int32_t* offsets_o, int32_t* perm_o,
                    int32_t* inv_o, float* S_x_o, uint8_t* hq_codes_o, uint8_t* hq_scales_o, float* h32_o) {
   int R = T * k;
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
@@ -396,7 +399,8 @@ void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, 
     uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 16);
     uint8_t* ac = (uint8_t*)malloc((size_t)R * H / 2);
     uint8_t* as = (uint8_t*)malloc((size_t)R * H / 16);
-    orc_quantize(x, T, H, H, 1, &S_x, xc, xs);
+    if (S_x_in) S_x = *S_x_in;
+    orc_quantize(x, T, H, H, S_x_in ? 0 : 1, &S_x, xc, xs);
     for (int r = 0; r < R; ++r) {
       memcpy(ac + (int64_t)r * H / 2, xc + (int64_t)perm[r] * H / 2, (size_t)H / 2);
       memcpy(as + (int64_t)r * H / 16, xs + (int64_t)perm[r] * H / 16, (size_t)H / 16);
@@ -449,7 +453,7 @@ void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, 
 void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, int H, int I, int E, int k,
                          const uint8_t* w13_codes, const uint8_t* w13_scales, const float* w13_S,
                          const uint8_t* w2_codes, const uint8_t* w2_scales, const float* w2_S, float S_h,
-                         double* out) {
+                         const float* S_x_in, double* out) {
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
   orc_route(logits, T, E, k, ids, w);
@@ -457,8 +461,8 @@ void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, i
   if (mode == 0) {
     uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
     uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 16);
-    float S_x = 0.0f;
-    orc_quantize(x, T, H, H, 1, &S_x, xc, xs);
+    float S_x = S_x_in ? *S_x_in : 0.0f;
+    orc_quantize(x, T, H, H, S_x_in ? 0 : 1, &S_x, xc, xs);
     orc_dequantize(xc, xs, S_x, T, H, xd);
     free(xc); free(xs);
   } else {

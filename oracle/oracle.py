@@ -58,7 +58,7 @@ def _declare(L):
     L.orc_combine.restype = None
     L.orc_combine.argtypes = [_P, _P, _P, C.c_int, C.c_int, _I64, _P]
     layer_args = [C.c_int, _P, _P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
-                  _P, _P, _P, _P, _P, _P, C.c_float, _P]
+                  _P, _P, _P, _P, _P, _P, C.c_float, _P, _P]
     L.orc_moe_layer.restype = None
     L.orc_moe_layer.argtypes = layer_args + [_P] * 9
     L.orc_moe_layer_naive.restype = None
@@ -215,9 +215,15 @@ def combine(Y, inv, w):
     return out
 
 
-def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False):
+def _sx(S_x):
+    return None if S_x is None else np.array([S_x], np.float32)
+
+
+def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False, S_x=None):
     """Full layer.  mode: 'w4a4' | 'w4a16'.  w13 / w2: (codes, scales, S[E]).
-    Returns out fp64 [T, H] (and a dict of intermediates if asked)."""
+    S_x: None = dynamic activation scale of x; else the given scale (for a
+    sample of rows of a larger batch).  Returns out fp64 [T, H] (and a dict
+    of intermediates if asked)."""
     x = _c(x, np.float32)
     logits = _c(logits, np.float32)
     T, H = x.shape
@@ -233,20 +239,21 @@ def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False):
     offsets = np.zeros(E + 1, np.int32)
     perm = np.zeros(R, np.int32)
     inv = np.zeros(R, np.int32)
-    S_x = np.zeros(1, np.float32)
+    S_x_out = np.zeros(1, np.float32)
     hq_c = np.zeros((R, I // 2), np.uint8)
     hq_s = np.zeros((R, I // 16), np.uint8)
     h32 = np.zeros((R, I), np.float32)
+    sx = _sx(S_x)
     lib().orc_moe_layer(m, _p(x), _p(logits), T, H, I, E, k, _p(c13), _p(s13), _p(S13), _p(c2), _p(s2), _p(S2),
-                        float(np.float32(S_h)), _p(out), _p(ids), _p(w), _p(offsets), _p(perm), _p(inv), _p(S_x),
+                        float(np.float32(S_h)), _p(sx), _p(out), _p(ids), _p(w), _p(offsets), _p(perm), _p(inv), _p(S_x_out),
                         _p(hq_c), _p(hq_s), _p(h32))
     if not intermediates:
         return out
-    return out, dict(ids=ids, w=w, offsets=offsets, perm=perm, inv=inv, S_x=np.float32(S_x[0]),
+    return out, dict(ids=ids, w=w, offsets=offsets, perm=perm, inv=inv, S_x=np.float32(S_x_out[0]),
                      hq_codes=hq_c, hq_scales=hq_s, h32=h32)
 
 
-def moe_layer_naive(mode, x, logits, k, w13, w2, S_h):
+def moe_layer_naive(mode, x, logits, k, w13, w2, S_h, S_x=None):
     x = _c(x, np.float32)
     logits = _c(logits, np.float32)
     T, H = x.shape
@@ -256,8 +263,9 @@ def moe_layer_naive(mode, x, logits, k, w13, w2, S_h):
     I = c2.shape[2] * 2
     out = np.zeros((T, H), np.float64)
     m = 0 if mode == "w4a4" else 1
+    sx = _sx(S_x)
     lib().orc_moe_layer_naive(m, _p(x), _p(logits), T, H, I, E, k, _p(c13), _p(s13), _p(S13), _p(c2), _p(s2),
-                              _p(S2), float(np.float32(S_h)), _p(out))
+                              _p(S2), float(np.float32(S_h)), _p(sx), _p(out))
     return out
 
 

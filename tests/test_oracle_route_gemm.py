@@ -268,3 +268,22 @@ def test_layer_w4a16_vs_numpy_on_dequantised_weights(orc):
     # quantised matrix), so nothing is grossly wrong with the encoding itself
     ref32 = _numpy_moe(x, logits, cfg.k, w13f.astype(np.float64), w2f.astype(np.float64), cfg.I)
     assert np.linalg.norm(out - ref32) / np.linalg.norm(ref32) < 0.25
+
+
+def test_layer_token_subset_with_batch_scale(orc):
+    """Rows of the layer are independent once the activation scale is fixed:
+    running a subset of tokens (with the full batch's scale and the logits of
+    only the experts they use) reproduces those rows of the full layer."""
+    cfg = wl.small_variant(wl.CONFIGS["decode_c16"], H=256, I=128, E=32)
+    x, logits, w13f, w2f = _layer_inputs(cfg)
+    w13 = orc.quantize_experts(w13f)
+    w2 = orc.quantize_experts(w2f)
+    full = orc.moe_layer("w4a4", x, logits, cfg.k, w13, w2, cfg.S_h)
+    S_x = orc.tensor_scale(x)
+    assert np.array_equal(full, orc.moe_layer("w4a4", x, logits, cfg.k, w13, w2, cfg.S_h, S_x=S_x))
+    toks = [3, 11]
+    ids, _ = orc.route(logits[toks], cfg.k)
+    used = np.unique(ids)
+    sub = orc.moe_layer("w4a4", x[toks], logits[toks][:, used], cfg.k,
+                        tuple(a[used] for a in w13), tuple(a[used] for a in w2), cfg.S_h, S_x=S_x)
+    assert np.array_equal(sub, full[toks])
