@@ -1,0 +1,444 @@
+"""Benchmark of the NVFP4 MoE layer (decode) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_c16|decode_b512|wide] [--mode w4a4|w4a16]
+
+Prints ONE JSON line (rank 0).  A step is one full MoE layer forward over the
+workload's batch: quantise -> route/permute/gather -> gate_up grouped GEMM ->
+SwiGLU+requant -> down grouped GEMM -> combine, all through the C ABI.  The
+timed steps are replays of one CUDA graph holding K captured steps, with
+CUDA events around the gate_up grouped GEMM of every step (the dominant
+kernel) for the roofline figure.  Weights are random N(0, 0.02) quantised on
+the GPU; activations N(0, 1) bf16; routing logits per the workload recipe.
+Touched weights per step exceed the 129 MB L2 by an order of magnitude, so no
+L2 flush is needed between steps.
+
+--impl reference times the CPU oracle (the slow C restatement) on a bounded
+sample of the same workload; it is the baseline arm, not a GPU code path.
+Multi-GPU: the path does not shard (replicas only); every rank runs its own
+replica and value = all ranks' tokens / max time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WEIGHT_BYTES_PER_ELEM = 0.5 + 1.0 / 16  # E2M1 codes + one E4M3 scale per 16
+
+
+def _load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append([c.strip() for c in line.split(",")])
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for fn in ("gemm_w4a4.cu", "gemm_w4a16.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload, mode):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if there is none or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get("%s/%s" % (workload, mode))
+    if not e or e.get("kernel_hash") != _kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def gpu_weights(cfg, dev, B, wl, seed=0):
+    import torch
+    out = []
+    for which, N, K in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
+        codes = torch.empty(cfg.E, N, K // 2, dtype=torch.uint8, device=dev)
+        scales = torch.empty(cfg.E, N, K // 16, dtype=torch.uint8, device=dev)
+        S = torch.empty(cfg.E, dtype=torch.float32, device=dev)
+        for e in range(cfg.E):
+            wf = wl.expert_weight_fp32(which, e, N, K, seed, device=dev)
+            _, _, s = B.nvfp4_quantize(wf, codes=codes[e], scales=scales[e])
+            S[e:e + 1].copy_(s)
+        del wf
+        packed = B.nvfp4_pack_weight_scales(scales, cfg.E, N, K)
+        del scales
+        out.append((codes, packed, S))
+    return out
+
+
+def oracle_sample(cfg, mode, ntok, seed=0):
+    """Prepare the oracle's inputs for the first `ntok` tokens of the
+    workload (weights of the experts they use, quantised by the oracle; the
+    whole batch's activation scale).  Returns a callable that runs the
+    oracle's layer forward on that sample once."""
+    from nvfp4_mixture_experts_top_gb300 import workloads as wl
+    from oracle import oracle as orc
+    x = wl.activations_bf16(cfg.T, cfg.H, seed).float().numpy()
+    logits = wl.router_logits(cfg, seed).numpy()
+    toks = list(range(ntok))
+    ids, _ = orc.route(logits[toks], cfg.k)
+    used = np.unique(ids)
+    w13 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed).numpy()
+                                         for e in used]))
+    w2 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed).numpy()
+                                        for e in used]))
+    S_x = orc.tensor_scale(x) if mode == "w4a4" else None
+    xs, ls = x[toks], logits[toks][:, used]
+
+    def run():
+        orc.moe_layer(mode, xs, ls, cfg.k, w13, w2, cfg.S_h, S_x=S_x)
+    return run
+
+
+def cpu_baseline(cfg, mode, ntok, seed=0):
+    """Time the oracle (as it stands) on the first `ntok` tokens of the
+    workload on the host cores.  Returns (tokens/s, cores, seconds)."""
+    from oracle import oracle as orc
+    run = oracle_sample(cfg, mode, ntok, seed)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return ntok / dt, orc.num_threads(), dt
+
+
+def run_reference(args, cfg, metric, unit):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    ntok = args.ref_tokens
+    run = oracle_sample(cfg, args.mode, ntok)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        run()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    val = ntok / (ms / 1e3)
+    sample = "first %d tokens of the %s batch, oracle layer forward (weights pre-quantised)" % (ntok, cfg.name)
+    line = {"impl": "reference", "metric": metric, "value": val, "unit": unit, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "mode": args.mode, "T": cfg.T, "hidden": cfg.H,
+                       "intermediate": cfg.I, "experts": cfg.E, "top_k": cfg.k, "routing": cfg.routing},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_c16", choices=["decode_c16", "decode_b512", "wide", "tiny"])
+    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16"])
+    ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
+    ap.add_argument("--baseline-tokens", type=int, default=4, help="tokens of the in-run CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from nvfp4_mixture_experts_top_gb300 import workloads as wl
+    cfg = wl.CONFIGS[args.workload]
+    metric = "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name)
+    unit = "tokens/s"
+    if args.impl == "reference":
+        return run_reference(args, cfg, metric, unit)
+
+    import torch
+    import torch.distributed as dist
+
+    from nvfp4_mixture_experts_top_gb300 import binding as B
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.load()
+    B.nvfp4_device_check()
+    mode = B.MOE_W4A4 if args.mode == "w4a4" else B.MOE_W4A16
+
+    (w13, w2) = gpu_weights(cfg, dev, B, wl)
+    x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
+    logits = wl.router_logits(cfg, device=dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    I, H, k, T, R = cfg.I, cfg.H, cfg.k, cfg.T, cfg.R
+
+    # intermediates of the staged step (same kernels as moe_layer_forward)
+    ws_route = torch.empty(max(B.load().moe_align_permute_workspace_bytes(T, cfg.E, k), 256), dtype=torch.uint8,
+                           device=dev)
+    S_x = torch.zeros(4, dtype=torch.float32, device=dev)
+    qws = torch.empty(256, dtype=torch.uint8, device=dev)
+    xq_c = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
+    xq_s = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    inv = torch.empty(R, dtype=torch.int32, device=dev)
+    a_c = torch.empty(R, H // 2, dtype=torch.uint8, device=dev)
+    a_s = torch.empty(R, H // 16, dtype=torch.uint8, device=dev)
+    a_b = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    G = torch.empty(R, 2 * I, dtype=torch.float32, device=dev)
+    h_c = torch.empty(R, I // 2, dtype=torch.uint8, device=dev)
+    h_s = torch.empty(R, I // 16, dtype=torch.uint8, device=dev)
+    h_b = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
+    Y = torch.empty(R, H, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, dtype=torch.float32, device=dev)
+    L = B.load()
+    P = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+
+    def chk(s):
+        if s != 0:
+            raise B.Nvfp4Error("step", s)
+
+    def step(ev_pair=None):
+        st = torch.cuda.current_stream().cuda_stream
+        if mode == B.MOE_W4A4:
+            chk(L.nvfp4_quantize(P(x), 0, T, H, H, P(S_x), 1, P(xq_c), P(xq_s), P(qws), 256, st))
+            chk(L.moe_align_permute(P(logits), T, cfg.E, k, P(ids), P(tw), P(offs), P(perm), P(inv), 1, P(xq_c),
+                                    P(xq_s), H, P(a_c), P(a_s), P(status), P(ws_route), ws_route.numel(), st))
+            if ev_pair:
+                ev_pair[0].record()
+            chk(L.moe_grouped_gemm_nvfp4(0, P(a_c), P(a_s), P(S_x), P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
+                                         cfg.E, 2 * I, H, R, P(G), P(status), st))
+            if ev_pair:
+                ev_pair[1].record()
+            chk(L.moe_swiglu_requant(P(G), R, I, 0, P(S_h), P(h_c), P(h_s), None, st))
+            chk(L.moe_grouped_gemm_nvfp4(0, P(h_c), P(h_s), P(S_h), P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
+                                         cfg.E, H, I, R, P(Y), P(status), st))
+        else:
+            chk(L.moe_align_permute(P(logits), T, cfg.E, k, P(ids), P(tw), P(offs), P(perm), P(inv), 2, P(x), None,
+                                    H, P(a_b), None, P(status), P(ws_route), ws_route.numel(), st))
+            if ev_pair:
+                ev_pair[0].record()
+            chk(L.moe_grouped_gemm_nvfp4(1, P(a_b), None, None, P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
+                                         cfg.E, 2 * I, H, R, P(G), P(status), st))
+            if ev_pair:
+                ev_pair[1].record()
+            chk(L.moe_swiglu_requant(P(G), R, I, 1, None, None, None, P(h_b), st))
+            chk(L.moe_grouped_gemm_nvfp4(1, P(h_b), None, None, P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
+                                         cfg.E, H, I, R, P(Y), P(status), st))
+        chk(L.moe_combine(P(Y), P(inv), P(tw), T, k, H, 1, P(out), st))
+
+    launches_per_step = 10 if mode == B.MOE_W4A4 else 8
+
+    # warm-up (eager)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(status.item()))
+    # the staged step and the one-call layer agree bit for bit
+    ref_out = B.moe_layer_forward(mode, x, logits, k, w13, w2, S_h)
+    torch.cuda.synchronize()
+    if not torch.equal(ref_out, out):
+        raise RuntimeError("staged step and moe_layer_forward disagree")
+
+    # touched experts -> algorithmic bytes
+    counts = np.diff(offs.cpu().numpy())
+    touched = int((counts > 0).sum())
+    w13_bytes = touched * 2 * I * H * WEIGHT_BYTES_PER_ELEM
+    w2_bytes = touched * H * I * WEIGHT_BYTES_PER_ELEM
+    act_in = R * H * (WEIGHT_BYTES_PER_ELEM if mode == B.MOE_W4A4 else 2.0)
+    gemm1_bytes = w13_bytes + act_in + R * 2 * I * 4
+    layer_weight_bytes = w13_bytes + w2_bytes
+
+    # capture K steps with per-step events around the gate_up GEMM
+    K = args.steps
+    def timing_event():
+        # recorded inside the captured graph: must be an external event node
+        return torch.cuda.Event(enable_timing=True, external=True)
+
+    evs = [(timing_event(), timing_event()) for _ in range(K)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(K):
+                step(evs[i])
+    torch.cuda.synchronize()
+    graph.replay()  # one untimed replay (graph upload)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if not args.no_clocks:
+        clocks.start()
+        t_end = time.time() + 1.0  # clock window under load before the timed region
+        while time.time() < t_end:
+            graph.replay()
+        torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if not args.no_clocks:
+        clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    gemm_ms = [a.elapsed_time(b) for a, b in evs]
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d" % int(status.item()))
+    ms_step = ms_total / K
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    value = world * T / (ms_step / 1e3)
+
+    # end to end through the one-call API with host buffers
+    x_h = x.cpu().pin_memory()
+    lg_h = logits.cpu().pin_memory()
+    out_h = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(logits)
+    out_d = torch.empty_like(out)
+    wsl = torch.empty(B.moe_layer_workspace_bytes(mode, T, H, I, cfg.E, k), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        B.moe_layer_forward(mode, x_d, lg_d, k, w13, w2, S_h, out=out_d, workspace=wsl)
+        out_h.copy_(out_d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    te0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_s = (time.perf_counter() - te0) / K
+    if not torch.equal(out_h, out.cpu()):
+        raise RuntimeError("e2e result differs from the device-timed step")
+
+    hbm, _, peak_kind = _load_peaks()
+    gemm_avg_ms = statistics.mean(gemm_ms)
+    achieved = gemm1_bytes / (gemm_avg_ms / 1e3) / 1e9
+    result = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp4(e2m1)xfp4, fp32 accumulate" if mode == B.MOE_W4A4 else "fp4(e2m1)xbf16, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised on the GPU)",
+        "config": {"workload": cfg.name, "mode": args.mode, "T": T, "hidden": H, "intermediate": I,
+                   "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "no flush: %.2f GB of touched weights per step >> 129 MB L2" % (layer_weight_bytes / 1e9),
+                   "timing": "CUDA graph of %d steps, CUDA events" % K},
+        "roofline": {"kernel": "moe_grouped_gemm_nvfp4 gate_up (%s)" % args.mode, "bound": "hbm",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gemm1_bytes,
+                     "avg_launch_ms": gemm_avg_ms, "traffic": _traffic(cfg.name, args.mode)},
+        "layer_hbm": {"weight_bytes_per_step": layer_weight_bytes,
+                      "achieved_gbs": layer_weight_bytes / (ms_step / 1e3) / 1e9,
+                      "frac_of_peak": layer_weight_bytes / (ms_step / 1e3) / 1e9 / hbm},
+        "e2e": {"value": world * T / e2e_s, "unit": unit, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 4},
+        "gpu_launches": launches_per_step * K,
+    }
+    if not args.no_clocks:
+        result["clocks"] = clocks.summary()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, dt = cpu_baseline(cfg, args.mode, args.baseline_tokens)
+        result["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                                  "sample": "first %d tokens of the batch (%.1f s of oracle work)" % (
+                                      args.baseline_tokens, dt)}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * nvfp4moe.h -- C ABI of the NVFP4 mixture-of-experts decode path for GB300
+ * (sm_103a).
+ *
+ * The operation: a routed mixture-of-experts FFN whose weights are NVFP4 --
+ * FP4 E2M1 elements, one E4M3 block scale per 16 elements along K, and one
+ * FP32 per-tensor scale ("The Benchmark That Confirmed the Ceiling: NVFP4
+ * Cutlass on sm_120", section "The NVFP4 Pivot").  One layer is
+ *   route top-k -> permute by expert -> grouped GEMM gate_up -> SwiGLU ->
+ *   requantise to NVFP4 -> grouped GEMM down -> weighted combine,
+ * with tiny and ragged per-expert M ("The 2x Gap: Diagnosing Suboptimal FP4
+ * GEMM Kernels on Blackwell SM120", section "The Investigation So Far":
+ * 256 experts, 8 active, ~16 tokens per expert).  Two modes: W4A4 (FP4
+ * activations too) and W4A16 (BF16 activations, FP4 weights dequantised in
+ * the kernel) ("The 24% Ceiling", section "The Core Insight").
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers unless a comment says otherwise.  The
+ *    caller owns and frees every buffer; the library never allocates device
+ *    memory and keeps no per-call state (only cached device properties and
+ *    kernel attributes).
+ *  - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns without synchronising.
+ *  - Arguments are validated on the host before anything is launched, so a
+ *    failing call launches nothing.  The return value is an nvfp4_status.
+ *  - Kernels that consume routing data check it and report problems through
+ *    the optional `dev_status` word (int32, device memory; the kernel writes
+ *    a nonzero nvfp4_status there and skips the bad work; it never traps).
+ *  - All device pointers must be 16-byte aligned.
+ *  - Layouts are row-major.  NVFP4 tensors [rows, cols] are stored as
+ *      codes  uint8 [rows, cols/2]  (element 2i in the low nibble of byte i)
+ *      scales uint8 [rows, cols/16] (E4M3 "FN" block scales, linear)
+ *      S      fp32 scalar           (per-tensor decode scale)
+ *    and decode as value = e2m1(code) * e4m3(scale) * S.
+ *  - Requires compute capability 10.3 (GB300); other devices get
+ *    NVFP4_E_ARCH.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t; /* the same type as cudaStream_t */
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_E_INVAL = 1,          /* null pointer, negative size, bad enum       */
+  NVFP4_E_SHAPE = 2,          /* a size violates a documented constraint     */
+  NVFP4_E_ALIGN = 3,          /* a pointer is not 16-byte aligned            */
+  NVFP4_E_WORKSPACE = 4,      /* workspace missing or too small              */
+  NVFP4_E_ARCH = 5,           /* device is not compute capability 10.3       */
+  NVFP4_E_CUDA = 6,           /* a CUDA runtime/driver call failed           */
+  NVFP4_E_DEVICE_TIMEOUT = 7, /* (device) a bounded wait ran out             */
+  NVFP4_E_BAD_ROUTING = 8     /* (device) inconsistent expert offsets / ids  */
+} nvfp4_status;
+
+enum { NVFP4_DT_BF16 = 0, NVFP4_DT_F32 = 1 };
+enum { NVFP4_SCALE_STATIC = 0, NVFP4_SCALE_DYNAMIC = 1 };
+enum { MOE_W4A4 = 0, MOE_W4A16 = 1 };
+enum { MOE_ACT_NONE = 0, MOE_ACT_NVFP4 = 1, MOE_ACT_BF16 = 2 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvfp4_status_string(int status);
+
+/* Checks that the current device is a GB300 (CC 10.3) and caches its
+ * properties.  Returns NVFP4_OK or NVFP4_E_ARCH / NVFP4_E_CUDA. */
+int nvfp4_device_check(void);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_quantize -- NVFP4 quantisation of a row-major matrix.
+ * Defined by "The Benchmark That Confirmed the Ceiling", section "The NVFP4
+ * Pivot" (group-16 E4M3 scales over FP4 E2M1) and the per-tensor `alpha` of
+ * the scaled FP4 GEMM interface ("The 2x Gap", section "Discovering the
+ * sgl_kernel Alternative").  Per 16-element block along a row:
+ *   b = (amax_block / 6) / S               (two fp32 IEEE divisions)
+ *   scale = E4M3(b)                        (round-to-nearest-even, saturate 448)
+ *   d = e4m3(scale) * S                    (fp32)
+ *   code_i = E2M1(x_i / d)                 (RNE, saturate 6, sign kept)
+ * S == 0 or d == 0 gives scale 0 and codes 0.
+ *   x          [rows, cols] of x_dtype (NVFP4_DT_BF16 or NVFP4_DT_F32), row
+ *              stride ld_x elements (ld_x >= cols)
+ *   S          device fp32 scalar.  scale_mode NVFP4_SCALE_STATIC: read.
+ *              NVFP4_SCALE_DYNAMIC: written with amax(|x|) / 2688.
+ *   codes      out [rows, cols/2]; scales out [rows, cols/16]
+ *   workspace  >= nvfp4_quantize_workspace_bytes() bytes (dynamic mode only;
+ *              may be NULL in static mode)
+ * Constraints: cols % 16 == 0, ld_x % 8 == 0 (bf16) / % 4 == 0 (f32).
+ * ------------------------------------------------------------------------ */
+size_t nvfp4_quantize_workspace_bytes(int64_t rows, int64_t cols);
+int nvfp4_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x, float* S,
+                   int scale_mode, uint8_t* codes, uint8_t* scales, void* workspace, size_t workspace_bytes,
+                   nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_pack_weight_scales -- one-time reshuffle of expert weight block
+ * scales from the linear layout [E, N, K/16] into the layout the grouped
+ * GEMM reads (no counterpart on the pages; it is weight preparation, done
+ * once per set of weights, outside the per-step path).
+ * Packed layout: for expert e, 128-row tile nt = n / 128, 64-column block
+ * kb = k / 64, a 512-byte atom at byte offset ((e*N/128 + nt)*K/64 + kb)*512;
+ * inside it, row r = n % 128 and scale j = (k % 64) / 16 sit at byte
+ * (r % 32) * 16 + (r / 32) * 4 + j.
+ *   scales_linear  [E, N, K/16];  scales_packed  out, E*N*K/16 bytes.
+ * Constraints: N % 128 == 0, K % 256 == 0.
+ * ------------------------------------------------------------------------ */
+int nvfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, uint8_t* scales_packed,
+                             nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_align_permute -- router top-k plus the expert permutation.
+ * Routing: "The 2x Gap", section "The Investigation So Far" (top-8 of 256
+ * experts); "Native FP4 Is Slower ...", section 1 (22 of 512).  Per token t:
+ *   topk_ids[t, :] = the k experts with the largest logits, in descending
+ *                    logit order, ties to the lower expert id;
+ *   topk_w[t, j]   = exp(l_j - l_max) / sum over the k selected (fp32).
+ * Permutation ("expert-scatter-gather", "The 2x Gap", same section): the
+ * T*k (token, slot) pairs sorted stably by (expert, token):
+ *   expert_offsets [E+1]: exclusive prefix sum of per-expert counts;
+ *   perm[r]             : source token of permuted row r;
+ *   inv[t*k + j]        : permuted row of pair (t, j).
+ * Optional gather (act_kind != MOE_ACT_NONE): permuted activation rows
+ *   act_out[r] = act_in[perm[r]]; NVFP4 rows copy codes [.., act_cols/2] and
+ *   scales [.., act_cols/16]; BF16 rows copy [.., act_cols] bf16.
+ *   logits  fp32 [T, E];  topk_ids int32 [T, k];  topk_w fp32 [T, k]
+ *   workspace >= moe_align_permute_workspace_bytes(T, E, k)
+ * Constraints: 1 <= k <= min(E, 32), E <= 1024, T >= 0; act_cols % 32 == 0.
+ * ------------------------------------------------------------------------ */
+size_t moe_align_permute_workspace_bytes(int T, int E, int k);
+int moe_align_permute(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                      int32_t* expert_offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
+                      const uint8_t* act_in_scales, int64_t act_cols, void* act_out, uint8_t* act_out_scales,
+                      int32_t* dev_status, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_grouped_gemm_nvfp4 -- ragged grouped GEMM over experts.
+ * "The 2x Gap", sections "The Investigation So Far" and "Discovering the
+ * sgl_kernel Alternative" (scaled FP4 GEMM: block scales on both operands
+ * and one alpha); "The Benchmark That Confirmed the Ceiling", section "The
+ * NVFP4 Pivot" (native FP4xFP4 versus W4A16 dequantise-to-BF16).  For every
+ * permuted row r of expert e (expert_offsets[e] <= r < expert_offsets[e+1]):
+ *   W4A4 : out[r, n] = a_S * w_S[e] * sum_k dec(a[r,k]) * dec(w[e,n,k])
+ *   W4A16: out[r, n] =        w_S[e] * sum_k a[r,k]      * dec(w[e,n,k])
+ * with dec(.) = e2m1(code) * e4m3(block scale), fp32 accumulation.
+ *   W4A4 : a = codes [R, K/2], a_scales = [R, K/16], a_S = device fp32 scalar
+ *   W4A16: a = bf16 [R, K], a_scales = NULL, a_S = NULL
+ *   w_codes        [E, N, K/2]
+ *   w_scales_packed  from nvfp4_pack_weight_scales
+ *   w_S            fp32 [E]
+ *   expert_offsets int32 [E+1], expert_offsets[E] must equal R (checked on
+ *                  the device; a violation sets dev_status to
+ *                  NVFP4_E_BAD_ROUTING and skips the bad experts)
+ *   out            fp32 [R, N]
+ * Constraints: N % 128 == 0, K % 256 == 0, R >= 0.  Rows of out that belong
+ * to no expert are not written.
+ * ------------------------------------------------------------------------ */
+int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, const float* a_S,
+                           const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                           const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
+                           int32_t* dev_status, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_swiglu_requant -- SwiGLU on the gate_up output and requantisation.
+ * h[r, i] = silu(G[r, i]) * G[r, I + i], silu(x) = x / (1 + exp(-x)), fp32.
+ *   W4A4 : h is quantised to NVFP4 with the static decode scale *S_h
+ *          (same rule as nvfp4_quantize): h_codes [R, I/2], h_scales
+ *          [R, I/16]; h_bf16 unused (NULL).
+ *   W4A16: h is rounded to bf16 (RNE) into h_bf16 [R, I]; the NVFP4 outputs
+ *          and S_h are unused (NULL).
+ *   G fp32 [R, 2I] (gate columns 0..I-1, up columns I..2I-1).
+ * Constraints: I % 16 == 0.
+ * ------------------------------------------------------------------------ */
+int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
+                       uint8_t* h_scales, void* h_bf16, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_combine -- weighted combine of the expert outputs, done as a gather
+ * (deterministic, no atomics):
+ *   out[t, n] = sum_{j < k} topk_w[t, j] * Y[inv[t*k + j], n]   (fp32, j order)
+ *   Y fp32 [T*k, H]; out [T, H] of out_dtype (NVFP4_DT_F32 or NVFP4_DT_BF16).
+ * Constraints: H % 4 == 0.
+ * ------------------------------------------------------------------------ */
+int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, int k, int H, int out_dtype,
+                void* out, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_layer_forward -- the whole layer in one call: every step above,
+ * enqueued in order on `stream` with no host synchronisation, so the call
+ * can be captured in a CUDA graph.
+ *   mode        MOE_W4A4 or MOE_W4A16
+ *   x           bf16 [T, H]; logits fp32 [T, E]
+ *   w13_*       gate_up weights: codes [E, 2I, H/2], packed scales, S [E]
+ *   w2_*        down weights:    codes [E, H, I/2],  packed scales, S [E]
+ *   S_h         device fp32 scalar, static decode scale of h (W4A4 only)
+ *   out         fp32 [T, H]
+ *   workspace   >= moe_layer_workspace_bytes(mode, T, H, I, E, k); holds
+ *               every intermediate (routing, activations, G, h, Y)
+ * Constraints: H % 256 == 0, I % 256 == 0 (2I and H % 128 follow).
+ * ------------------------------------------------------------------------ */
+size_t moe_layer_workspace_bytes(int mode, int T, int H, int I, int E, int k);
+int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H, int I, int E, int k,
+                      const uint8_t* w13_codes, const uint8_t* w13_scales_packed, const float* w13_S,
+                      const uint8_t* w2_codes, const uint8_t* w2_scales_packed, const float* w2_S,
+                      const float* S_h, float* out, int32_t* dev_status, void* workspace,
+                      size_t workspace_bytes, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,243 @@
+"""Thin Python binding of ``libnvfp4moe.so`` (the C ABI in include/nvfp4moe.h).
+
+Each function has the name of its C entry point, takes torch tensors that
+already live on the GPU, passes their data pointers and the current CUDA
+stream, and raises ``Nvfp4Error`` if the library returns a status other than
+NVFP4_OK.  Every computation runs in the library's kernels; this module only
+marshals arguments and allocates outputs with torch.  There is no fallback:
+if the library cannot be loaded, importing the functions raises.
+"""
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+
+NVFP4_OK = 0
+NVFP4_DT_BF16, NVFP4_DT_F32 = 0, 1
+NVFP4_SCALE_STATIC, NVFP4_SCALE_DYNAMIC = 0, 1
+MOE_W4A4, MOE_W4A16 = 0, 1
+MOE_ACT_NONE, MOE_ACT_NVFP4, MOE_ACT_BF16 = 0, 1, 2
+STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4_E_ALIGN", 4: "NVFP4_E_WORKSPACE",
+                5: "NVFP4_E_ARCH", 6: "NVFP4_E_CUDA", 7: "NVFP4_E_DEVICE_TIMEOUT", 8: "NVFP4_E_BAD_ROUTING"}
+
+# every symbol the header declares, in declaration order
+EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspace_bytes", "nvfp4_quantize",
+           "nvfp4_pack_weight_scales", "moe_align_permute_workspace_bytes", "moe_align_permute",
+           "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine", "moe_layer_workspace_bytes",
+           "moe_layer_forward")
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, STATUS_NAMES.get(status, status)))
+
+
+_lib = None
+
+_P, _I, _I64, _SZ = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load the library (building it in-tree first if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libnvfp4moe.so is not built (%s); run __graft_entry__.build()" % path)
+    L = C.CDLL(path)
+    L.nvfp4_status_string.restype = C.c_char_p
+    L.nvfp4_status_string.argtypes = [_I]
+    L.nvfp4_device_check.restype = _I
+    L.nvfp4_device_check.argtypes = []
+    L.nvfp4_quantize_workspace_bytes.restype = _SZ
+    L.nvfp4_quantize_workspace_bytes.argtypes = [_I64, _I64]
+    L.nvfp4_quantize.restype = _I
+    L.nvfp4_quantize.argtypes = [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _P, _SZ, _P]
+    L.nvfp4_pack_weight_scales.restype = _I
+    L.nvfp4_pack_weight_scales.argtypes = [_P, _I, _I, _I, _P, _P]
+    L.moe_align_permute_workspace_bytes.restype = _SZ
+    L.moe_align_permute_workspace_bytes.argtypes = [_I, _I, _I]
+    L.moe_align_permute.restype = _I
+    L.moe_align_permute.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
+    L.moe_grouped_gemm_nvfp4.restype = _I
+    L.moe_grouped_gemm_nvfp4.argtypes = [_I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]
+    L.moe_swiglu_requant.restype = _I
+    L.moe_swiglu_requant.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P]
+    L.moe_combine.restype = _I
+    L.moe_combine.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P]
+    L.moe_layer_workspace_bytes.restype = _SZ
+    L.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+    L.moe_layer_forward.restype = _I
+    L.moe_layer_forward.argtypes = [_I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(fn, status):
+    if status != NVFP4_OK:
+        raise Nvfp4Error(fn, status)
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+# ---------------------------------------------------------------------------
+# entry points (names as in the C ABI)
+# ---------------------------------------------------------------------------
+
+def nvfp4_device_check():
+    _check("nvfp4_device_check", load().nvfp4_device_check())
+
+
+def nvfp4_quantize(x, S=None, codes=None, scales=None, workspace=None):
+    """Quantise x [rows, cols] (bf16 or fp32, CUDA) to NVFP4.  S=None ->
+    dynamic scale (returned as a 1-element fp32 tensor); otherwise S is a
+    1-element fp32 CUDA tensor read as the static decode scale."""
+    L = load()
+    rows, cols = x.shape
+    dev = x.device
+    dt = NVFP4_DT_BF16 if x.dtype == torch.bfloat16 else NVFP4_DT_F32
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be bf16 or fp32")
+    dynamic = S is None
+    if dynamic:
+        S = torch.zeros(4, dtype=torch.float32, device=dev)
+    if codes is None:
+        codes = _empty((rows, cols // 2), torch.uint8, dev)
+    if scales is None:
+        scales = _empty((rows, cols // 16), torch.uint8, dev)
+    if dynamic and workspace is None:
+        workspace = _empty(int(L.nvfp4_quantize_workspace_bytes(rows, cols)), torch.uint8, dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("nvfp4_quantize", L.nvfp4_quantize(_ptr(x), dt, rows, cols, x.stride(0), _ptr(S),
+                                              NVFP4_SCALE_DYNAMIC if dynamic else NVFP4_SCALE_STATIC, _ptr(codes),
+                                              _ptr(scales), _ptr(workspace), ws_bytes, _stream()))
+    return codes, scales, S[:1]
+
+
+def nvfp4_pack_weight_scales(scales_linear, E, N, K, out=None):
+    L = load()
+    if out is None:
+        out = _empty(E * N * (K // 16), torch.uint8, scales_linear.device)
+    _check("nvfp4_pack_weight_scales",
+           L.nvfp4_pack_weight_scales(_ptr(scales_linear), E, N, K, _ptr(out), _stream()))
+    return out
+
+
+def moe_align_permute(logits, k, act=None, act_kind=MOE_ACT_NONE, dev_status=None):
+    """Route + permute.  act: None, (codes, scales) for NVFP4 rows, or a bf16
+    [T, H] tensor.  Returns dict(ids, w, offsets, perm, inv[, act_codes,
+    act_scales | act_bf16])."""
+    L = load()
+    T, E = logits.shape
+    dev = logits.device
+    R = T * k
+    ids = _empty((T, k), torch.int32, dev)
+    w = _empty((T, k), torch.float32, dev)
+    offsets = _empty((E + 1,), torch.int32, dev)
+    perm = _empty((max(R, 1),), torch.int32, dev)
+    inv = _empty((max(R, 1),), torch.int32, dev)
+    ws = _empty(max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256), torch.uint8, dev)
+    out = dict(ids=ids, w=w, offsets=offsets, perm=perm[:R], inv=inv[:R])
+    a_in = a_in_sc = a_out = a_out_sc = None
+    cols = 0
+    if act_kind == MOE_ACT_NVFP4:
+        a_in, a_in_sc = act
+        cols = a_in.shape[1] * 2
+        a_out = _empty((max(R, 1), cols // 2), torch.uint8, dev)
+        a_out_sc = _empty((max(R, 1), cols // 16), torch.uint8, dev)
+        out["act_codes"], out["act_scales"] = a_out[:R], a_out_sc[:R]
+    elif act_kind == MOE_ACT_BF16:
+        a_in = act
+        cols = a_in.shape[1]
+        a_out = _empty((max(R, 1), cols), torch.bfloat16, dev)
+        out["act_bf16"] = a_out[:R]
+    _check("moe_align_permute",
+           L.moe_align_permute(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _ptr(offsets), _ptr(perm), _ptr(inv),
+                               act_kind, _ptr(a_in), _ptr(a_in_sc), cols, _ptr(a_out), _ptr(a_out_sc),
+                               _ptr(dev_status), _ptr(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_grouped_gemm_nvfp4(mode, a, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, N, K, out=None,
+                           dev_status=None):
+    L = load()
+    E = w_S.shape[0]
+    R = a.shape[0]
+    if out is None:
+        out = _empty((max(R, 1), N), torch.float32, a.device)[:R]
+    _check("moe_grouped_gemm_nvfp4",
+           L.moe_grouped_gemm_nvfp4(mode, _ptr(a), _ptr(a_scales), _ptr(a_S), _ptr(w_codes), _ptr(w_scales_packed),
+                                    _ptr(w_S), _ptr(offsets), E, N, K, R, _ptr(out), _ptr(dev_status), _stream()))
+    return out
+
+
+def moe_swiglu_requant(G, mode, S_h=None):
+    L = load()
+    R, I2 = G.shape
+    I = I2 // 2
+    dev = G.device
+    if mode == MOE_W4A4:
+        hc = _empty((max(R, 1), I // 2), torch.uint8, dev)
+        hs = _empty((max(R, 1), I // 16), torch.uint8, dev)
+        _check("moe_swiglu_requant",
+               L.moe_swiglu_requant(_ptr(G), R, I, mode, _ptr(S_h), _ptr(hc), _ptr(hs), None, _stream()))
+        return hc[:R], hs[:R]
+    hb = _empty((max(R, 1), I), torch.bfloat16, dev)
+    _check("moe_swiglu_requant", L.moe_swiglu_requant(_ptr(G), R, I, mode, None, None, None, _ptr(hb), _stream()))
+    return hb[:R]
+
+
+def moe_combine(Y, inv, topk_w, out_dtype=torch.float32):
+    L = load()
+    T, k = topk_w.shape
+    H = Y.shape[1]
+    out = _empty((T, H), out_dtype, Y.device)
+    dt = NVFP4_DT_F32 if out_dtype == torch.float32 else NVFP4_DT_BF16
+    _check("moe_combine", L.moe_combine(_ptr(Y), _ptr(inv), _ptr(topk_w), T, k, H, dt, _ptr(out), _stream()))
+    return out
+
+
+def moe_layer_workspace_bytes(mode, T, H, I, E, k):
+    return int(load().moe_layer_workspace_bytes(mode, T, H, I, E, k))
+
+
+def moe_layer_forward(mode, x, logits, k, w13, w2, S_h, out=None, workspace=None, dev_status=None):
+    """Whole layer.  w13 / w2: (codes, packed scales, S[E]) on the GPU."""
+    L = load()
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2[0].shape[2] * 2
+    dev = x.device
+    if out is None:
+        out = _empty((T, H), torch.float32, dev)
+    if workspace is None:
+        workspace = _empty(moe_layer_workspace_bytes(mode, T, H, I, E, k), torch.uint8, dev)
+    _check("moe_layer_forward",
+           L.moe_layer_forward(mode, _ptr(x), _ptr(logits), T, H, I, E, k, _ptr(w13[0]), _ptr(w13[1]), _ptr(w13[2]),
+                               _ptr(w2[0]), _ptr(w2[1]), _ptr(w2[2]), _ptr(S_h), _ptr(out), _ptr(dev_status),
+                               _ptr(workspace), workspace.numel(), _stream()))
+    return out

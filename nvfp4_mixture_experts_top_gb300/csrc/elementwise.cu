@@ -1,0 +1,256 @@
+// elementwise.cu -- HBM-bound kernels of the NVFP4 MoE path: quantiser
+// (with the warp-shuffle tensor amax), weight-scale packing, SwiGLU +
+// requantisation, and the weighted combine.
+//
+// All of them are one-pass streaming kernels: coalesced 16-byte loads and
+// stores, grids sized in multiples of the SM count, no shared-memory staging
+// (nothing is reused).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4moe {
+
+// ---------------------------------------------------------------------------
+// tensor amax (dynamic per-tensor scale)
+// ---------------------------------------------------------------------------
+
+// Eight consecutive inputs widened to fp32 (16- or 32-byte aligned load).
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* v);
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float* v) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float* v) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// amax over [rows, cols] (cols % 8 == 0) -> atomicMax on the bit pattern
+// (|x| >= 0, so unsigned order equals float order).
+template <typename T>
+__global__ void __launch_bounds__(256) amax_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+                                                   int64_t ld, uint32_t* __restrict__ amax_bits) {
+  const int64_t vec_per_row = cols / 8;
+  const int64_t nvec = rows * vec_per_row;
+  float m = 0.0f;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / vec_per_row, c = (i % vec_per_row) * 8;
+    float v[8];
+    load8<T>(x + r * ld + c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ float wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) b = fmaxf(b, wmax[w]);
+    atomicMax(amax_bits, __float_as_uint(b));
+  }
+}
+
+// One thread per 16-element block.  dynamic: S = amax / 2688 from the amax
+// word; static: S read from *S.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+                                                       int64_t ld, float* __restrict__ S, int dynamic,
+                                                       const uint32_t* __restrict__ amax_bits,
+                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  float s;
+  if (dynamic) {
+    s = __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *S = s;
+  } else {
+    s = *S;
+  }
+  const int64_t nb_row = cols / 16;
+  const int64_t nblk = rows * nb_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb_row, b = i % nb_row;
+    float v[16];
+    load8<T>(x + r * ld + b * 16, v);
+    load8<T>(x + r * ld + b * 16 + 8, v + 8);
+    uint32_t w0, w1;
+    const uint32_t sc = quantize_block16(v, s, w0, w1);
+    *reinterpret_cast<uint2*>(codes + r * (cols / 2) + b * 8) = make_uint2(w0, w1);
+    scales[r * nb_row + b] = (uint8_t)sc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// weight-scale packing: linear [E, N, K/16] -> 512-byte atoms
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restrict__ in, int64_t E, int64_t N,
+                                                          int64_t K, uint8_t* __restrict__ out) {
+  const int64_t kb_n = K / 64;                  // 4-scale words per row
+  const int64_t total = E * N * kb_n;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / kb_n, kb = i % kb_n;   // row = e*N + n
+    const int64_t e = row / N, n = row % N;
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(in + row * (K / 16) + kb * 4);
+    const int64_t nt = n / 128, r = n % 128;
+    const int64_t atom = (e * (N / 128) + nt) * kb_n + kb;
+    *reinterpret_cast<uint32_t*>(out + atom * 512 + (r % 32) * 16 + (r / 32) * 4) = word;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU + requantisation (one thread per 16-element block of h)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __restrict__ G, int64_t R, int64_t I,
+                                                             int mode, const float* __restrict__ S_h,
+                                                             uint8_t* __restrict__ h_codes,
+                                                             uint8_t* __restrict__ h_scales,
+                                                             __nv_bfloat16* __restrict__ h_bf16) {
+  const int64_t nb_row = I / 16;
+  const int64_t nblk = R * nb_row;
+  const float s = (mode == MOE_W4A4) ? *S_h : 0.0f;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb_row, b = i % nb_row;
+    const float4* gp = reinterpret_cast<const float4*>(G + r * 2 * I + b * 16);
+    const float4* up = reinterpret_cast<const float4*>(G + r * 2 * I + I + b * 16);
+    float h[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 g = __ldg(gp + q), u = __ldg(up + q);
+      h[4 * q + 0] = silu_mul(g.x, u.x);
+      h[4 * q + 1] = silu_mul(g.y, u.y);
+      h[4 * q + 2] = silu_mul(g.z, u.z);
+      h[4 * q + 3] = silu_mul(g.w, u.w);
+    }
+    if (mode == MOE_W4A4) {
+      uint32_t w0, w1;
+      const uint32_t sc = quantize_block16(h, s, w0, w1);
+      *reinterpret_cast<uint2*>(h_codes + r * (I / 2) + b * 8) = make_uint2(w0, w1);
+      h_scales[r * nb_row + b] = (uint8_t)sc;
+    } else {
+      uint32_t w[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(h[2 * q], h[2 * q + 1]);
+        w[q] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(h_bf16 + r * I + b * 16);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine: out[t, n] = sum_j w[t, j] * Y[inv[t*k + j], n]  (gather, fp32)
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ Y, const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int T, int k, int64_t H,
+                                                      int out_dtype, void* __restrict__ out) {
+  const int64_t q_per_row = H / 4;
+  const int64_t total = (int64_t)T * q_per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / q_per_row, c = (i % q_per_row) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float wj = __ldg(w + t * k + j);
+      const int64_t r = __ldg(inv + t * k + j);
+      const float4 y = __ldg(reinterpret_cast<const float4*>(Y + r * H + c));
+      acc.x = __fadd_rn(acc.x, __fmul_rn(wj, y.x));
+      acc.y = __fadd_rn(acc.y, __fmul_rn(wj, y.y));
+      acc.z = __fadd_rn(acc.z, __fmul_rn(wj, y.z));
+      acc.w = __fadd_rn(acc.w, __fmul_rn(wj, y.w));
+    }
+    if (out_dtype == NVFP4_DT_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c) = acc;
+    } else {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&a);
+      v.y = *reinterpret_cast<const uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + t * H + c) = v;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+static int grid_for(int64_t work_items, int threads) {
+  const int64_t blocks = (work_items + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms() * 8;   // a few waves of resident CTAs
+  return (int)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+}
+
+cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,
+                            int dynamic, uint32_t* amax_ws, uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+  if (rows == 0) {
+    if (dynamic) return cudaMemsetAsync(S, 0, sizeof(float), st);
+    return cudaSuccess;
+  }
+  if (dynamic) {
+    cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    const int g = grid_for(rows * cols / 8, 256);
+    if (x_dtype == NVFP4_DT_BF16)
+      amax_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, amax_ws);
+    else
+      amax_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, amax_ws);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int g = grid_for(rows * cols / 16, 256);
+  if (x_dtype == NVFP4_DT_BF16)
+    quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, S,
+                                                      dynamic, amax_ws, codes, scales);
+  else
+    quantize_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, S, dynamic, amax_ws,
+                                              codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st) {
+  const int64_t total = (int64_t)E * N * (K / 64);
+  if (total == 0) return cudaSuccess;
+  pack_scales_kernel<<<grid_for(total, 256), 256, 0, st>>>(in, E, N, K, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
+                                  uint8_t* h_scales, void* h_bf16, cudaStream_t st) {
+  const int64_t nblk = (int64_t)R * (I / 16);
+  if (nblk == 0) return cudaSuccess;
+  swiglu_requant_kernel<<<grid_for(nblk, 256), 256, 0, st>>>(G, R, I, mode, S_h, h_codes, h_scales,
+                                                             static_cast<__nv_bfloat16*>(h_bf16));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H, int out_dtype,
+                           void* out, cudaStream_t st) {
+  const int64_t total = (int64_t)T * (H / 4);
+  if (total == 0) return cudaSuccess;
+  combine_kernel<<<grid_for(total, 256), 256, 0, st>>>(Y, inv, w, T, k, H, out_dtype, out);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4moe

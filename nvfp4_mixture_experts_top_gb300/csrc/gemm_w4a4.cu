@@ -1,0 +1,352 @@
+// gemm_w4a4.cu -- ragged grouped NVFP4 x NVFP4 GEMM over experts on the
+// 5th-generation tensor cores (tcgen05, kind::mxf4nvf4, block scale 16, UE4M3).
+//
+// Decode shapes: every expert sees 0..~64 tokens but streams a full weight
+// matrix, so the kernel is built to stream weights at HBM speed:
+//  * swap-AB: the weight tile (128 output rows x K) is the MMA's M=128 side
+//    and the expert's tokens are its N side, in groups of 32 (N=32 per MMA,
+//    up to 4 groups = 128 tokens per pass sharing one weight tile).
+//  * persistent CTAs (one per SM) walk the (expert, 128-row tile) work units
+//    in a static round-robin; empty experts cost one offsets read.
+//  * warp-specialised: warp 0 issues TMA (weights with an evict-first L2
+//    policy, activations evict-last since every tile of the expert re-reads
+//    them), warp 1 issues tcgen05.cp (block scales -> TMEM) and tcgen05.mma,
+//    warps 2-5 drain the fp32 accumulators from TMEM (tcgen05.ld) and store.
+//  * a 5-stage shared-memory ring (36 KB per stage) and two TMEM accumulator
+//    buffers, so loads, MMAs and the epilogue of the previous unit overlap.
+//  * every mbarrier wait is bounded; a timeout sets NVFP4_E_DEVICE_TIMEOUT,
+//    drains in-flight copies and MMAs, frees TMEM and returns.
+//
+// Operand layouts in shared memory (all K-major, 128-byte rows):
+//   weight codes   [128 rows][128 B]  TMA, 128-byte swizzle
+//   token codes    [32 rows][128 B]   per group, TMA, 128-byte swizzle
+//   weight scales  4 x 512-byte atoms (pre-packed, one bulk copy)
+//   token scales   [32 rows][16 B]    per group, TMA, no swizzle
+// Block scales in TMEM: a 32-lane x 4-column patch per 128 rows (row r in lane
+// r % 32 of every lane quarter, column r / 32, byte = 16-element block within
+// the MMA's K=64).  A group's raw [32][16 B] scale tile copied as-is puts the
+// scales of MMA step kk in column kk, which is the layout for N <= 32.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tmap.h"
+
+namespace nvfp4moe {
+namespace w4a4 {
+
+constexpr int BM = 128;     // weight rows per tile
+constexpr int KC = 256;     // K elements per stage (= one 128-byte swizzle row)
+constexpr int TG = 32;      // tokens per MMA
+constexpr int MAXG = 4;     // token groups per pass
+constexpr int STAGES = 5;
+constexpr int TOK_PER_PASS = TG * MAXG;
+
+constexpr uint32_t W_BYTES = BM * KC / 2;    // 16384
+constexpr uint32_t A_BYTES = TG * KC / 2;    // 4096
+constexpr uint32_t WS_BYTES = BM * KC / 16;  // 2048
+constexpr uint32_t AS_BYTES = TG * KC / 16;  // 512
+constexpr uint32_t OFF_A = W_BYTES;                        // 16384
+constexpr uint32_t OFF_WS = OFF_A + MAXG * A_BYTES;         // 32768
+constexpr uint32_t OFF_AS = OFF_WS + WS_BYTES;              // 34816
+constexpr uint32_t STAGE_BYTES = OFF_AS + MAXG * AS_BYTES;  // 36864
+static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+
+// TMEM columns: two accumulators of 128 fp32 columns, then per stage 16
+// columns of weight scales (4 per MMA step) and 16 of token scales (4 per
+// group).
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = TOK_PER_PASS;  // 128
+constexpr uint32_t SF_BASE = 2 * ACC_COLS;   // 256
+constexpr uint32_t SF_STAGE = 32;
+static_assert(SF_BASE + STAGES * SF_STAGE <= TMEM_COLS, "TMEM budget");
+
+constexpr int NUM_THREADS = 192;  // warp0 TMA, warp1 MMA, warps2-5 epilogue
+
+struct Params {
+  const uint8_t* w_scales;  // packed atoms
+  const float* w_S;
+  const float* a_S;
+  const int32_t* offsets;
+  float* out;
+  int32_t* dev_status;
+  int E, N, K, R;
+};
+
+// Rows [m0, m1) of expert e, or an empty range if the offsets are invalid.
+__device__ __forceinline__ void expert_rows(const Params& p, int e, int& m0, int& m1) {
+  m0 = __ldg(p.offsets + e);
+  m1 = __ldg(p.offsets + e + 1);
+  if (m0 < 0 || m1 < m0 || m1 > p.R) m0 = m1 = 0;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      report_status(dev_status, NVFP4_E_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
+                     const __grid_constant__ CUtensorMap tm_as, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NT = p.N / BM;
+  const int KCH = p.K / KC;
+  const int units = p.E * NT;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4 * 32);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_as);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (__ldg(p.offsets + p.E) != p.R || __ldg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int e = u / NT, nt = u % NT;
+        int m0, m1;
+        expert_rows(p, e, m0, m1);
+        for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+          const int ntok = min(TOK_PER_PASS, m1 - r0);
+          const int ng = (ntok + TG - 1) / TG;
+          const uint32_t bytes = W_BYTES + WS_BYTES + ng * (A_BYTES + AS_BYTES);
+          const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
+          for (int kc = 0; kc < KCH; ++kc) {
+            if (!wait_or_abort(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sb = smem + stage * STAGE_BYTES;
+            mbar_arrive_expect_tx(&full_bar[stage], bytes);
+            tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
+            bulk_load(sb + OFF_WS, wsc + (size_t)kc * 4 * 512, WS_BYTES, &full_bar[stage], pol_w);
+            for (int g = 0; g < ng; ++g) {
+              tma_load_2d(sb + OFF_A + g * A_BYTES, &tm_a, &full_bar[stage], kc * (KC / 2), r0 + g * TG, pol_a);
+              tma_load_2d(sb + OFF_AS + g * AS_BYTES, &tm_as, &full_bar[stage], kc * (KC / 16), r0 + g * TG, pol_a);
+            }
+            issued_mask |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // copies already issued must land before the CTA's shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued_mask >> s) & 1u) mbar_wait(&full_bar[s], (issued_par >> s) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_mxf4nvf4(BM, TG);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t smem_base = smem_u32(smem);
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int e = u / NT;
+        int m0, m1;
+        expert_rows(p, e, m0, m1);
+        for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+          const int ntok = min(TOK_PER_PASS, m1 - r0);
+          const int ng = (ntok + TG - 1) / TG;
+          if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_col = tmem + acc * ACC_COLS;
+          for (int kc = 0; kc < KCH; ++kc) {
+            if (!wait_or_abort(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sb = smem_base + stage * STAGE_BYTES;
+            const uint32_t sfa = tmem + SF_BASE + stage * SF_STAGE;
+            const uint32_t sfb = sfa + 16;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
+            for (int g = 0; g < ng; ++g) tc_cp_32x128b_x4(sfb + 4 * g, desc_sf(sb + OFF_AS + g * AS_BYTES));
+            const uint64_t adesc = desc_sw128(sb);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              for (int g = 0; g < ng; ++g) {
+                const uint64_t bdesc = desc_sw128(sb + OFF_A + g * A_BYTES);
+                // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
+                mma_mxf4nvf4(d_col + g * TG, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * g + kk,
+                             (kc | kk) != 0);
+              }
+            }
+            tc_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          tc_commit(&acc_full[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
+          }
+        }
+      }
+      // every MMA issued by this thread has finished once drain_bar flips
+      tc_commit(&drain_bar);
+      mbar_wait(&drain_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int e = u / NT, nt = u % NT;
+      int m0, m1;
+      expert_rows(p, e, m0, m1);
+      const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + e));
+      const int n = nt * BM + q * 32 + lane;
+      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+        const int ntok = min(TOK_PER_PASS, m1 - r0);
+        const int ng = (ntok + TG - 1) / TG;
+        // lane 0 waits, the warp follows its verdict (tcgen05.ld is warp-collective)
+        int got = 1;
+        if (lane == 0) got = wait_or_abort(&acc_full[acc], acc_phase, &abort_flag, p.dev_status) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int g = 0; g < ng; ++g) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS + g * TG, r);
+          tmem_ld_wait();
+          const int tb = r0 + g * TG;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (tb + j < m1) p.out[(size_t)(tb + j) * p.N + n] = __fmul_rn(__uint_as_float(r[j]), alpha);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace w4a4
+
+cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
+                             const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                             const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
+                             cudaStream_t st) {
+  using namespace w4a4;
+  if (R == 0 || E == 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tm_w, tm_a, tm_as;
+  cudaError_t err;
+  // weight codes: [E*N rows, K/2 bytes], box 128 B x 128 rows, 128-byte swizzle
+  err = make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, true);
+  if (err != cudaSuccess) return err;
+  // token codes: [R rows, K/2 bytes], box 128 B x 32 rows, 128-byte swizzle
+  err = make_tmap_2d_u8(&tm_a, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TG, true);
+  if (err != cudaSuccess) return err;
+  // token scales: [R rows, K/16 bytes], box 16 B x 32 rows, no swizzle
+  err = make_tmap_2d_u8(&tm_as, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TG, false);
+  if (err != cudaSuccess) return err;
+  Params p;
+  p.w_scales = w_scales_packed;
+  p.w_S = w_S;
+  p.a_S = a_S;
+  p.offsets = offsets;
+  p.out = out;
+  p.dev_status = dev_status;
+  p.E = E;
+  p.N = N;
+  p.K = K;
+  p.R = R;
+  const int units = E * (N / BM);
+  const int grid = units < num_sms() ? units : num_sms();
+  gemm_w4a4_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, p);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4moe

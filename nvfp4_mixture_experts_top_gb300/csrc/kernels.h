@@ -1,0 +1,37 @@
+// kernels.h -- launchers of the NVFP4 MoE kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4moe {
+
+int num_sms();  // SM count of the current device (cached)
+
+cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,
+                            int dynamic, uint32_t* amax_ws, uint8_t* codes, uint8_t* scales, cudaStream_t st);
+cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st);
+cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
+                                  uint8_t* h_scales, void* h_bf16, cudaStream_t st);
+cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H,
+                           int out_dtype, void* out, cudaStream_t st);
+
+// Routing: top-k + stable counting sort + optional gather.  ws must hold
+// route_workspace_bytes(T, E).
+size_t route_workspace_bytes(int T, int E);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                         int32_t* offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
+                         const uint8_t* act_in_scales, int64_t act_cols, void* act_out, uint8_t* act_out_scales,
+                         int32_t* dev_status, void* ws, cudaStream_t st);
+
+// Grouped GEMMs.  Return cudaSuccess or the launch/setup error; host-side
+// argument checks happen before these are called.
+cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
+                             const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                             const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
+                             cudaStream_t st);
+cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const uint8_t* w_scales_packed,
+                              const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
+                              int32_t* dev_status, cudaStream_t st);
+
+}  // namespace nvfp4moe

@@ -1,0 +1,61 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function
+that include/nvfp4moe.h declares (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+from conftest import ROOT
+
+
+def _declared():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([a-z][a-z0-9_]+)\s*\(", text, re.M)
+    return names
+
+
+def test_header_declares_the_path():
+    names = set(_declared())
+    for n in ("nvfp4_quantize", "moe_align_permute", "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from nvfp4_mixture_experts_top_gb300 import binding, build
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(binding.EXPORTS) == set(_declared())
+
+
+def test_status_strings_without_gpu():
+    from nvfp4_mixture_experts_top_gb300 import binding
+    L = binding.load()
+    for s in range(9):
+        assert L.nvfp4_status_string(s).startswith(b"NVFP4_")
+    assert L.moe_layer_workspace_bytes(0, 16, 4096, 2048, 256, 8) > 16 * 8 * 2 * 2048 * 4
+
+
+def test_host_validation_without_gpu():
+    """Argument errors are caught on the host, before any device call."""
+    from nvfp4_mixture_experts_top_gb300 import binding
+    L = binding.load()
+    # cols not a multiple of 16 -> E_SHAPE; null scale pointer -> E_INVAL
+    assert L.nvfp4_quantize(None, 0, 4, 24, 24, ctypes.c_void_p(16), 0, None, None, None, 0, None) == 2
+    assert L.nvfp4_quantize(None, 0, 4, 32, 32, None, 0, None, None, None, 0, None) == 1
+    # misaligned pointer -> E_ALIGN
+    assert L.nvfp4_quantize(ctypes.c_void_p(8), 0, 4, 32, 32, ctypes.c_void_p(16), 0, ctypes.c_void_p(16),
+                            ctypes.c_void_p(16), None, 0, None) == 3
+    # grouped GEMM with N % 128 != 0 -> E_SHAPE; bad mode -> E_INVAL
+    assert L.moe_grouped_gemm_nvfp4(0, None, None, None, None, None, None, None, 4, 100, 256, 8, None, None,
+                                    None) == 2
+    assert L.moe_grouped_gemm_nvfp4(7, None, None, None, None, None, None, None, 4, 128, 256, 8, None, None,
+                                    None) == 1
+    # routing with k > 32 -> E_SHAPE
+    assert L.moe_align_permute(None, 4, 64, 33, None, None, ctypes.c_void_p(16), None, None, 0, None, None, 0,
+                               None, None, None, None, 0, None) == 2

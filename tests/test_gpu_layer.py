@@ -1,0 +1,167 @@
+"""Full MoE layer on the GPU against the oracle.
+
+* tiny workload: every intermediate and the output, all tokens.
+* decode workloads at full size, in the launch configuration the benchmark
+  times (moe_layer_forward): sampled tokens, computed by the oracle one by
+  one from the same fp32 weights (regenerated from their seeds) and the
+  whole batch's activation scale.
+
+Where a requantised intermediate code of h differs between the two sides,
+the oracle's own fp32 h must lie within 1e-4 (relative) of that code's
+rounding midpoint: the GPU accumulates G in fp32 on the tensor cores and the
+oracle in fp64, so h may differ in its last bits and a value that close to a
+midpoint may round either way.  Tokens whose h rows hold such a flip are
+held to the relative-Frobenius bound only; every other token meets both
+bounds."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_close, cuda_or_skip, errors, nvfp4_ambiguous, to_dev, unpack_codes, upload_weights
+from nvfp4_mixture_experts_top_gb300 import binding as B
+from nvfp4_mixture_experts_top_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_weights(orc, cfg, experts, seed=0):
+    w13 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed).numpy()
+                                         for e in experts]))
+    w2 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed).numpy()
+                                        for e in experts]))
+    return w13, w2
+
+
+def gpu_weights(cfg, dev, seed=0):
+    """Quantise every expert on the GPU (product quantiser), pack scales."""
+    out = []
+    for which, N, K in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
+        codes = torch.empty(cfg.E, N, K // 2, dtype=torch.uint8, device=dev)
+        scales = torch.empty(cfg.E, N, K // 16, dtype=torch.uint8, device=dev)
+        S = torch.empty(cfg.E, dtype=torch.float32, device=dev)
+        for e in range(cfg.E):
+            wf = wl.expert_weight_fp32(which, e, N, K, seed, device=dev)
+            _, _, s = B.nvfp4_quantize(wf, codes=codes[e], scales=scales[e])
+            S[e:e + 1].copy_(s)
+        packed = B.nvfp4_pack_weight_scales(scales, cfg.E, N, K)
+        out.append(((codes, packed, S), scales))
+    return out
+
+
+def staged(mode, x, logits, cfg, w13, w2, S_h):
+    """The layer through the individual entry points (exposes intermediates)."""
+    k, I, H = cfg.k, cfg.I, cfg.H
+    R = cfg.R
+    d = {}
+    if mode == B.MOE_W4A4:
+        xc, xs, S_x = B.nvfp4_quantize(x)
+        rt = B.moe_align_permute(logits, k, act=(xc, xs), act_kind=B.MOE_ACT_NVFP4)
+        G = B.moe_grouped_gemm_nvfp4(mode, rt["act_codes"], rt["act_scales"], S_x, *w13, rt["offsets"], 2 * I, H)
+        hc, hs = B.moe_swiglu_requant(G, mode, S_h)
+        Y = B.moe_grouped_gemm_nvfp4(mode, hc, hs, S_h, *w2, rt["offsets"], H, I)
+        d.update(S_x=S_x, hc=hc, hs=hs)
+    else:
+        rt = B.moe_align_permute(logits, k, act=x, act_kind=B.MOE_ACT_BF16)
+        G = B.moe_grouped_gemm_nvfp4(mode, rt["act_bf16"], None, None, *w13, rt["offsets"], 2 * I, H)
+        hb = B.moe_swiglu_requant(G, mode)
+        Y = B.moe_grouped_gemm_nvfp4(mode, hb, None, None, *w2, rt["offsets"], H, I)
+        d.update(hb=hb)
+    out = B.moe_combine(Y, rt["inv"], rt["w"])
+    d.update(rt=rt, G=G, Y=Y, out=out)
+    return d
+
+
+MODES = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16}
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+def test_layer_tiny_all_intermediates(orc, mode):
+    dev = cuda_or_skip()
+    cfg = wl.CONFIGS["tiny"]
+    m = MODES[mode]
+    xt = wl.activations_bf16(cfg.T, cfg.H)
+    logits = wl.router_logits(cfg)
+    w13, w2 = _oracle_weights(orc, cfg, range(cfg.E))
+    ref, mids = orc.moe_layer(mode, xt.float().numpy(), logits.numpy(), cfg.k, w13, w2, cfg.S_h, intermediates=True)
+    g13 = upload_weights(w13, cfg.E, 2 * cfg.I, cfg.H, dev)
+    g2 = upload_weights(w2, cfg.E, cfg.H, cfg.I, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    x, lg = xt.to(dev), logits.to(dev)
+    d = staged(m, x, lg, cfg, g13, g2, S_h)
+    fused = B.moe_layer_forward(m, x, lg, cfg.k, g13, g2, S_h)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, d["out"])
+    assert np.array_equal(d["rt"]["ids"].cpu().numpy(), mids["ids"])
+    assert np.array_equal(d["rt"]["offsets"].cpu().numpy(), mids["offsets"])
+    assert np.array_equal(d["rt"]["perm"].cpu().numpy(), mids["perm"])
+    assert np.array_equal(d["rt"]["inv"].cpu().numpy(), mids["inv"])
+    if mode == "w4a4":
+        assert float(d["S_x"].item()) == float(mids["S_x"])
+        amb = nvfp4_ambiguous(mids["h32"], cfg.S_h, rel=1e-4)
+        flips = unpack_codes(d["hc"].cpu().numpy()) != unpack_codes(mids["hq_codes"])
+        assert not (flips & ~amb).any()
+    assert_close(d["out"].cpu().numpy(), ref, "tiny " + mode)
+
+
+def _sampled_check(orc, cfg, mode, tokens, dev):
+    m = MODES[mode]
+    x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
+    logits = wl.router_logits(cfg, device=dev)
+    (g13, s13), (g2, s2) = gpu_weights(cfg, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    d = staged(m, x, logits, cfg, g13, g2, S_h)
+    fused = B.moe_layer_forward(m, x, logits, cfg.k, g13, g2, S_h)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, d["out"]), "moe_layer_forward differs from the staged calls"
+    # oracle on the sampled tokens, with only the experts they use
+    x_np = x.float().cpu().numpy()
+    lg_np = logits.cpu().numpy()
+    ids, _ = orc.route(lg_np[tokens], cfg.k)
+    used = np.unique(ids)
+    w13, w2 = _oracle_weights(orc, cfg, used)
+    # the GPU quantised the same weights: identical codes and scales
+    for i, e in enumerate(used):
+        assert np.array_equal(g13[0][e].cpu().numpy(), w13[0][i]) and np.array_equal(s13[e].cpu().numpy(), w13[1][i])
+        assert np.array_equal(g2[0][e].cpu().numpy(), w2[0][i]) and np.array_equal(s2[e].cpu().numpy(), w2[1][i])
+    S_x = orc.tensor_scale(x_np) if mode == "w4a4" else None
+    if mode == "w4a4":
+        assert float(d["S_x"].item()) == float(S_x)
+    ref, mids = orc.moe_layer(mode, x_np[tokens], lg_np[tokens][:, used], cfg.k, w13, w2, cfg.S_h,
+                              intermediates=True, S_x=S_x)
+    got = d["out"].cpu().numpy()[tokens]
+    flipped_tok = np.zeros(len(tokens), bool)
+    if mode == "w4a4":
+        inv_g = d["rt"]["inv"].cpu().numpy().reshape(cfg.T, cfg.k)
+        hc_g = unpack_codes(d["hc"].cpu().numpy())
+        hc_o = unpack_codes(mids["hq_codes"])
+        amb = nvfp4_ambiguous(mids["h32"], cfg.S_h, rel=1e-4)
+        inv_o = mids["inv"].reshape(len(tokens), cfg.k)
+        for i, t in enumerate(tokens):
+            for j in range(cfg.k):
+                rg, ro = inv_g[t, j], inv_o[i, j]
+                diff = hc_g[rg] != hc_o[ro]
+                assert not (diff & ~amb[ro]).any(), "h code differs away from a rounding midpoint"
+                flipped_tok[i] |= diff.any()
+    rel, _ = errors(got, ref)
+    assert rel <= 1e-3, rel
+    for i in range(len(tokens)):
+        if not flipped_tok[i]:
+            assert_close(got[i], ref[i], "%s %s token %d" % (cfg.name, mode, tokens[i]))
+    return rel
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+def test_layer_decode_c16_full_size(orc, mode):
+    dev = cuda_or_skip()
+    _sampled_check(orc, wl.CONFIGS["decode_c16"], mode, [0, 9], dev)
+
+
+def test_layer_decode_b512_full_size(orc):
+    dev = cuda_or_skip()
+    _sampled_check(orc, wl.CONFIGS["decode_b512"], "w4a4", [0, 257, 511], dev)
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+def test_layer_wide_full_size(orc, mode):
+    dev = cuda_or_skip()
+    _sampled_check(orc, wl.CONFIGS["wide"], mode, [5], dev)
