@@ -218,11 +218,15 @@ def main():
     ap.add_argument("--baseline-tokens", type=int, default=4, help="tokens of the in-run CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (smaller device footprint for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     from nvfp4_mixture_experts_top_gb300 import workloads as wl
     cfg = wl.CONFIGS[args.workload]
+    if args.experts:
+        cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)
     metric = "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name)
     unit = "tokens/s"
     if args.impl == "reference":
@@ -359,10 +363,13 @@ def main():
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # profiler range = the timed region (ncu --profile-from-start off)
+    torch.cuda.profiler.start()
     t0.record()
     graph.replay()
     t1.record()
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     if world > 1:
         dist.barrier()
     if not args.no_clocks:

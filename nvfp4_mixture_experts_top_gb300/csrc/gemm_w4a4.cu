@@ -24,8 +24,9 @@
 //   token scales   [32 rows][16 B]    per group, TMA, no swizzle
 // Block scales in TMEM: a 32-lane x 4-column patch per 128 rows (row r in lane
 // r % 32 of every lane quarter, column r / 32, byte = 16-element block within
-// the MMA's K=64).  A group's raw [32][16 B] scale tile copied as-is puts the
-// scales of MMA step kk in column kk, which is the layout for N <= 32.
+// the MMA's K=64), starting on a 4-column boundary for every MMA.  One MMA per
+// K step covers all ng token groups (N = 32*ng); its token-scale patch is made
+// by an in-place shared-memory transpose of the TMA'd scale tiles.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -62,7 +63,7 @@ constexpr uint32_t SF_BASE = 2 * ACC_COLS;   // 256
 constexpr uint32_t SF_STAGE = 32;
 static_assert(SF_BASE + STAGES * SF_STAGE <= TMEM_COLS, "TMEM budget");
 
-constexpr int NUM_THREADS = 192;  // warp0 TMA, warp1 MMA, warps2-5 epilogue
+constexpr int NUM_THREADS = 192;  // warp0 TMA, warp1 MMA (+ scale repack), warps2-5 epilogue
 
 struct Params {
   const uint8_t* w_scales;  // packed atoms
@@ -194,64 +195,91 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mxf4nvf4(BM, TG);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      const uint32_t smem_base = smem_u32(smem);
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const int e = u / NT;
-        int m0, m1;
-        expert_rows(p, e, m0, m1);
-        for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-          const int ntok = min(TOK_PER_PASS, m1 - r0);
-          const int ng = (ntok + TG - 1) / TG;
-          if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
+    // The whole warp waits for a stage and repacks the token scales in place;
+    // lane 0 then issues the scale copies and the MMAs.
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const uint32_t smem_base = smem_u32(smem);
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int e = u / NT;
+      int m0, m1;
+      expert_rows(p, e, m0, m1);
+      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+        const int ntok = min(TOK_PER_PASS, m1 - r0);
+        const int ng = (ntok + TG - 1) / TG;
+        const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
+        int got = 1;
+        if (lane == 0) got = wait_or_abort(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_col = tmem + acc * ACC_COLS;
+        for (int kc = 0; kc < KCH; ++kc) {
+          got = 1;
+          if (lane == 0) got = wait_or_abort(&full_bar[stage], phase, &abort_flag, p.dev_status) ? 1 : 0;
+          if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t d_col = tmem + acc * ACC_COLS;
-          for (int kc = 0; kc < KCH; ++kc) {
-            if (!wait_or_abort(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
-              ok = false;
-              break;
-            }
+          // Token scales arrive as [group g][token i][16 B = K steps kk 0..3 x 4
+          // scales].  Every MMA's scale operand must start on a 4-column
+          // boundary, so rewrite them in place as [kk][token i][group g x 4 B]:
+          // copied with tcgen05.cp, row i of block kk puts the scales of token
+          // 32g + i for step kk in lane i, column g (the N = 32*ng layout).
+          uint8_t* as_tile = smem + stage * STAGE_BYTES + OFF_AS;
+          uint4 v[MAXG];
+#pragma unroll
+          for (int g = 0; g < MAXG; ++g) v[g] = *reinterpret_cast<const uint4*>(as_tile + g * AS_BYTES + lane * 16);
+          __syncwarp();
+          const uint32_t w[MAXG][4] = {{v[0].x, v[0].y, v[0].z, v[0].w}, {v[1].x, v[1].y, v[1].z, v[1].w},
+                                       {v[2].x, v[2].y, v[2].z, v[2].w}, {v[3].x, v[3].y, v[3].z, v[3].w}};
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            *reinterpret_cast<uint4*>(as_tile + kk * AS_BYTES + lane * 16) =
+                make_uint4(w[0][kk], w[1][kk], w[2][kk], w[3][kk]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
             tc_fence_after();
             const uint32_t sb = smem_base + stage * STAGE_BYTES;
             const uint32_t sfa = tmem + SF_BASE + stage * SF_STAGE;
             const uint32_t sfb = sfa + 16;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) tc_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
-            for (int g = 0; g < ng; ++g) tc_cp_32x128b_x4(sfb + 4 * g, desc_sf(sb + OFF_AS + g * AS_BYTES));
-            const uint64_t adesc = desc_sw128(sb);
-#pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              for (int g = 0; g < ng; ++g) {
-                const uint64_t bdesc = desc_sw128(sb + OFF_A + g * A_BYTES);
-                // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
-                mma_mxf4nvf4(d_col + g * TG, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * g + kk,
-                             (kc | kk) != 0);
-              }
+              tc_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
+              tc_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
             }
+            const uint64_t adesc = desc_sw128(sb);
+            const uint64_t bdesc = desc_sw128(sb + OFF_A);  // the ng group tiles are one [32*ng x 128 B] tile
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
+              mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
+                           (kc | kk) != 0);
             tc_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
           }
-          if (!ok) break;
-          tc_commit(&acc_full[acc]);
-          if (++acc == 2) {
-            acc = 0;
-            acc_phase ^= 1;
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
           }
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit(&acc_full[acc]);
+        __syncwarp();
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
-      // every MMA issued by this thread has finished once drain_bar flips
+    }
+    // every MMA issued by this warp has finished once drain_bar flips
+    if (lane == 0) {
       tc_commit(&drain_bar);
       mbar_wait(&drain_bar, 0);
     }

@@ -24,10 +24,12 @@ from nvfp4_mixture_experts_top_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-def _oracle_weights(orc, cfg, experts, seed=0):
-    w13 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed).numpy()
+def _oracle_weights(orc, cfg, experts, seed=0, device="cpu"):
+    """fp32 weights from their seeds (on `device`, the generator the GPU side
+    used), quantised by the oracle."""
+    w13 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed, device).cpu().numpy()
                                          for e in experts]))
-    w2 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed).numpy()
+    w2 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed, device).cpu().numpy()
                                         for e in experts]))
     return w13, w2
 
@@ -118,7 +120,7 @@ def _sampled_check(orc, cfg, mode, tokens, dev):
     lg_np = logits.cpu().numpy()
     ids, _ = orc.route(lg_np[tokens], cfg.k)
     used = np.unique(ids)
-    w13, w2 = _oracle_weights(orc, cfg, used)
+    w13, w2 = _oracle_weights(orc, cfg, used, device=dev)
     # the GPU quantised the same weights: identical codes and scales
     for i, e in enumerate(used):
         assert np.array_equal(g13[0][e].cpu().numpy(), w13[0][i]) and np.array_equal(s13[e].cpu().numpy(), w13[1][i])

@@ -44,9 +44,10 @@ def test_swiglu_w4a16_bf16(orc, R, I):
     torch.cuda.synchronize()
     ref = orc.swiglu(G)
     got = hb.float().cpu().numpy()
-    # bf16 rounding of the fp32 value: at most half a bf16 ulp plus fp32 noise
+    # bf16 rounding of the fp32 value: at most half a bf16 ulp (<= 2^-8
+    # relative at the bottom of a binade) plus fp32 noise
     err = np.abs(got - ref)
-    assert np.all(err <= np.abs(ref) * (2.0 ** -8 * 0.5 + 1e-6) + 1e-30)
+    assert np.all(err <= np.abs(ref) * (2.0 ** -8 + 1e-6) + 1e-30)
 
 
 @pytest.mark.parametrize("T,k,H", [(1, 1, 4), (16, 8, 4096), (64, 22, 256), (7, 3, 6144)])
