@@ -4,14 +4,17 @@
 // Decode shapes: every expert sees 0..~64 tokens but streams a full weight
 // matrix, so the kernel is built to stream weights at HBM speed:
 //  * swap-AB: the weight tile (128 output rows x K) is the MMA's M=128 side
-//    and the expert's tokens are its N side, in groups of 32 (N=32 per MMA,
-//    up to 4 groups = 128 tokens per pass sharing one weight tile).
+//    and the expert's tokens are its N side: one MMA per K step covers up to
+//    4 groups of 32 tokens (N = 32*ng), 128 tokens per pass over the weights.
 //  * persistent CTAs (one per SM) walk the (expert, 128-row tile) work units
 //    in a static round-robin; empty experts cost one offsets read.
-//  * warp-specialised: warp 0 issues TMA (weights with an evict-first L2
-//    policy, activations evict-last since every tile of the expert re-reads
-//    them), warp 1 issues tcgen05.cp (block scales -> TMEM) and tcgen05.mma,
-//    warps 2-5 drain the fp32 accumulators from TMEM (tcgen05.ld) and store.
+//  * warp-specialised, every warp converged; single operations are issued
+//    through elect.sync (issuing tcgen05 work from a diverged lane costs
+//    several times more issue cycles, which at N = 32 is the bottleneck):
+//      warp 0    TMA producer (weights evict-first, activations evict-last)
+//      warp 1    tcgen05.cp of block scales into TMEM + tcgen05.mma
+//      warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32 stores
+//      warp 6    token-scale preparation (shared-memory transpose, below)
 //  * a 5-stage shared-memory ring (36 KB per stage) and two TMEM accumulator
 //    buffers, so loads, MMAs and the epilogue of the previous unit overlap.
 //  * every mbarrier wait is bounded; a timeout sets NVFP4_E_DEVICE_TIMEOUT,
@@ -19,26 +22,33 @@
 //
 // Operand layouts in shared memory (all K-major, 128-byte rows):
 //   weight codes   [128 rows][128 B]  TMA, 128-byte swizzle
-//   token codes    [32 rows][128 B]   per group, TMA, 128-byte swizzle
+//   token codes    [32 rows][128 B]   per group, TMA, 128-byte swizzle; the ng
+//                                     group tiles form one [32*ng][128 B] tile
 //   weight scales  4 x 512-byte atoms (pre-packed, one bulk copy)
 //   token scales   [32 rows][16 B]    per group, TMA, no swizzle
 // Block scales in TMEM: a 32-lane x 4-column patch per 128 rows (row r in lane
 // r % 32 of every lane quarter, column r / 32, byte = 16-element block within
-// the MMA's K=64), starting on a 4-column boundary for every MMA.  One MMA per
-// K step covers all ng token groups (N = 32*ng); its token-scale patch is made
-// by an in-place shared-memory transpose of the TMA'd scale tiles.
+// the MMA's K=64), starting on a 4-column boundary for every MMA.  The token
+// scales arrive as [group g][token i][K step kk x 4 B]; warp 6 rewrites them in
+// place as [kk][token i][group g x 4 B], so that block kk copied with
+// tcgen05.cp puts token 32g + i's scales for step kk in lane i, column g.
 #include <cuda.h>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
 
+// Timestamp hooks for pipeline studies; empty in the library build.
+#ifndef W4A4_TRACE
+#define W4A4_TRACE(point, index)
+#endif
+
 namespace nvfp4moe {
 namespace w4a4 {
 
 constexpr int BM = 128;     // weight rows per tile
 constexpr int KC = 256;     // K elements per stage (= one 128-byte swizzle row)
-constexpr int TG = 32;      // tokens per MMA
+constexpr int TG = 32;      // tokens per group
 constexpr int MAXG = 4;     // token groups per pass
 constexpr int STAGES = 5;
 constexpr int TOK_PER_PASS = TG * MAXG;
@@ -55,15 +65,14 @@ static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 
 // TMEM columns: two accumulators of 128 fp32 columns, then per stage 16
-// columns of weight scales (4 per MMA step) and 16 of token scales (4 per
-// group).
+// columns of weight scales and 16 of token scales (4 per K step each).
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = TOK_PER_PASS;  // 128
 constexpr uint32_t SF_BASE = 2 * ACC_COLS;   // 256
 constexpr uint32_t SF_STAGE = 32;
 static_assert(SF_BASE + STAGES * SF_STAGE <= TMEM_COLS, "TMEM budget");
 
-constexpr int NUM_THREADS = 192;  // warp0 TMA, warp1 MMA (+ scale repack), warps2-5 epilogue
+constexpr int NUM_THREADS = 224;  // 7 warps, roles above
 
 struct Params {
   const uint8_t* w_scales;  // packed atoms
@@ -82,28 +91,12 @@ __device__ __forceinline__ void expert_rows(const Params& p, int e, int& m0, int
   if (m0 < 0 || m1 < m0 || m1 > p.R) m0 = m1 = 0;
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      *abort_flag = 1;
-      report_status(dev_status, NVFP4_E_DEVICE_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_as, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t sf_ready[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
@@ -120,11 +113,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
+      mbar_init(&sf_ready[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4 * 32);
+      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -148,89 +142,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const int e = u / NT, nt = u % NT;
-        int m0, m1;
-        expert_rows(p, e, m0, m1);
-        for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-          const int ntok = min(TOK_PER_PASS, m1 - r0);
-          const int ng = (ntok + TG - 1) / TG;
-          const uint32_t bytes = W_BYTES + WS_BYTES + ng * (A_BYTES + AS_BYTES);
-          const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
-          for (int kc = 0; kc < KCH; ++kc) {
-            if (!wait_or_abort(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
-              ok = false;
-              break;
-            }
-            uint8_t* sb = smem + stage * STAGE_BYTES;
-            mbar_arrive_expect_tx(&full_bar[stage], bytes);
-            tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
-            bulk_load(sb + OFF_WS, wsc + (size_t)kc * 4 * 512, WS_BYTES, &full_bar[stage], pol_w);
-            for (int g = 0; g < ng; ++g) {
-              tma_load_2d(sb + OFF_A + g * A_BYTES, &tm_a, &full_bar[stage], kc * (KC / 2), r0 + g * TG, pol_a);
-              tma_load_2d(sb + OFF_AS + g * AS_BYTES, &tm_as, &full_bar[stage], kc * (KC / 16), r0 + g * TG, pol_a);
-            }
-            issued_mask |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
+    int it_p = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int e = u / NT, nt = u % NT;
+      int m0, m1;
+      expert_rows(p, e, m0, m1);
+      const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
+      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+        const int ng = (min(TOK_PER_PASS, m1 - r0) + TG - 1) / TG;
+        const uint32_t bytes = W_BYTES + WS_BYTES + ng * (A_BYTES + AS_BYTES);
+        for (int kc = 0; kc < KCH; ++kc) {
+          if (!warp_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = smem + stage * STAGE_BYTES;
+          if (lane == 0) W4A4_TRACE(0, it_p);
+          ew_arrive_expect_tx(&full_bar[stage], bytes);
+          ew_tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
+          ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * 4 * 512, WS_BYTES, &full_bar[stage], pol_w);
+          for (int g = 0; g < ng; ++g) {
+            ew_tma_load_2d(sb + OFF_A + g * A_BYTES, &tm_a, &full_bar[stage], kc * (KC / 2), r0 + g * TG, pol_a);
+            ew_tma_load_2d(sb + OFF_AS + g * AS_BYTES, &tm_as, &full_bar[stage], kc * (KC / 16), r0 + g * TG, pol_a);
+          }
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          ++it_p;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
           }
         }
       }
-      if (!ok) {
-        // copies already issued must land before the CTA's shared memory goes away
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued_mask >> s) & 1u) mbar_wait(&full_bar[s], (issued_par >> s) & 1u);
-      }
+    }
+    if (!ok && lane == 0) {
+      // copies already issued must land before the CTA's shared memory goes away
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued_mask >> s) & 1u) mbar_wait(&full_bar[s], (issued_par >> s) & 1u);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp waits for a stage and repacks the token scales in place;
-    // lane 0 then issues the scale copies and the MMAs.
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ token-scale preparation
     int stage = 0;
     uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
     bool ok = true;
-    const uint32_t smem_base = smem_u32(smem);
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const int e = u / NT;
       int m0, m1;
       expert_rows(p, e, m0, m1);
       for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-        const int ntok = min(TOK_PER_PASS, m1 - r0);
-        const int ng = (ntok + TG - 1) / TG;
-        const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
-        int got = 1;
-        if (lane == 0) got = wait_or_abort(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status) ? 1 : 0;
-        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_col = tmem + acc * ACC_COLS;
         for (int kc = 0; kc < KCH; ++kc) {
-          got = 1;
-          if (lane == 0) got = wait_or_abort(&full_bar[stage], phase, &abort_flag, p.dev_status) ? 1 : 0;
-          if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+          if (!warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
             ok = false;
             break;
           }
-          // Token scales arrive as [group g][token i][16 B = K steps kk 0..3 x 4
-          // scales].  Every MMA's scale operand must start on a 4-column
-          // boundary, so rewrite them in place as [kk][token i][group g x 4 B]:
-          // copied with tcgen05.cp, row i of block kk puts the scales of token
-          // 32g + i for step kk in lane i, column g (the N = 32*ng layout).
           uint8_t* as_tile = smem + stage * STAGE_BYTES + OFF_AS;
           uint4 v[MAXG];
 #pragma unroll
@@ -242,36 +213,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < 4; ++kk)
             *reinterpret_cast<uint4*>(as_tile + kk * AS_BYTES + lane * 16) =
                 make_uint4(w[0][kk], w[1][kk], w[2][kk], w[3][kk]);
-          fence_proxy_async_smem();
+          fence_proxy_async_smem();  // generic writes -> visible to tcgen05.cp (async proxy)
           __syncwarp();
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t sb = smem_base + stage * STAGE_BYTES;
-            const uint32_t sfa = tmem + SF_BASE + stage * SF_STAGE;
-            const uint32_t sfb = sfa + 16;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              tc_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
-              tc_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
-            }
-            const uint64_t adesc = desc_sw128(sb);
-            const uint64_t bdesc = desc_sw128(sb + OFF_A);  // the ng group tiles are one [32*ng x 128 B] tile
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
-              mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
-                           (kc | kk) != 0);
-            tc_commit(&empty_bar[stage]);
+          ew_arrive(&sf_ready[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
           }
-          __syncwarp();
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    int it_c = 0;
+    const uint32_t smem_base = smem_u32(smem);
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int e = u / NT;
+      int m0, m1;
+      expert_rows(p, e, m0, m1);
+      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+        const int ng = (min(TOK_PER_PASS, m1 - r0) + TG - 1) / TG;
+        const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
+        if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_col = tmem + acc * ACC_COLS;
+        for (int kc = 0; kc < KCH; ++kc) {
+          // sf_ready is arrived after the scale warp saw full_bar; waiting on
+          // both keeps the TMA completion directly observed by this warp
+          if (!warp_wait(&sf_ready[stage], phase, &abort_flag, p.dev_status) ||
+              !warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) W4A4_TRACE(1, it_c);
+          tc_fence_after();
+          const uint32_t sb = smem_base + stage * STAGE_BYTES;
+          const uint32_t sfa = tmem + SF_BASE + stage * SF_STAGE;
+          const uint32_t sfb = sfa + 16;
+          const uint64_t adesc = desc_sw128(sb);
+          const uint64_t bdesc = desc_sw128(sb + OFF_A);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            ew_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
+            ew_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
+            // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
+            ew_mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
+                            (kc | kk) != 0);
+          }
+          ew_commit(&empty_bar[stage]);
+          if (lane == 0) W4A4_TRACE(2, it_c);
+          ++it_c;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit(&acc_full[acc]);
-        __syncwarp();
+        ew_commit(&acc_full[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
@@ -279,35 +286,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     // every MMA issued by this warp has finished once drain_bar flips
-    if (lane == 0) {
-      tc_commit(&drain_bar);
-      mbar_wait(&drain_bar, 0);
-    }
+    ew_commit(&drain_bar);
+    if (lane == 0) mbar_wait(&drain_bar, 0);
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (warps 2-5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    int it_e = 0;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const int e = u / NT, nt = u % NT;
       int m0, m1;
       expert_rows(p, e, m0, m1);
+      if (m1 <= m0) continue;
       const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + e));
       const int n = nt * BM + q * 32 + lane;
       for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-        const int ntok = min(TOK_PER_PASS, m1 - r0);
-        const int ng = (ntok + TG - 1) / TG;
-        // lane 0 waits, the warp follows its verdict (tcgen05.ld is warp-collective)
-        int got = 1;
-        if (lane == 0) got = wait_or_abort(&acc_full[acc], acc_phase, &abort_flag, p.dev_status) ? 1 : 0;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
-        if (!got) {
+        const int ng = (min(TOK_PER_PASS, m1 - r0) + TG - 1) / TG;
+        if (!warp_wait(&acc_full[acc], acc_phase, &abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (lane == 0 && q == 0) W4A4_TRACE(3, it_e);
         for (int g = 0; g < ng; ++g) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS + g * TG, r);
@@ -319,7 +322,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&acc_empty[acc]);
+        __syncwarp();
+        ew_arrive(&acc_empty[acc]);
+        if (lane == 0 && q == 0) W4A4_TRACE(4, it_e);
+        ++it_e;
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
