@@ -208,6 +208,38 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
                       const float* S_h, float* out, int32_t* dev_status, void* workspace,
                       size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * moe_align_permute_noalloc -- moe_align_permute for callers that cannot
+ * give the library scratch memory.  (The reference pages have no counterpart:
+ * this is an interface convenience of this library, not a step of the method.)
+ *
+ * Some callers own every byte of device memory themselves -- a serving engine
+ * or plugin host with one pre-reserved arena and no workspace hook -- or run
+ * latency-critical code that must never call cudaMalloc, which can
+ * synchronise the whole device.  They can pass inputs and outputs but no
+ * workspace.  This entry point computes exactly what moe_align_permute
+ * computes (same arguments and results, minus `workspace`) and keeps its
+ * scratch in a fixed array of NVFP4MOE_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library's own device memory: it allocates nothing and calls no allocating
+ * routine.
+ *   - Limit: the scratch holds 8 * ceil(T / 32) * E bytes; a larger problem
+ *     (e.g. T > 2048 tokens at E = 1024 experts, T > 16384 at E = 128) is
+ *     refused with NVFP4_E_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - The array is shared by every call on a device and stays allocated while
+ *     the library is loaded.  Calls that overlap on the GPU (different streams
+ *     with no ordering between them) race on it; order them on one stream.
+ *     Nothing in it has to start at zero: each call writes every scratch word
+ *     before reading it.
+ * ------------------------------------------------------------------------ */
+#define NVFP4MOE_NOALLOC_SCRATCH_BYTES (512 * 1024)
+int moe_align_permute_noalloc(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                              int32_t* expert_offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
+                              const uint8_t* act_in_scales, int64_t act_cols, void* act_out,
+                              uint8_t* act_out_scales, int32_t* dev_status, nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4
 EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspace_bytes", "nvfp4_quantize",
            "nvfp4_pack_weight_scales", "moe_align_permute_workspace_bytes", "moe_align_permute",
            "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine", "moe_layer_workspace_bytes",
-           "moe_layer_forward")
+           "moe_layer_forward", "moe_align_permute_noalloc")
 
 
 class Nvfp4Error(RuntimeError):
@@ -79,6 +79,8 @@ def load(build_if_missing: bool = True):
     L.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
     L.moe_layer_forward.restype = _I
     L.moe_layer_forward.argtypes = [_I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_align_permute_noalloc.restype = _I
+    L.moe_align_permute_noalloc.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P, _P]
     _lib = L
     return L
 

@@ -1,0 +1,85 @@
+"""moe_align_permute_noalloc: the routing entry point for callers that cannot
+give the library scratch memory (a host that owns all device memory and offers
+no workspace, or a latency-critical path that must not call cudaMalloc).
+
+It is checked through the C ABI against the ordinary moe_align_permute (which
+takes a caller workspace) on the same inputs: identical ids, offsets,
+permutation and gathered rows, routing weights within 1e-6.  Two calls in a
+row with different problem sizes exercise the shared fixed scratch, which is
+reused without clearing.  The file is named so that pytest collects it last.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import cuda_or_skip
+from nvfp4_mixture_experts_top_gb300 import binding as B
+from nvfp4_mixture_experts_top_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_LIMIT = 512 * 1024  # NVFP4MOE_NOALLOC_SCRATCH_BYTES
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _outputs(T, E, k, H, dev):
+    R = T * k
+    return dict(ids=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, device=dev),
+                offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                perm=torch.empty(R, dtype=torch.int32, device=dev), inv=torch.empty(R, dtype=torch.int32, device=dev),
+                codes=torch.empty(R, H // 2, dtype=torch.uint8, device=dev),
+                scales=torch.empty(R, H // 16, dtype=torch.uint8, device=dev),
+                status=torch.zeros(1, dtype=torch.int32, device=dev))
+
+
+def _call(noalloc, logits, k, xc, xs, out):
+    L = B.load()
+    T, E = logits.shape
+    H = xc.shape[1] * 2
+    st = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    common = (_p(logits), T, E, k, _p(out["ids"]), _p(out["w"]), _p(out["offsets"]), _p(out["perm"]), _p(out["inv"]),
+              B.MOE_ACT_NVFP4, _p(xc), _p(xs), H, _p(out["codes"]), _p(out["scales"]), _p(out["status"]))
+    if noalloc:
+        return L.moe_align_permute_noalloc(*common, st)
+    ws = torch.empty(max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256), dtype=torch.uint8,
+                     device=logits.device)
+    return L.moe_align_permute(*common, _p(ws), ws.numel(), st)
+
+
+def _case(name, dev):
+    cfg = wl.CONFIGS[name]
+    logits = wl.router_logits(cfg, device=dev)
+    x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
+    xc, xs, _ = B.nvfp4_quantize(x)
+    return cfg, logits, xc, xs
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    dev = cuda_or_skip()
+    for name in ("decode_b512", "decode_c16"):  # larger problem first, then a smaller one over its leftovers
+        cfg, logits, xc, xs = _case(name, dev)
+        ref = _outputs(cfg.T, cfg.E, cfg.k, cfg.H, dev)
+        got = _outputs(cfg.T, cfg.E, cfg.k, cfg.H, dev)
+        assert _call(False, logits, cfg.k, xc, xs, ref) == 0
+        assert _call(True, logits, cfg.k, xc, xs, got) == 0
+        torch.cuda.synchronize()
+        for key in ("ids", "offsets", "perm", "inv", "codes", "scales", "status"):
+            assert torch.equal(got[key], ref[key]), (name, key)
+        assert torch.allclose(got["w"], ref["w"], rtol=1e-6, atol=0), name
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    dev = cuda_or_skip()
+    E, k = 1024, 8
+    T = 2048 + 32  # 8 * ceil(T/32) * E = 8 * 65 * 1024 bytes > 512 KB
+    assert 8 * ((T + 31) // 32) * E > SCRATCH_LIMIT
+    logits = torch.zeros(T, E, device=dev)
+    out = _outputs(T, E, k, 256, dev)
+    xc = torch.zeros(T, 128, dtype=torch.uint8, device=dev)
+    xs = torch.zeros(T, 16, dtype=torch.uint8, device=dev)
+    assert _call(True, logits, k, xc, xs, out) == 4  # NVFP4_E_WORKSPACE, nothing launched
