@@ -104,9 +104,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _kernel_hash():
+def _kernel_hash(mode="w4a4"):
+    """Hash of the sources of the dominant kernel of a mode (staleness check
+    of the committed DRAM-traffic figure)."""
     h = hashlib.sha256()
-    for fn in ("gemm_w4a4.cu", "gemm_w4a16.cu", "common.cuh"):
+    for fn in ("gemm_%s.cu" % mode, "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -121,7 +123,7 @@ def _traffic(workload, mode):
     with open(p) as f:
         d = json.load(f)
     e = d.get("%s/%s" % (workload, mode))
-    if not e or e.get("kernel_hash") != _kernel_hash():
+    if not e or e.get("kernel_hash") != _kernel_hash(mode):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -206,13 +208,100 @@ def run_reference(args, cfg, metric, unit):
     print(json.dumps(line), flush=True)
 
 
+def run_gemm_sweep(args, wl):
+    """Single-expert NVFP4 GEMM, N=2048, K=6144, M in {1,16,64,512,4096}.
+    Each M is timed as a CUDA graph of back-to-back GEMMs rotating over enough
+    copies of A, W and out that their total exceeds twice the L2, so every
+    launch reads its operands from HBM.  value = FP4 TFLOPS at M=512."""
+    import torch
+
+    from nvfp4_mixture_experts_top_gb300 import binding as B
+    dev = torch.device("cuda", _dist()[2])
+    torch.cuda.set_device(dev)
+    B.load()
+    B.nvfp4_device_check()
+    hbm, bf16_tf, peak_kind = _load_peaks()
+    fp4_peak = bf16_tf * 6.0  # nominal dense FP4 : BF16 ratio (13.5 / 2.25)
+    N, K = wl.GEMM_SWEEP["N"], wl.GEMM_SWEEP["K"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    _, w = wl.gemm_operands_fp32(1, N, K, device=dev)
+    wc, ws, wS = B.nvfp4_quantize(w)
+    packed = B.nvfp4_pack_weight_scales(ws, 1, N, K)
+    del w
+    L = B.load()
+    rows = []
+    for M in wl.GEMM_SWEEP["Ms"]:
+        a, _ = wl.gemm_operands_fp32(M, 1, K, device=dev)
+        ac, as_, aS = B.nvfp4_quantize(a)
+        del a
+        per_copy = N * K * 0.5625 + M * K * 0.5625 + M * N * 4
+        copies = int(max(2, np.ceil(2 * l2 / per_copy)))
+        Ws = [(wc.clone(), packed.clone()) for _ in range(copies)]
+        As = [(ac.clone(), as_.clone()) for _ in range(copies)]
+        outs = [torch.empty(M, N, device=dev) for _ in range(copies)]
+        offs = torch.tensor([0, M], dtype=torch.int32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def launch(i):
+            st = torch.cuda.current_stream().cuda_stream
+            r = L.moe_grouped_gemm_nvfp4(0, As[i][0].data_ptr(), As[i][1].data_ptr(), aS.data_ptr(),
+                                         Ws[i][0].data_ptr(), Ws[i][1].data_ptr(), wS.data_ptr(), offs.data_ptr(),
+                                         1, N, K, M, outs[i].data_ptr(), status.data_ptr(), st)
+            if r != 0:
+                raise B.Nvfp4Error("moe_grouped_gemm_nvfp4", r)
+
+        for i in range(args.warmup):
+            launch(i % copies)
+        reps = max(args.steps, copies)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(reps):
+                    launch(i % copies)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status %d" % int(status.item()))
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        flops = 2.0 * M * N * K
+        tflops = flops / (us * 1e-6) / 1e12
+        gbs = per_copy / (us * 1e-6) / 1e9
+        roof_us = max(per_copy / (hbm * 1e9), flops / (fp4_peak * 1e12)) * 1e6
+        rows.append({"M": M, "us": us, "tflops": tflops, "gbs": gbs, "roofline_us": roof_us,
+                     "frac_of_roofline": roof_us / us, "bound": "hbm" if per_copy / (hbm * 1e9) > flops / (
+                         fp4_peak * 1e12) else "tensor", "copies": copies})
+        del Ws, As, outs, g
+    m512 = [r for r in rows if r["M"] == 512][0]
+    result = {"metric": "FP4 TFLOPS at M=512 (single-expert NVFP4 GEMM, N=2048, K=6144)", "value": m512["tflops"],
+              "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+              "ms_per_step": m512["us"] / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "fp4(e2m1)xfp4, fp32 accumulate", "data": "synthetic",
+              "config": {"workload": "gemm_sweep", "N": N, "K": K, "Ms": list(wl.GEMM_SWEEP["Ms"]),
+                         "l2": "rotating %d+ operand copies > 2x L2" % min(r["copies"] for r in rows)},
+              "roofline": {"bound": m512["bound"], "achieved": m512["tflops"], "peak": fp4_peak, "unit": "TFLOP/s",
+                           "frac": m512["tflops"] / fp4_peak,
+                           "peak_kind": "measured bf16 x nominal fp4/bf16 ratio 6 (%s)" % peak_kind,
+                           "traffic": None},
+              "sweep": rows, "gpu_launches": 1}
+    print(json.dumps(result), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_c16", choices=["decode_c16", "decode_b512", "wide", "tiny"])
+    ap.add_argument("--workload", default="decode_c16",
+                    choices=["decode_c16", "decode_b512", "wide", "tiny", "gemm_sweep"])
     ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16"])
     ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
     ap.add_argument("--baseline-tokens", type=int, default=4, help="tokens of the in-run CPU baseline")
@@ -224,6 +313,8 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     from nvfp4_mixture_experts_top_gb300 import workloads as wl
+    if args.workload == "gemm_sweep":
+        return run_gemm_sweep(args, wl)
     cfg = wl.CONFIGS[args.workload]
     if args.experts:
         cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)

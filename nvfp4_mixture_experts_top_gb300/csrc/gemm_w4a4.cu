@@ -6,8 +6,9 @@
 //  * swap-AB: the weight tile (128 output rows x K) is the MMA's M=128 side
 //    and the expert's tokens are its N side: one MMA per K step covers up to
 //    4 groups of 32 tokens (N = 32*ng), 128 tokens per pass over the weights.
-//  * persistent CTAs (one per SM) walk the (expert, 128-row tile) work units
-//    in a static round-robin; empty experts cost one offsets read.
+//  * persistent CTAs (one per SM) walk the work items -- (expert, 128-row
+//    tile, 128-token pass) -- in a static round-robin; each CTA first builds
+//    the per-expert item prefix from expert_offsets in shared memory.
 //  * warp-specialised, every warp converged; single operations are issued
 //    through elect.sync (issuing tcgen05 work from a diverged lane costs
 //    several times more issue cycles, which at N = 32 is the bottleneck):
@@ -91,6 +92,58 @@ __device__ __forceinline__ void expert_rows(const Params& p, int e, int& m0, int
   if (m0 < 0 || m1 < m0 || m1 > p.R) m0 = m1 = 0;
 }
 
+constexpr int MAX_E = 1024;
+
+// Work item = (expert e, 128-row weight tile nt, 128-token pass).  Items are
+// numbered expert-major, then tile, then pass, so the passes of one weight
+// tile run on neighbouring CTAs at the same time and share it through L2.
+// s_base[e] = number of items of experts < e (s_base[E] = all items).
+struct Item {
+  int e, nt, r0, m1, ng;
+};
+
+__device__ __forceinline__ void build_item_prefix(const Params& p, int NT, int* s_base, int lane) {
+  int carry = 0;
+  for (int e0 = 0; e0 < p.E; e0 += 32) {
+    const int e = e0 + lane;
+    int cnt = 0;
+    if (e < p.E) {
+      int m0, m1;
+      expert_rows(p, e, m0, m1);
+      cnt = NT * ((m1 - m0 + TOK_PER_PASS - 1) / TOK_PER_PASS);
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (e < p.E) s_base[e] = carry + x - cnt;
+    carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+  }
+  if (lane == 0) s_base[p.E] = carry;
+}
+
+__device__ __forceinline__ Item decode_item(int w, const int* s_base, int NT, const Params& p) {
+  int lo = 0, hi = p.E;  // s_base[lo] <= w < s_base[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_base[mid] <= w) lo = mid;
+    else hi = mid;
+  }
+  Item it;
+  int m0, m1;
+  expert_rows(p, lo, m0, m1);
+  const int passes = (m1 - m0 + TOK_PER_PASS - 1) / TOK_PER_PASS;
+  const int local = w - s_base[lo];
+  it.e = lo;
+  it.nt = local / passes;
+  it.r0 = m0 + (local % passes) * TOK_PER_PASS;
+  it.m1 = m1;
+  it.ng = (min(TOK_PER_PASS, m1 - it.r0) + TG - 1) / TG;
+  return it;
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_as, const Params p) {
@@ -103,12 +156,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
+  __shared__ int s_base[MAX_E + 1];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = p.N / BM;
   const int KCH = p.K / KC;
-  const int units = p.E * NT;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -131,10 +184,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&tmem_base_s, TMEM_COLS);
     tmem_relinquish();
   }
+  if (warp == 2) build_item_prefix(p, NT, s_base, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  const int items = s_base[p.E];
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(p.offsets + p.E) != p.R || __ldg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
@@ -149,13 +204,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
     int it_p = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int e = u / NT, nt = u % NT;
-      int m0, m1;
-      expert_rows(p, e, m0, m1);
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const Item it = decode_item(w, s_base, NT, p);
+      const int e = it.e, nt = it.nt, r0 = it.r0, ng = it.ng;
       const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
-      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-        const int ng = (min(TOK_PER_PASS, m1 - r0) + TG - 1) / TG;
+      {
         const uint32_t bytes = W_BYTES + WS_BYTES + ng * (A_BYTES + AS_BYTES);
         for (int kc = 0; kc < KCH; ++kc) {
           if (!warp_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
@@ -192,11 +245,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int e = u / NT;
-      int m0, m1;
-      expert_rows(p, e, m0, m1);
-      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      {
         for (int kc = 0; kc < KCH; ++kc) {
           if (!warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
             ok = false;
@@ -233,12 +283,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int it_c = 0;
     const uint32_t smem_base = smem_u32(smem);
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int e = u / NT;
-      int m0, m1;
-      expert_rows(p, e, m0, m1);
-      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-        const int ng = (min(TOK_PER_PASS, m1 - r0) + TG - 1) / TG;
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const int ng = decode_item(w, s_base, NT, p).ng;
+      {
         const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
         if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
@@ -296,15 +343,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     int it_e = 0;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int e = u / NT, nt = u % NT;
-      int m0, m1;
-      expert_rows(p, e, m0, m1);
-      if (m1 <= m0) continue;
-      const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + e));
-      const int n = nt * BM + q * 32 + lane;
-      for (int r0 = m0; ok && r0 < m1; r0 += TOK_PER_PASS) {
-        const int ng = (min(TOK_PER_PASS, m1 - r0) + TG - 1) / TG;
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const Item it = decode_item(w, s_base, NT, p);
+      const int r0 = it.r0, m1 = it.m1, ng = it.ng;
+      const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
+      const int n = it.nt * BM + q * 32 + lane;
+      {
         if (!warp_wait(&acc_full[acc], acc_phase, &abort_flag, p.dev_status)) {
           ok = false;
           break;
@@ -377,9 +421,10 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   p.N = N;
   p.K = K;
   p.R = R;
-  const int units = E * (N / BM);
-  const int grid = units < num_sms() ? units : num_sms();
-  gemm_w4a4_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, p);
+  if (E > MAX_E) return cudaErrorInvalidValue;
+  // the number of work items depends on the routing, which lives on the
+  // device: launch one persistent CTA per SM and let each find its items
+  gemm_w4a4_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, p);
   return cudaGetLastError();
 }
 
