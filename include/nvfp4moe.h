@@ -222,9 +222,10 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
  * scratch in a fixed array of NVFP4MOE_NOALLOC_SCRATCH_BYTES bytes inside the
  * library's own device memory: it allocates nothing and calls no allocating
  * routine.
- *   - Limit: the scratch holds 8 * ceil(T / 32) * E bytes; a larger problem
- *     (e.g. T > 2048 tokens at E = 1024 experts, T > 16384 at E = 128) is
- *     refused with NVFP4_E_WORKSPACE before anything is launched.
+ *   - Limit: a call needs 256 + 4 * ceil(T / 32) * E bytes of scratch (rounded
+ *     up to 256); a larger problem (e.g. T > 4064 tokens at E = 1024 experts,
+ *     T > 32736 at E = 128) is refused with NVFP4_E_WORKSPACE before anything
+ *     is launched.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
  *     stream capture.

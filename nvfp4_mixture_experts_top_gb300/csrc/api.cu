@@ -247,9 +247,6 @@ static LayerWs carve(void* base, int mode, int T, int H, int I, int E, int k) {
   w.Y = reinterpret_cast<float*>(take(R * H * 4));
   if (mode == MOE_W4A4) {
     w.S_x = reinterpret_cast<float*>(take(16));
-    w.amax = reinterpret_cast<uint32_t*>(take(256));
-    w.xq_codes = take((size_t)T * H / 2);
-    w.xq_scales = take((size_t)T * H / 16);
     w.a_codes = take(R * H / 2);
     w.a_scales = take(R * H / 16);
     w.h_codes = take(R * I / 2);
@@ -288,13 +285,16 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
   const int R = T * k;
   int s;
   if (mode == MOE_W4A4) {
-    s = nvfp4_quantize(x, NVFP4_DT_BF16, T, H, H, w.S_x, NVFP4_SCALE_DYNAMIC, w.xq_codes, w.xq_scales, w.amax, 256,
-                       stream);
-    if (s != NVFP4_OK) return s;
-    s = moe_align_permute(logits, T, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, MOE_ACT_NVFP4, w.xq_codes,
-                          w.xq_scales, H, w.a_codes, w.a_scales, dev_status, w.route,
-                          route_workspace_bytes(T, E), stream);
-    if (s != NVFP4_OK) return s;
+    // routing (+ the activation amax in the same pass), then the quantiser
+    // writes each token's NVFP4 row straight to its k permuted rows: the same
+    // results as nvfp4_quantize followed by moe_align_permute's gather
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_route_only(logits, T, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, dev_status, w.route, st, x, H) !=
+        cudaSuccess)
+      return NVFP4_E_CUDA;
+    if (launch_quantize_scatter(x, T, H, k, w.inv, static_cast<const uint32_t*>(w.route) + 1, w.S_x, w.a_codes,
+                                w.a_scales, st) != cudaSuccess)
+      return NVFP4_E_CUDA;
     s = moe_grouped_gemm_nvfp4(MOE_W4A4, w.a_codes, w.a_scales, w.S_x, w13_codes, w13_scales_packed, w13_S,
                                w.offsets, E, 2 * I, H, R, w.G, dev_status, stream);
     if (s != NVFP4_OK) return s;

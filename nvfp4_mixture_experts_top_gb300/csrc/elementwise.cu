@@ -92,6 +92,33 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ x, 
   }
 }
 
+// Quantise x [T, H] (bf16) with the dynamic scale S = amax / 2688 and write
+// every token's NVFP4 row straight to its k permuted rows inv[t*k + j]: the
+// quantiser and the row gather in one pass (each block quantised once).
+__global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int64_t H,
+                                                               int k, const int32_t* __restrict__ inv,
+                                                               const uint32_t* __restrict__ amax_bits,
+                                                               float* __restrict__ S, uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ scales) {
+  const float s = __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *S = s;
+  const int64_t nb_row = H / 16;
+  const int64_t nblk = (int64_t)T * nb_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / nb_row, b = i % nb_row;
+    float v[16];
+    load8<__nv_bfloat16>(x + t * H + b * 16, v);
+    load8<__nv_bfloat16>(x + t * H + b * 16 + 8, v + 8);
+    uint32_t w0, w1;
+    const uint8_t sc = (uint8_t)quantize_block16(v, s, w0, w1);
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = __ldg(inv + t * k + j);
+      *reinterpret_cast<uint2*>(codes + r * (H / 2) + b * 8) = make_uint2(w0, w1);
+      scales[r * nb_row + b] = sc;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // weight-scale packing: linear [E, N, K/16] -> 512-byte atoms
 // ---------------------------------------------------------------------------
@@ -226,6 +253,16 @@ cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t co
   else
     quantize_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, S, dynamic, amax_ws,
                                               codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
+                                    const uint32_t* amax_bits, float* S, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t st) {
+  const int64_t nblk = (int64_t)T * (H / 16);
+  if (nblk == 0) return cudaSuccess;
+  quantize_scatter_kernel<<<grid_for(nblk, 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x_bf16), T, H, k,
+                                                               inv, amax_bits, S, codes, scales);
   return cudaGetLastError();
 }
 

@@ -38,6 +38,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
+#include "workitems.cuh"
 
 // Timestamp hooks for pipeline studies; empty in the library build.
 #ifndef W4A4_TRACE
@@ -85,64 +86,6 @@ struct Params {
   int E, N, K, R;
 };
 
-// Rows [m0, m1) of expert e, or an empty range if the offsets are invalid.
-__device__ __forceinline__ void expert_rows(const Params& p, int e, int& m0, int& m1) {
-  m0 = __ldg(p.offsets + e);
-  m1 = __ldg(p.offsets + e + 1);
-  if (m0 < 0 || m1 < m0 || m1 > p.R) m0 = m1 = 0;
-}
-
-constexpr int MAX_E = 1024;
-
-// Work item = (expert e, 128-row weight tile nt, 128-token pass).  Items are
-// numbered expert-major, then tile, then pass, so the passes of one weight
-// tile run on neighbouring CTAs at the same time and share it through L2.
-// s_base[e] = number of items of experts < e (s_base[E] = all items).
-struct Item {
-  int e, nt, r0, m1, ng;
-};
-
-__device__ __forceinline__ void build_item_prefix(const Params& p, int NT, int* s_base, int lane) {
-  int carry = 0;
-  for (int e0 = 0; e0 < p.E; e0 += 32) {
-    const int e = e0 + lane;
-    int cnt = 0;
-    if (e < p.E) {
-      int m0, m1;
-      expert_rows(p, e, m0, m1);
-      cnt = NT * ((m1 - m0 + TOK_PER_PASS - 1) / TOK_PER_PASS);
-    }
-    int x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (e < p.E) s_base[e] = carry + x - cnt;
-    carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-  }
-  if (lane == 0) s_base[p.E] = carry;
-}
-
-__device__ __forceinline__ Item decode_item(int w, const int* s_base, int NT, const Params& p) {
-  int lo = 0, hi = p.E;  // s_base[lo] <= w < s_base[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_base[mid] <= w) lo = mid;
-    else hi = mid;
-  }
-  Item it;
-  int m0, m1;
-  expert_rows(p, lo, m0, m1);
-  const int passes = (m1 - m0 + TOK_PER_PASS - 1) / TOK_PER_PASS;
-  const int local = w - s_base[lo];
-  it.e = lo;
-  it.nt = local / passes;
-  it.r0 = m0 + (local % passes) * TOK_PER_PASS;
-  it.m1 = m1;
-  it.ng = (min(TOK_PER_PASS, m1 - it.r0) + TG - 1) / TG;
-  return it;
-}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
@@ -156,7 +99,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
-  __shared__ int s_base[MAX_E + 1];
+  __shared__ int s_base[kMaxExperts + 1];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,7 +127,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&tmem_base_s, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) build_item_prefix(p, NT, s_base, lane);
+  const ExpertRows xr{p.offsets, p.E, p.R};
+  if (warp == 2) build_item_prefix<TOK_PER_PASS>(xr, NT, s_base, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -205,7 +149,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int it_p = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const Item it = decode_item(w, s_base, NT, p);
+      const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const int e = it.e, nt = it.nt, r0 = it.r0, ng = it.ng;
       const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
       {
@@ -284,7 +228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int it_c = 0;
     const uint32_t smem_base = smem_u32(smem);
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const int ng = decode_item(w, s_base, NT, p).ng;
+      const int ng = decode_item<TOK_PER_PASS>(w, s_base, NT, xr).ng;
       {
         const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
         if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
@@ -344,7 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int it_e = 0;
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const Item it = decode_item(w, s_base, NT, p);
+      const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const int r0 = it.r0, m1 = it.m1, ng = it.ng;
       const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
       const int n = it.nt * BM + q * 32 + lane;
@@ -402,13 +346,13 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   CUtensorMap tm_w, tm_a, tm_as;
   cudaError_t err;
   // weight codes: [E*N rows, K/2 bytes], box 128 B x 128 rows, 128-byte swizzle
-  err = make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, true);
+  err = make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, 128);
   if (err != cudaSuccess) return err;
   // token codes: [R rows, K/2 bytes], box 128 B x 32 rows, 128-byte swizzle
-  err = make_tmap_2d_u8(&tm_a, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TG, true);
+  err = make_tmap_2d_u8(&tm_a, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TG, 128);
   if (err != cudaSuccess) return err;
   // token scales: [R rows, K/16 bytes], box 16 B x 32 rows, no swizzle
-  err = make_tmap_2d_u8(&tm_as, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TG, false);
+  err = make_tmap_2d_u8(&tm_as, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TG, 0);
   if (err != cudaSuccess) return err;
   Params p;
   p.w_scales = w_scales_packed;
@@ -421,7 +365,7 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   p.N = N;
   p.K = K;
   p.R = R;
-  if (E > MAX_E) return cudaErrorInvalidValue;
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
   // the number of work items depends on the routing, which lives on the
   // device: launch one persistent CTA per SM and let each find its items
   gemm_w4a4_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, p);

@@ -19,6 +19,19 @@ cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, i
 // Routing: top-k + stable counting sort + optional gather.  ws must hold
 // route_workspace_bytes(T, E).
 size_t route_workspace_bytes(int T, int E);
+// Routing alone; with x_bf16 != NULL it also leaves amax(|x|) ([T, H] bf16)
+// as fp32 bits in the second word of ws (for nvfp4 quantisation).
+cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                              int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dev_status, void* ws,
+                              cudaStream_t st, const void* x_bf16, int64_t H);
+cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* act_in, const uint8_t* act_in_scales,
+                          int64_t act_cols, void* act_out, uint8_t* act_out_scales, cudaStream_t st);
+// Quantise x [T, H] bf16 with S = amax/2688 (amax bits from the routing
+// pass; S written to *S) and write each token's NVFP4 row to its k permuted
+// rows inv[t*k + j].
+cudaError_t launch_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
+                                    const uint32_t* amax_bits, float* S, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t st);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
                          const uint8_t* act_in_scales, int64_t act_cols, void* act_out, uint8_t* act_out_scales,

@@ -13,8 +13,9 @@
 // loads it, and is shared by every call on that GPU: two calls that overlap on
 // the GPU (different streams, no ordering between them) race on it and give
 // undefined results.  Every scratch word is written before it is read within
-// one call (the per-chunk expert masks and row bases are rebuilt from the
-// logits each time), so nothing has to be cleared between calls.
+// one call (the completion counter is cleared by the call itself, the
+// per-chunk expert masks are rebuilt from the logits each time), so the
+// caller never has to clear anything between calls.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,8 +25,8 @@
 namespace nvfp4moe {
 namespace {
 
-// Fixed scratch: per 32-token chunk and expert, one 32-bit token mask and one
-// 32-bit row base (8 bytes per chunk x expert).
+// Fixed scratch: a 256-byte header (completion counter) and, per 32-token
+// chunk and expert, one 32-bit token mask.
 __device__ __align__(256) static uint8_t g_route_scratch[NVFP4MOE_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;

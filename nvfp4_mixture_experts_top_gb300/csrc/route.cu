@@ -1,19 +1,21 @@
 // route.cu -- router top-k and the stable expert permutation (counting sort)
-// plus the gather of activation rows into permuted order.
+// in one launch, plus the gather of activation rows into permuted order.
 //
-// Four small kernels, no atomics whose order could change a result:
-//  1. topk_kernel     one CTA per chunk of 32 tokens, one warp per token:
-//                     register-resident logits, k rounds of warp-shuffle
-//                     arg-max (ties to the lower expert id), fp32 softmax over
-//                     the selected k; each chunk records, per expert, a 32-bit
-//                     mask of the chunk's tokens that chose it.
-//  2. scan_kernel     one CTA: per-expert counts (popcounts of the masks), an
-//                     exclusive block scan -> expert_offsets, and the base row
-//                     of every (chunk, expert) pair.
-//  3. scatter_kernel  per (token, slot): row = base[chunk][e] + popcount of
-//                     the mask bits of earlier tokens -> perm, inv.  Stable by
-//                     (expert, token) by construction.
-//  4. gather_kernel   one warp per permuted row, 16-byte vector copies.
+// route_kernel: one CTA per chunk of 32 tokens, one warp per token.
+//  1. top-k: the token's logits sit in registers (E/32 per lane, a
+//     compile-time count); k rounds of a warp-shuffle arg-max (ties to the
+//     lower expert id) give the experts in descending logit order; the weights
+//     are an fp32 softmax over the k selected logits.
+//  2. the chunk records, per expert, a 32-bit mask of its tokens that chose
+//     that expert (shared-memory atomicOr; the mask is order-independent).
+//  3. the last CTA to finish (device-scope counter) computes the per-expert
+//     counts (popcounts of all chunks' masks), an exclusive block scan ->
+//     expert_offsets, and then places every (token, slot) pair:
+//       row = offsets[e] + (rows of expert e in earlier chunks)
+//                        + popcount(mask bits of earlier tokens in the chunk)
+//     which is stable by (expert, token) by construction; then it resets the
+//     counter.
+// gather_kernel: one warp per permuted row, 16-byte vector copies.
 #include <math.h>
 
 #include "common.cuh"
@@ -24,131 +26,165 @@ namespace nvfp4moe {
 constexpr int kMaxE = 1024;
 constexpr int kChunk = 32;
 
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                   int32_t* __restrict__ ids, float* __restrict__ w,
-                                                   uint32_t* __restrict__ chunk_masks) {
+// Scratch layout: [0, 256) chunk counter and activation amax; then masks [C][E] u32.
+size_t route_workspace_bytes(int T, int E) {
+  const size_t C = (size_t)(T + kChunk - 1) / kChunk;
+  return 256 + ((C * (size_t)E * 4 + 255) & ~(size_t)255);
+}
+
+template <int NPER>
+__device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, int k, int lane, int& my_id,
+                                          float& my_w) {
+  float v[NPER];
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldg(l + e) : 0.0f;
+  }
+  uint32_t taken = 0;
+  my_id = 0;
+  float my_v = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    // local best among untaken entries (ascending id, strict > keeps the lower id on ties)
+    float bv = 0.0f;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (bi == 0x7FFFFFFF || v[i] > bv)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (oi != 0x7FFFFFFF && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_id = bi;
+      my_v = bv;
+    }
+  }
+  const float lmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+  const float ex = (lane < k) ? expf(__fsub_rn(my_v, lmax)) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+  my_w = __fdiv_rn(ex, sum);
+}
+
+template <int NPER>
+__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                     int32_t* __restrict__ ids, float* __restrict__ w,
+                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                                     int32_t* __restrict__ inv, uint32_t* __restrict__ counter,
+                                                     uint32_t* __restrict__ masks, int32_t* dev_status,
+                                                     const __nv_bfloat16* __restrict__ x, int64_t H,
+                                                     uint32_t* __restrict__ amax_bits) {
   __shared__ uint32_t mask[kMaxE];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0;
-  __syncthreads();
+  __shared__ int32_t base[kMaxE];
+  __shared__ int32_t warp_tot[32];
+  __shared__ bool last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  const int nper = (E + 31) / 32;
-  for (int tl = warp; tl < kChunk; tl += (int)(blockDim.x >> 5)) {
-    const int t = c * kChunk + tl;
-    if (t >= T) break;
-    const float* l = logits + (int64_t)t * E;
-    float v[kMaxE / 32];
+  const int C = gridDim.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0;
+  __syncthreads();
+
+  // 1-2: top-k of this chunk's tokens, chunk mask (and, when x is given, the
+  // amax of the token's activation row for the per-tensor NVFP4 scale)
+  const int t = c * kChunk + warp;
+  if (t < T && x != nullptr) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+    float m = 0.0f;
+    for (int64_t i = lane; i < H / 8; i += 32) {
+      const uint4 u = __ldg(row + i);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (i < nper && e < E) ? __ldg(l + e) : 0.0f;
+      for (int q = 0; q < 4; ++q)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
     }
-    uint32_t taken = 0;
-    int my_id = 0;
-    float my_v = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      // local best among untaken entries of this lane (ascending expert id,
-      // strict >, so the lowest id wins a tie)
-      float bv = 0.0f;
-      int bi = 0x7FFFFFFF;
 #pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i) {
-        const int e = lane + 32 * i;
-        if (i < nper && e < E && !((taken >> i) & 1u)) {
-          if (bi == 0x7FFFFFFF || v[i] > bv) {
-            bv = v[i];
-            bi = e;
-          }
-        }
-      }
-      // warp arg-max: larger value wins; equal values -> lower id
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-        const bool better = (oi != 0x7FFFFFFF) && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi));
-        if (better) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_id = bi;
-        my_v = bv;
-      }
-    }
-    const float lmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-    const float ex = (lane < k) ? expf(__fsub_rn(my_v, lmax)) : 0.0f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) atomicMax(amax_bits, __float_as_uint(m));
+  }
+  if (t < T) {
+    int my_id;
+    float my_w;
+    topk_warp<NPER>(logits + (int64_t)t * E, E, k, lane, my_id, my_w);
     if (lane < k) {
       ids[(int64_t)t * k + lane] = my_id;
-      w[(int64_t)t * k + lane] = __fdiv_rn(ex, sum);
-      atomicOr(&mask[my_id], 1u << tl);
+      w[(int64_t)t * k + lane] = my_w;
+      atomicOr(&mask[my_id], 1u << warp);
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_masks[(int64_t)c * E + e] = mask[e];
-}
+  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = mask[e];
 
-__global__ void __launch_bounds__(1024) scan_kernel(const uint32_t* __restrict__ masks, int C, int E, int R,
-                                                    int32_t* __restrict__ offsets, int32_t* __restrict__ base,
-                                                    int32_t* dev_status) {
-  __shared__ int32_t warp_tot[32];
+  // 3: the last chunk to finish does the scan and the scatter
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(counter, 1u) == (uint32_t)(C - 1));
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+
   const int e = threadIdx.x;
-  const int lane = e & 31, warp = e >> 5;
   int cnt = 0;
   if (e < E)
-    for (int c = 0; c < C; ++c) cnt += __popc(masks[(int64_t)c * E + e]);
-  // inclusive warp scan
-  int x = cnt;
+    for (int cc = 0; cc < C; ++cc) cnt += __popc(__ldcg(masks + (int64_t)cc * E + e));
+  int incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
   }
-  if (lane == 31) warp_tot[warp] = x;
+  if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int t = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+    int s = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
-      if (lane >= o) t += y;
+      const int y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += y;
     }
-    warp_tot[lane] = t;  // inclusive over warps
+    warp_tot[lane] = s;
   }
   __syncthreads();
-  const int excl = x - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
+  const int excl = incl - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
   if (e < E) {
     offsets[e] = excl;
+    base[e] = excl;
     if (e == E - 1) {
       offsets[E] = excl + cnt;
-      if (excl + cnt != R) report_status(dev_status, NVFP4_E_BAD_ROUTING);
-    }
-    int run = excl;
-    for (int c = 0; c < C; ++c) {
-      base[(int64_t)c * E + e] = run;
-      run += __popc(masks[(int64_t)c * E + e]);
+      if (excl + cnt != T * k) report_status(dev_status, NVFP4_E_BAD_ROUTING);
     }
   }
-}
-
-__global__ void scatter_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ masks,
-                               const int32_t* __restrict__ base, int T, int E, int k, int32_t* __restrict__ perm,
-                               int32_t* __restrict__ inv) {
-  const int c = blockIdx.x;
-  const int tl = threadIdx.x / k, j = threadIdx.x % k;
-  const int t = c * kChunk + tl;
-  if (tl >= kChunk || t >= T) return;
-  const int e = ids[(int64_t)t * k + j];
-  const uint32_t m = masks[(int64_t)c * E + e];
-  const int rank = __popc(m & ((1u << tl) - 1u));
-  const int row = base[(int64_t)c * E + e] + rank;
-  perm[row] = t;
-  inv[(int64_t)t * k + j] = row;
+  __syncthreads();
+  // chunks in order: pairs of chunk cc go after the rows of earlier chunks
+  for (int cc = 0; cc < C; ++cc) {
+    for (int pidx = threadIdx.x; pidx < kChunk * k; pidx += blockDim.x) {
+      const int tl = pidx / k, j = pidx % k;
+      const int tt = cc * kChunk + tl;
+      if (tt < T) {
+        const int ee = __ldcg(ids + (int64_t)tt * k + j);
+        const uint32_t m = __ldcg(masks + (int64_t)cc * E + ee);
+        const int row = base[ee] + __popc(m & ((1u << tl) - 1u));
+        perm[row] = tt;
+        inv[(int64_t)tt * k + j] = row;
+      }
+    }
+    __syncthreads();
+    if (e < E) base[e] += __popc(__ldcg(masks + (int64_t)cc * E + e));
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *counter = 0;
 }
 
 // One warp per permuted row: copy `row_bytes` (and `sc_bytes` of scales).
@@ -171,40 +207,50 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
   }
 }
 
-size_t route_workspace_bytes(int T, int E) {
-  const size_t C = (size_t)(T + kChunk - 1) / kChunk;
-  return ((2 * C * (size_t)E * 4) + 255) & ~(size_t)255;
+cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                              int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dev_status, void* ws,
+                              cudaStream_t st, const void* x_bf16, int64_t H) {
+  if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st);
+  const int C = (T + kChunk - 1) / kChunk;
+  uint32_t* counter = static_cast<uint32_t*>(ws);      // word 0: chunk counter, word 1: activation amax
+  uint32_t* masks = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
+  cudaError_t e = cudaMemsetAsync(counter, 0, 2 * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  const int nper = (E + 31) / 32;
+#define NVFP4MOE_ROUTE(NP)                                                                                   \
+  route_kernel<NP><<<C, 1024, 0, st>>>(logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, counter, masks, \
+                                       dev_status, static_cast<const __nv_bfloat16*>(x_bf16), H, counter + 1)
+  if (nper <= 1) NVFP4MOE_ROUTE(1);
+  else if (nper <= 2) NVFP4MOE_ROUTE(2);
+  else if (nper <= 4) NVFP4MOE_ROUTE(4);
+  else if (nper <= 8) NVFP4MOE_ROUTE(8);
+  else if (nper <= 16) NVFP4MOE_ROUTE(16);
+  else NVFP4MOE_ROUTE(32);
+#undef NVFP4MOE_ROUTE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* act_in, const uint8_t* act_in_scales,
+                          int64_t act_cols, void* act_out, uint8_t* act_out_scales, cudaStream_t st) {
+  if (R == 0 || act_kind == MOE_ACT_NONE) return cudaSuccess;
+  const int64_t row_bytes = (act_kind == MOE_ACT_NVFP4) ? act_cols / 2 : act_cols * 2;
+  const int64_t sc_bytes = (act_kind == MOE_ACT_NVFP4) ? act_cols / 16 : 0;
+  int blocks = (R + 7) / 8;
+  const int cap = num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  gather_kernel<<<blocks, 256, 0, st>>>(perm, R, static_cast<const uint8_t*>(act_in), act_in_scales, row_bytes,
+                                        sc_bytes, static_cast<uint8_t*>(act_out), act_out_scales);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
                          const uint8_t* act_in_scales, int64_t act_cols, void* act_out, uint8_t* act_out_scales,
                          int32_t* dev_status, void* ws, cudaStream_t st) {
-  if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st);
-  const int C = (T + kChunk - 1) / kChunk;
-  uint32_t* masks = static_cast<uint32_t*>(ws);
-  int32_t* base = reinterpret_cast<int32_t*>(masks + (size_t)C * E);
-  topk_kernel<<<C, 256, 0, st>>>(logits, T, E, k, topk_ids, topk_w, masks);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      launch_route_only(logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, dev_status, ws, st, nullptr, 0);
   if (e != cudaSuccess) return e;
-  scan_kernel<<<1, 1024, 0, st>>>(masks, C, E, T * k, offsets, base, dev_status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  scatter_kernel<<<C, kChunk * k, 0, st>>>(topk_ids, masks, base, T, E, k, perm, inv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (act_kind != MOE_ACT_NONE) {
-    const int R = T * k;
-    const int64_t row_bytes = (act_kind == MOE_ACT_NVFP4) ? act_cols / 2 : act_cols * 2;
-    const int64_t sc_bytes = (act_kind == MOE_ACT_NVFP4) ? act_cols / 16 : 0;
-    int blocks = (R + 7) / 8;
-    const int cap = num_sms() * 8;
-    if (blocks > cap) blocks = cap;
-    gather_kernel<<<blocks, 256, 0, st>>>(perm, R, static_cast<const uint8_t*>(act_in), act_in_scales, row_bytes,
-                                          sc_bytes, static_cast<uint8_t*>(act_out), act_out_scales);
-    e = cudaGetLastError();
-  }
-  return e;
+  return launch_gather(perm, T * k, act_kind, act_in, act_in_scales, act_cols, act_out, act_out_scales, st);
 }
 
 }  // namespace nvfp4moe

@@ -9,9 +9,9 @@
 namespace nvfp4moe {
 
 // 2-D uint8 tensor [rows, inner] with row pitch `pitch` bytes; box of
-// box_inner bytes x box_rows rows; 128-byte swizzle if `swizzle128`.
+// box_inner bytes x box_rows rows; swizzle_bytes = 0 (none), 64 or 128.
 // Out-of-bounds box elements are zero-filled by the copy.
 cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch,
-                            uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+                            uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
 
 }  // namespace nvfp4moe

@@ -76,8 +76,8 @@ def test_noalloc_matches_workspace_entry_point_twice():
 def test_noalloc_refuses_problems_beyond_its_scratch():
     dev = cuda_or_skip()
     E, k = 1024, 8
-    T = 2048 + 32  # 8 * ceil(T/32) * E = 8 * 65 * 1024 bytes > 512 KB
-    assert 8 * ((T + 31) // 32) * E > SCRATCH_LIMIT
+    T = 4096 + 32  # 256 + 4 * ceil(T/32) * E = 256 + 4 * 129 * 1024 bytes > 512 KB
+    assert 256 + 4 * ((T + 31) // 32) * E > SCRATCH_LIMIT
     logits = torch.zeros(T, E, device=dev)
     out = _outputs(T, E, k, 256, dev)
     xc = torch.zeros(T, 128, dtype=torch.uint8, device=dev)
