@@ -7,12 +7,12 @@
 // rounding is the fp32 accumulation, as in the W4A4 kernel.
 //
 // Structure (swap-AB as in the W4A4 kernel: 128 weight rows are the MMA's M
-// side, up to 2 groups of 32 tokens its N side; K step 128 per stage):
-//  warp 0       TMA: raw weight codes [128 rows][64 B] (64-byte swizzle),
-//               packed scales (1 KB), token tiles [32 rows][64 bf16] per group
+// side, up to 2 groups of 32 tokens its N side; K step 256 per stage):
+//  warp 0       TMA: raw weight codes [128 rows][128 B] (128-byte swizzle),
+//               packed scales (2 KB), token tiles [32 rows][64 bf16] per group
 //               and 64-element atom (128-byte swizzle)
 //  warps 6-13   dequantise: warp (quarter q, half h) turns rows 32q..32q+31,
-//               K elements 64h..64h+63 of the stage into BF16 and writes them
+//               K elements 128h..128h+127 of the stage into BF16 and writes them
 //               straight into tensor memory (tcgen05.st), where the MMA reads
 //               its A operand -- no shared-memory round trip for the 4x larger
 //               BF16 tile
@@ -35,29 +35,30 @@ namespace nvfp4moe {
 namespace w4a16 {
 
 constexpr int BM = 128;
-constexpr int KC = 128;     // K elements per stage
+constexpr int KC = 256;     // K elements per stage
 constexpr int TG = 32;
 constexpr int MAXG = 2;     // token groups per pass
-constexpr int RSTAGES = 8;  // raw stages
-constexpr int ASLOTS = 4;   // dequantised operand slots in TMEM (dequantisation runs ahead of the MMAs)
+constexpr int RSTAGES = 4;  // raw stages
+constexpr int ASLOTS = 3;   // dequantised operand slots in TMEM (dequantisation runs ahead of the MMAs)
 constexpr int TOK_PER_PASS = TG * MAXG;
 
 constexpr uint32_t B_GROUP = TG * 128;              // 4096: one group's 64-element atom
 constexpr uint32_t B_ATOM = MAXG * B_GROUP;          // 8192: all groups' rows of one atom
+constexpr int NATOM = KC / 64;                       // 4 atoms of 64 bf16 per stage
 constexpr uint32_t OFF_B = 0;                        // [atom][group][32 rows][128 B]
-constexpr uint32_t OFF_W = OFF_B + 2 * B_ATOM;       // 16384: raw codes [128][64 B], 64-byte swizzle
-constexpr uint32_t W_BYTES = BM * KC / 2;            // 8192
-constexpr uint32_t OFF_WS = OFF_W + W_BYTES;         // 24576: packed scales, 2 atoms
-constexpr uint32_t WS_BYTES = BM * KC / 16;          // 1024
-constexpr uint32_t RSTAGE_BYTES = 25600;             // 25 KB
+constexpr uint32_t OFF_W = OFF_B + NATOM * B_ATOM;   // 32768: raw codes [128][128 B], 128-byte swizzle
+constexpr uint32_t W_BYTES = BM * KC / 2;            // 16384
+constexpr uint32_t OFF_WS = OFF_W + W_BYTES;         // 49152: packed scales, 4 atoms
+constexpr uint32_t WS_BYTES = BM * KC / 16;          // 2048
+constexpr uint32_t RSTAGE_BYTES = 51200;             // 50 KB
 static_assert(OFF_WS + WS_BYTES <= RSTAGE_BYTES && RSTAGE_BYTES % 1024 == 0, "raw stage layout");
 constexpr uint32_t SMEM_BYTES = RSTAGES * RSTAGE_BYTES + 1024;
 
-// TMEM: two accumulators of 64 columns, then four A slots of 64 columns
-// (128 rows x 128 bf16 = 64 32-bit columns).
+// TMEM: two accumulators of 64 columns, then three A slots of 128 columns
+// (128 rows x 256 bf16 = 128 32-bit columns).
 constexpr uint32_t ACC_COLS = TOK_PER_PASS;  // 64
 constexpr uint32_t A_COL0 = 2 * ACC_COLS;    // 128
-constexpr uint32_t A_SLOT_COLS = KC / 2;     // 64
+constexpr uint32_t A_SLOT_COLS = KC / 2;     // 128
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(A_COL0 + ASLOTS * A_SLOT_COLS <= TMEM_COLS, "TMEM budget");
 
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
       const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const uint8_t* wsc = p.w_scales + ((size_t)(it.e * NT + it.nt) * (p.K / 64)) * 512;
-      const uint32_t bytes = W_BYTES + WS_BYTES + it.ng * 2 * B_GROUP;
+      const uint32_t bytes = W_BYTES + WS_BYTES + it.ng * NATOM * B_GROUP;
       for (int kc = 0; kc < KCH; ++kc) {
         if (!warp_wait(&raw_empty[stage], phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
@@ -170,10 +171,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) W4A16_TRACE(0, it_p);
         ew_arrive_expect_tx(&raw_full[stage], bytes);
         ew_tma_load_2d(sb + OFF_W, &tm_w, &raw_full[stage], kc * (KC / 2), it.e * p.N + it.nt * BM, pol_w);
-        ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * 2 * 512, WS_BYTES, &raw_full[stage], pol_w);
+        ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * NATOM * 512, WS_BYTES, &raw_full[stage], pol_w);
         for (int g = 0; g < it.ng; ++g)
 #pragma unroll
-          for (int a = 0; a < 2; ++a)
+          for (int a = 0; a < NATOM; ++a)
             // x is a byte coordinate: (kc*KC + a*64) bf16 elements * 2 bytes
             ew_tma_load_2d(sb + OFF_B + a * B_ATOM + g * B_GROUP, &tm_b, &raw_full[stage], (kc * KC + a * 64) * 2,
                            it.r0 + g * TG, pol_b);
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ dequantise
     const int q = warp & 3;             // TMEM lane quarter this warp may write
-    const int h = (warp - 6) >> 2;      // K half of the stage
+    const int h = (warp - 6) >> 2;      // K half of the stage (128 elements)
     const int r = q * 32 + lane;        // weight row within the tile
     int stage = 0, slot = 0;
     uint32_t phase = 0, slot_phase = 0;
@@ -297,25 +298,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         if (lane == 0 && warp == 6) W4A16_TRACE(1, it_d);
-        const uint8_t* sw = smem + stage * RSTAGE_BYTES + OFF_W + r * 64;
+        const uint8_t* sw = smem + stage * RSTAGE_BYTES + OFF_W + r * 128;
         const uint8_t* ss = smem + stage * RSTAGE_BYTES + OFF_WS;
-        // row r's 32 bytes for K half h: 16-byte chunks 2h and 2h+1, placed by
-        // the 64-byte swizzle at chunk ^ ((r >> 1) & 3)
-        const int sw_x = (r >> 1) & 3;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(sw + ((2 * h) ^ sw_x) * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(sw + ((2 * h + 1) ^ sw_x) * 16);
-        // the 4 block scales of row r for K half h: one word of packed atom h
-        const uint32_t s4 = *reinterpret_cast<const uint32_t*>(ss + h * 512 + (r & 31) * 16 + (r >> 5) * 4);
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t outw[32];
+        // row r's 64 bytes for K half h: 16-byte chunks 4h..4h+3, placed by the
+        // 128-byte swizzle at chunk ^ (r & 7)
+        const int sw_x = r & 7;
+        const uint32_t a_col = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + slot * A_SLOT_COLS + 64 * h;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 16-element block j of this half
-          const __half sh = __float2half_rn(f32_from_e4m3((s4 >> (8 * j)) & 0xFFu));
-          const __half2 s2 = __halves2half2(sh, sh);
-          dequant8(words[2 * j], s2, outw + 8 * j);
-          dequant8(words[2 * j + 1], s2, outw + 8 * j + 4);
+        for (int part = 0; part < 2; ++part) {  // 64 elements: chunks 4h+2part, 4h+2part+1
+          const uint4 c0 = *reinterpret_cast<const uint4*>(sw + ((4 * h + 2 * part) ^ sw_x) * 16);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(sw + ((4 * h + 2 * part + 1) ^ sw_x) * 16);
+          // the 4 block scales of these 64 elements: one word of packed atom 2h+part
+          const uint32_t s4 =
+              *reinterpret_cast<const uint32_t*>(ss + (2 * h + part) * 512 + (r & 31) * 16 + (r >> 5) * 4);
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t outw[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // 16-element block j
+            const __half sh = __float2half_rn(f32_from_e4m3((s4 >> (8 * j)) & 0xFFu));
+            const __half2 s2 = __halves2half2(sh, sh);
+            dequant8(words[2 * j], s2, outw + 8 * j);
+            dequant8(words[2 * j + 1], s2, outw + 8 * j + 4);
+          }
+          tmem_st_32x32b_x32(a_col + 32 * part, outw);
         }
-        tmem_st_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + slot * A_SLOT_COLS + 32 * h, outw);
         tmem_st_wait();
         if (lane == 0 && warp == 6) W4A16_TRACE(2, it_d);
         if (lane == 0) W4A16_TRACE(5 + warp - 6, it_d);
@@ -359,9 +365,9 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
     attr_set = true;
   }
   CUtensorMap tm_w, tm_b;
-  // raw weight codes: [E*N rows, K/2 bytes], box 64 B x 128 rows, 64-byte swizzle
+  // raw weight codes: [E*N rows, K/2 bytes], box 128 B x 128 rows, 128-byte swizzle
   cudaError_t err =
-      make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, 64);
+      make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, 128);
   if (err != cudaSuccess) return err;
   // bf16 tokens viewed as bytes: [R rows, 2K bytes], box 128 B x 32 rows, 128-byte swizzle
   err = make_tmap_2d_u8(&tm_b, a_bf16, (uint64_t)K * 2, (uint64_t)R, (uint64_t)K * 2, 128, TG, 128);
