@@ -347,9 +347,6 @@ def main():
     ws_route = torch.empty(max(B.load().moe_align_permute_workspace_bytes(T, cfg.E, k), 256), dtype=torch.uint8,
                            device=dev)
     S_x = torch.zeros(4, dtype=torch.float32, device=dev)
-    qws = torch.empty(256, dtype=torch.uint8, device=dev)
-    xq_c = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
-    xq_s = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     tw = torch.empty(T, k, dtype=torch.float32, device=dev)
     offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
@@ -374,9 +371,11 @@ def main():
     def step(ev_pair=None):
         st = torch.cuda.current_stream().cuda_stream
         if mode == B.MOE_W4A4:
-            chk(L.nvfp4_quantize(P(x), 0, T, H, H, P(S_x), 1, P(xq_c), P(xq_s), P(qws), 256, st))
-            chk(L.moe_align_permute(P(logits), T, cfg.E, k, P(ids), P(tw), P(offs), P(perm), P(inv), 1, P(xq_c),
-                                    P(xq_s), H, P(a_c), P(a_s), P(status), P(ws_route), ws_route.numel(), st))
+            # routing + activation quantisation straight into permuted rows
+            # (the kernels moe_layer_forward runs)
+            chk(L.moe_route_quantize_nvfp4(P(x), P(logits), T, H, cfg.E, k, P(ids), P(tw), P(offs), P(perm),
+                                           P(inv), P(S_x), P(a_c), P(a_s), P(status), P(ws_route),
+                                           ws_route.numel(), st))
             if ev_pair:
                 ev_pair[0].record()
             chk(L.moe_grouped_gemm_nvfp4(0, P(a_c), P(a_s), P(S_x), P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
@@ -400,7 +399,9 @@ def main():
                                          cfg.E, H, I, R, P(Y), P(status), st))
         chk(L.moe_combine(P(Y), P(inv), P(tw), T, k, H, 1, P(out), st))
 
-    launches_per_step = 10 if mode == B.MOE_W4A4 else 8
+    # kernels of this library per step: W4A4 route, quantise-scatter, 2 GEMMs,
+    # SwiGLU-requant, combine; W4A16 route, gather, 2 GEMMs, SwiGLU, combine
+    launches_per_step = 6
 
     # warm-up (eager)
     for _ in range(args.warmup):

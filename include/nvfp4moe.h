@@ -137,6 +137,26 @@ int moe_align_permute(const float* logits, int T, int E, int k, int32_t* topk_id
                       int32_t* dev_status, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_route_quantize_nvfp4 -- the W4A4 front half of the layer in one call:
+ * routing and permutation exactly as moe_align_permute, and the activations
+ * x quantised to NVFP4 with the dynamic per-tensor scale exactly as
+ * nvfp4_quantize, written straight into permuted order.  Results are
+ * identical to nvfp4_quantize(x, DYNAMIC) followed by moe_align_permute with
+ * an NVFP4 gather; the fused form reads x once (routing and amax in one
+ * pass) and skips the unpermuted intermediate.
+ *   x bf16 [T, H]; logits fp32 [T, E]
+ *   outputs: topk_ids, topk_w, expert_offsets, perm, inv as in
+ *   moe_align_permute; S_x (device fp32 scalar, amax(|x|)/2688); a_codes
+ *   [T*k, H/2], a_scales [T*k, H/16] in permuted row order
+ *   workspace >= moe_align_permute_workspace_bytes(T, E, k)
+ * Constraints: as moe_align_permute, and H % 256 == 0.
+ * ------------------------------------------------------------------------ */
+int moe_route_quantize_nvfp4(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                             float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, float* S_x,
+                             uint8_t* a_codes, uint8_t* a_scales, int32_t* dev_status, void* workspace,
+                             size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_grouped_gemm_nvfp4 -- ragged grouped GEMM over experts.
  * "The 2x Gap", sections "The Investigation So Far" and "Discovering the
  * sgl_kernel Alternative" (scaled FP4 GEMM: block scales on both operands

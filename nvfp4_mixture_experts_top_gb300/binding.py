@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4
 EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspace_bytes", "nvfp4_quantize",
            "nvfp4_pack_weight_scales", "moe_align_permute_workspace_bytes", "moe_align_permute",
            "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine", "moe_layer_workspace_bytes",
-           "moe_layer_forward", "moe_align_permute_noalloc")
+           "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4")
 
 
 class Nvfp4Error(RuntimeError):
@@ -79,6 +79,8 @@ def load(build_if_missing: bool = True):
     L.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
     L.moe_layer_forward.restype = _I
     L.moe_layer_forward.argtypes = [_I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_route_quantize_nvfp4.restype = _I
+    L.moe_route_quantize_nvfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_align_permute_noalloc.restype = _I
     L.moe_align_permute_noalloc.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P, _P]
     _lib = L
@@ -181,6 +183,31 @@ def moe_align_permute(logits, k, act=None, act_kind=MOE_ACT_NONE, dev_status=Non
            L.moe_align_permute(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _ptr(offsets), _ptr(perm), _ptr(inv),
                                act_kind, _ptr(a_in), _ptr(a_in_sc), cols, _ptr(a_out), _ptr(a_out_sc),
                                _ptr(dev_status), _ptr(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_route_quantize_nvfp4(x, logits, k, dev_status=None):
+    """Routing + NVFP4 quantisation of x [T, H] bf16 written in permuted order.
+    Returns dict(ids, w, offsets, perm, inv, S_x, act_codes, act_scales)."""
+    L = load()
+    T, H = x.shape
+    E = logits.shape[1]
+    dev = x.device
+    R = T * k
+    out = dict(ids=_empty((T, k), torch.int32, dev), w=_empty((T, k), torch.float32, dev),
+               offsets=_empty((E + 1,), torch.int32, dev), perm=_empty((max(R, 1),), torch.int32, dev),
+               inv=_empty((max(R, 1),), torch.int32, dev), S_x=torch.zeros(4, dtype=torch.float32, device=dev),
+               act_codes=_empty((max(R, 1), H // 2), torch.uint8, dev),
+               act_scales=_empty((max(R, 1), H // 16), torch.uint8, dev))
+    ws = _empty(max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256), torch.uint8, dev)
+    _check("moe_route_quantize_nvfp4",
+           L.moe_route_quantize_nvfp4(_ptr(x), _ptr(logits), T, H, E, k, _ptr(out["ids"]), _ptr(out["w"]),
+                                      _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv"]), _ptr(out["S_x"]),
+                                      _ptr(out["act_codes"]), _ptr(out["act_scales"]), _ptr(dev_status), _ptr(ws),
+                                      ws.numel(), _stream()))
+    for key in ("perm", "inv", "act_codes", "act_scales"):
+        out[key] = out[key][:R]
+    out["S_x"] = out["S_x"][:1]
     return out
 
 

@@ -3,6 +3,7 @@
 // point allocates device memory or synchronises.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/nvfp4moe.h"
@@ -21,6 +22,12 @@ int current_device() {
   return d;
 }
 }  // namespace
+
+int fault_injection_drop_stage() {
+  const char* v = getenv("NVFP4MOE_TEST_DROP_STAGE");
+  if (v == nullptr || *v == 0) return -1;
+  return atoi(v);
+}
 
 int num_sms() {
   const int d = current_device();
@@ -162,6 +169,39 @@ int moe_align_permute(const float* logits, int T, int E, int k, int32_t* topk_id
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_route_quantize_nvfp4(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                             float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, float* S_x,
+                             uint8_t* a_codes, uint8_t* a_scales, int32_t* dev_status, void* workspace,
+                             size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
+  if (k > E || k > 32 || E > 1024 || H % 256 != 0) return NVFP4_E_SHAPE;
+  if (expert_offsets == nullptr || S_x == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(expert_offsets) || !aligned16(S_x)) return NVFP4_E_ALIGN;
+  if (T > 0) {
+    if (x == nullptr || logits == nullptr || topk_ids == nullptr || topk_w == nullptr || perm == nullptr ||
+        inv == nullptr || a_codes == nullptr || a_scales == nullptr)
+      return NVFP4_E_INVAL;
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(perm) ||
+        !aligned16(inv) || !aligned16(a_codes) || !aligned16(a_scales))
+      return NVFP4_E_ALIGN;
+    if (workspace == nullptr || workspace_bytes < route_workspace_bytes(T, E)) return NVFP4_E_WORKSPACE;
+    if (!aligned16(workspace)) return NVFP4_E_ALIGN;
+  }
+  CHECK_ARCH();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (cudaMemsetAsync(S_x, 0, sizeof(float), st) != cudaSuccess) return NVFP4_E_CUDA;
+    return cuda_status(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st));
+  }
+  // routing (+ the activation amax in the same pass), then the quantiser
+  // writes each token's NVFP4 row straight to its k permuted rows
+  if (launch_route_only(logits, T, E, k, topk_ids, topk_w, expert_offsets, perm, inv, dev_status, workspace, st, x,
+                        H) != cudaSuccess)
+    return NVFP4_E_CUDA;
+  return cuda_status(launch_quantize_scatter(x, T, H, k, inv, static_cast<const uint32_t*>(workspace) + 1, S_x,
+                                             a_codes, a_scales, st));
+}
+
 int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, const float* a_S,
                            const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                            const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
@@ -285,16 +325,9 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
   const int R = T * k;
   int s;
   if (mode == MOE_W4A4) {
-    // routing (+ the activation amax in the same pass), then the quantiser
-    // writes each token's NVFP4 row straight to its k permuted rows: the same
-    // results as nvfp4_quantize followed by moe_align_permute's gather
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_route_only(logits, T, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, dev_status, w.route, st, x, H) !=
-        cudaSuccess)
-      return NVFP4_E_CUDA;
-    if (launch_quantize_scatter(x, T, H, k, w.inv, static_cast<const uint32_t*>(w.route) + 1, w.S_x, w.a_codes,
-                                w.a_scales, st) != cudaSuccess)
-      return NVFP4_E_CUDA;
+    s = moe_route_quantize_nvfp4(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_codes,
+                                 w.a_scales, dev_status, w.route, route_workspace_bytes(T, E), stream);
+    if (s != NVFP4_OK) return s;
     s = moe_grouped_gemm_nvfp4(MOE_W4A4, w.a_codes, w.a_scales, w.S_x, w13_codes, w13_scales_packed, w13_S,
                                w.offsets, E, 2 * I, H, R, w.G, dev_status, stream);
     if (s != NVFP4_OK) return s;

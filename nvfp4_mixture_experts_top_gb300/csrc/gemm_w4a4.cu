@@ -84,6 +84,8 @@ struct Params {
   float* out;
   int32_t* dev_status;
   int E, N, K, R;
+  int drop_stage;  // fault injection for tests: producer stage index never armed (-1: none)
+  int splits;      // K splits per work item: 1, or 2 (the halves add into a zeroed output)
 };
 
 
@@ -133,7 +135,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const int items = s_base[p.E];
+  // work unit = (item, K split); splits is 1, or 2 when the items alone
+  // cannot fill the GPU (the two K halves then add into a zeroed output)
+  const int units = s_base[p.E] * p.splits;
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(p.offsets + p.E) != p.R || __ldg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
@@ -148,19 +152,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
     int it_p = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int w = u / p.splits, split = u % p.splits;
+      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const int e = it.e, nt = it.nt, r0 = it.r0, ng = it.ng;
       const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
       {
         const uint32_t bytes = W_BYTES + WS_BYTES + ng * (A_BYTES + AS_BYTES);
-        for (int kc = 0; kc < KCH; ++kc) {
+        for (int kc = kc0; kc < kc1; ++kc) {
           if (!warp_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
             ok = false;
             break;
           }
           uint8_t* sb = smem + stage * STAGE_BYTES;
           if (lane == 0) W4A4_TRACE(0, it_p);
+          if (it_p == p.drop_stage) {
+            // fault injection (tests only): this stage is never armed, so the
+            // consumers' bounded waits run out and the kernel aborts cleanly
+            ++it_p;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           ew_arrive_expect_tx(&full_bar[stage], bytes);
           ew_tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
           ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * 4 * 512, WS_BYTES, &full_bar[stage], pol_w);
@@ -189,9 +205,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int w = u / p.splits, split = u % p.splits;
+      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       {
-        for (int kc = 0; kc < KCH; ++kc) {
+        for (int kc = kc0; kc < kc1; ++kc) {
           if (!warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
             ok = false;
             break;
@@ -227,7 +245,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int it_c = 0;
     const uint32_t smem_base = smem_u32(smem);
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int w = u / p.splits, split = u % p.splits;
+      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       const int ng = decode_item<TOK_PER_PASS>(w, s_base, NT, xr).ng;
       {
         const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
@@ -237,7 +257,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_col = tmem + acc * ACC_COLS;
-        for (int kc = 0; kc < KCH; ++kc) {
+        for (int kc = kc0; kc < kc1; ++kc) {
           // sf_ready is arrived after the scale warp saw full_bar; waiting on
           // both keeps the TMA completion directly observed by this warp
           if (!warp_wait(&sf_ready[stage], phase, &abort_flag, p.dev_status) ||
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ew_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
             // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
             ew_mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
-                            (kc | kk) != 0);
+                            (kc != kc0 || kk != 0));
           }
           ew_commit(&empty_bar[stage]);
           if (lane == 0) W4A4_TRACE(2, it_c);
@@ -287,7 +307,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     int it_e = 0;
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int w = u / p.splits, split = u % p.splits;
+      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const int r0 = it.r0, m1 = it.m1, ng = it.ng;
       const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
@@ -306,7 +328,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int tb = r0 + g * TG;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (tb + j < m1) p.out[(size_t)(tb + j) * p.N + n] = __fmul_rn(__uint_as_float(r[j]), alpha);
+            if (tb + j < m1) {
+              float* dst = p.out + (size_t)(tb + j) * p.N + n;
+              const float v = __fmul_rn(__uint_as_float(r[j]), alpha);
+              // two K halves: 0 + a + b == 0 + b + a, so the sum is the same in either order
+              if (p.splits == 1) *dst = v;
+              else atomicAdd(dst, v);
+            }
           }
         }
         tc_fence_before();
@@ -365,9 +393,19 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   p.N = N;
   p.K = K;
   p.R = R;
+  p.drop_stage = fault_injection_drop_stage();
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   // the number of work items depends on the routing, which lives on the
   // device: launch one persistent CTA per SM and let each find its items
+  // Split K in two when even the largest possible number of work items,
+  // tiles x (experts + R/128) passes, cannot fill every SM once.  Exactly two
+  // partial sums keep the result independent of their arrival order.
+  const long long max_items = (long long)(N / BM) * ((long long)E + (R + TOK_PER_PASS - 1) / TOK_PER_PASS);
+  p.splits = (max_items < num_sms() && (K / KC) >= 2) ? 2 : 1;
+  if (p.splits == 2) {
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
+    if (e != cudaSuccess) return e;
+  }
   gemm_w4a4_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, p);
   return cudaGetLastError();
 }

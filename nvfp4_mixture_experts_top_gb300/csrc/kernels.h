@@ -8,6 +8,13 @@ namespace nvfp4moe {
 
 int num_sms();  // SM count of the current device (cached)
 
+// Fault injection for the failure-detection tests: the value of the
+// environment variable NVFP4MOE_TEST_DROP_STAGE (read at every launch), or -1
+// when it is unset.  A grouped GEMM launched with it set never arms that
+// pipeline stage, so its bounded waits run out: it reports
+// NVFP4_E_DEVICE_TIMEOUT in dev_status, drains, frees TMEM and returns.
+int fault_injection_drop_stage();
+
 cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,
                             int dynamic, uint32_t* amax_ws, uint8_t* codes, uint8_t* scales, cudaStream_t st);
 cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st);

@@ -1,0 +1,55 @@
+"""Failure detection on the GPU without faulting it.
+
+The grouped GEMM's waits are bounded.  With the test-only fault injection
+(NVFP4MOE_TEST_DROP_STAGE: the producer never arms one pipeline stage) the
+consumers' waits run out: the kernel must report NVFP4_E_DEVICE_TIMEOUT in
+the status word, drain its copies and MMAs, free its tensor memory and
+return -- and the context must stay usable: the same GEMM right after gives
+the oracle's result.  Routing errors are reported the same way (status word,
+no trap): see test_gpu_gemm.py::test_gemm_bad_offsets_report_status.
+"""
+import os
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_close, cuda_or_skip, to_dev, upload_weights
+from nvfp4_mixture_experts_top_gb300 import binding as B
+from nvfp4_mixture_experts_top_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+NVFP4_E_DEVICE_TIMEOUT = 7
+
+
+def test_gemm_bounded_wait_times_out_and_context_survives(orc):
+    dev = cuda_or_skip()
+    E, N, K = 2, 128, 512
+    counts = [5, 3]
+    offs = np.array([0, 5, 8], np.int32)
+    w = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, N, K).numpy() for e in range(E)]))
+    a = wl.random_fp32((8, K), seed=1, tag="fail").to(torch.bfloat16).float().numpy()
+    ac, as_, aS = orc.quantize(a)
+    wd = upload_weights(w, E, N, K, dev)
+    args = (to_dev(ac, dev), to_dev(as_, dev), to_dev(np.array([aS]), dev), *wd, to_dev(offs, dev), N, K)
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    os.environ["NVFP4MOE_TEST_DROP_STAGE"] = "0"
+    try:
+        t0 = time.time()
+        B.moe_grouped_gemm_nvfp4(B.MOE_W4A4, *args, dev_status=status)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["NVFP4MOE_TEST_DROP_STAGE"]
+    assert int(status.item()) == NVFP4_E_DEVICE_TIMEOUT
+    assert elapsed < 30.0
+
+    status.zero_()
+    out = B.moe_grouped_gemm_nvfp4(B.MOE_W4A4, *args, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(out.cpu().numpy(), orc.grouped_gemm_w4a4(ac, as_, aS, w[0], w[1], w[2], offs), "after timeout")
+    assert sum(counts) == 8

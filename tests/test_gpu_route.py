@@ -71,3 +71,22 @@ def test_route_zero_tokens():
     dev = cuda_or_skip()
     out = B.moe_align_permute(torch.zeros(0, 16, device=dev), 2)
     assert not out["offsets"].cpu().numpy().any()
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_c16", "decode_b512", "wide"])
+def test_route_quantize_fused_matches_staged(orc, name):
+    """moe_route_quantize_nvfp4 (routing + quantisation straight into
+    permuted rows) gives exactly what nvfp4_quantize followed by
+    moe_align_permute's NVFP4 gather gives, and the oracle's S_x."""
+    dev = cuda_or_skip()
+    cfg = wl.CONFIGS[name]
+    logits = wl.router_logits(cfg, device=dev)
+    x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
+    fused = B.moe_route_quantize_nvfp4(x, logits, cfg.k)
+    codes, scales, S = B.nvfp4_quantize(x)
+    staged = B.moe_align_permute(logits, cfg.k, act=(codes, scales), act_kind=B.MOE_ACT_NVFP4)
+    torch.cuda.synchronize()
+    for key in ("ids", "w", "offsets", "perm", "inv", "act_codes", "act_scales"):
+        assert torch.equal(fused[key], staged[key]), key
+    assert torch.equal(fused["S_x"], S)
+    assert float(S.item()) == float(orc.tensor_scale(x.float().cpu().numpy()))
