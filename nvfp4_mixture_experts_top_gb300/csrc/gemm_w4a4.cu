@@ -23,10 +23,10 @@
 //
 // Operand layouts in shared memory (all K-major, 128-byte rows):
 //   weight codes   [128 rows][128 B]  TMA, 128-byte swizzle
-//   token codes    [32 rows][128 B]   per group, TMA, 128-byte swizzle; the ng
-//                                     group tiles form one [32*ng][128 B] tile
+//   token codes    [32*ng rows][128 B] TMA, 128-byte swizzle: one 32-row box
+//                                     for one group, one 128-row box otherwise
 //   weight scales  4 x 512-byte atoms (pre-packed, one bulk copy)
-//   token scales   [32 rows][16 B]    per group, TMA, no swizzle
+//   token scales   [32*ng rows][16 B]  TMA, no swizzle, boxes as for the codes
 // Block scales in TMEM: a 32-lane x 4-column patch per 128 rows (row r in lane
 // r % 32 of every lane quarter, column r / 32, byte = 16-element block within
 // the MMA's K=64), starting on a 4-column boundary for every MMA.  The token
@@ -91,7 +91,8 @@ struct Params {
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
-                     const __grid_constant__ CUtensorMap tm_as, const Params p) {
+                     const __grid_constant__ CUtensorMap tm_as, const __grid_constant__ CUtensorMap tm_a4,
+                     const __grid_constant__ CUtensorMap tm_as4, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t sf_ready[STAGES];
@@ -124,6 +125,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_as);
+    prefetch_tmap(&tm_a4);
+    prefetch_tmap(&tm_as4);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, TMEM_COLS);
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int e = it.e, nt = it.nt, r0 = it.r0, ng = it.ng;
       const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
       {
-        const uint32_t bytes = W_BYTES + WS_BYTES + ng * (A_BYTES + AS_BYTES);
+        const uint32_t bytes = W_BYTES + WS_BYTES + (ng == 1 ? 1 : MAXG) * (A_BYTES + AS_BYTES);
         for (int kc = kc0; kc < kc1; ++kc) {
           if (!warp_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
             ok = false;
@@ -180,9 +183,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ew_arrive_expect_tx(&full_bar[stage], bytes);
           ew_tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
           ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * 4 * 512, WS_BYTES, &full_bar[stage], pol_w);
-          for (int g = 0; g < ng; ++g) {
-            ew_tma_load_2d(sb + OFF_A + g * A_BYTES, &tm_a, &full_bar[stage], kc * (KC / 2), r0 + g * TG, pol_a);
-            ew_tma_load_2d(sb + OFF_AS + g * AS_BYTES, &tm_as, &full_bar[stage], kc * (KC / 16), r0 + g * TG, pol_a);
+          // one copy per operand whatever the token count: a 32-row box for a
+          // single group, a 128-row box (all groups) otherwise -- TMA issue
+          // costs ~100 cycles per copy, so per-group copies would bound the
+          // stage rate of many-token passes
+          if (ng == 1) {
+            ew_tma_load_2d(sb + OFF_A, &tm_a, &full_bar[stage], kc * (KC / 2), r0, pol_a);
+            ew_tma_load_2d(sb + OFF_AS, &tm_as, &full_bar[stage], kc * (KC / 16), r0, pol_a);
+          } else {
+            ew_tma_load_2d(sb + OFF_A, &tm_a4, &full_bar[stage], kc * (KC / 2), r0, pol_a);
+            ew_tma_load_2d(sb + OFF_AS, &tm_as4, &full_bar[stage], kc * (KC / 16), r0, pol_a);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -371,7 +381,7 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap tm_w, tm_a, tm_as;
+  CUtensorMap tm_w, tm_a, tm_as, tm_a4, tm_as4;
   cudaError_t err;
   // weight codes: [E*N rows, K/2 bytes], box 128 B x 128 rows, 128-byte swizzle
   err = make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, 128);
@@ -381,6 +391,11 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   if (err != cudaSuccess) return err;
   // token scales: [R rows, K/16 bytes], box 16 B x 32 rows, no swizzle
   err = make_tmap_2d_u8(&tm_as, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TG, 0);
+  if (err != cudaSuccess) return err;
+  // the same two tensors with 128-row boxes (all token groups of a pass)
+  err = make_tmap_2d_u8(&tm_a4, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TOK_PER_PASS, 128);
+  if (err != cudaSuccess) return err;
+  err = make_tmap_2d_u8(&tm_as4, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TOK_PER_PASS, 0);
   if (err != cudaSuccess) return err;
   Params p;
   p.w_scales = w_scales_packed;
@@ -406,7 +421,7 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
-  gemm_w4a4_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, p);
+  gemm_w4a4_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4, p);
   return cudaGetLastError();
 }
 
