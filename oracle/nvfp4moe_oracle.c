@@ -18,6 +18,9 @@
  *    (a, b, block_scale_a, block_scale_b, alpha) -- i.e. per-block scales on
  *    both operands plus one per-tensor coefficient; section "The Investigation
  *    So Far": routed top-8 of 256 experts, ~16 tokens per expert.
+ *  - "The Benchmark That Confirmed the Ceiling: NVFP4 Cutlass on sm_120",
+ *    sections "Introduction" and "The NVFP4 Pivot": the stock checkpoint is
+ *    MXFP4 -- group-32 blocks with UE8M0 (power-of-two) scales.
  *  - "The 24% Ceiling: Diagnosing the Limits of NVFP4 Quantization on
  *    Blackwell SM120 GPUs", section "The Core Insight": W4A16 keeps the
  *    activations in BF16, W4A4 quantises them to FP4 as well.
@@ -38,6 +41,12 @@
  *    block decode scale gives scale code 0 and element code 0.
  *  - Packing: two E2M1 codes per byte, element 2i in the low nibble; block
  *    scales stored linearly as [rows, cols/16].
+ *  - MXFP4 (the group-32, UE8M0 format the pages name as the stock
+ *    checkpoint's): the OCP MX conversion -- shared exponent
+ *    floor(log2(amax_block)) - 2 (E2M1's largest magnitude is 1.5 * 2^2),
+ *    clamped to the UE8M0 range, elements E2M1(RNE, satfinite) of x / 2^E;
+ *    an all-zero block takes the smallest scale.  No per-tensor scale.
+ *    Scales stored linearly as [rows, cols/32].
  *  - Router: top-k by logit, ties to the lower expert id, descending order;
  *    weights = softmax over the k selected logits (fp64 here).
  *  - Permutation: stable by (expert, token).
@@ -229,6 +238,79 @@ void orc_dequantize(const uint8_t* codes, const uint8_t* scales, float S, int64_
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP4 quantisation (OCP MX: E2M1 elements, one UE8M0 scale per 32)      */
+/* ------------------------------------------------------------------------ */
+
+/* UE8M0 decode: an unsigned 8-bit exponent, value 2^(code - 127); code 0xFF
+ * is NaN. */
+double orc_ue8m0_value(int code) {
+  code &= 0xFF;
+  if (code == 0xFF) return NAN;
+  return ldexp(1.0, code - 127);
+}
+
+/* Quantise one 32-element block to MXFP4.  The shared exponent is
+ * E = floor(log2(amax)) - 2, where 2 is the exponent of E2M1's largest
+ * magnitude (6 = 1.5 * 2^2); E is clamped to the UE8M0 range [-127, 127],
+ * and an all-zero block takes E = -127.  Scale code = E + 127.  Element
+ * code = E2M1(RNE, satfinite, sign kept) of q = x / 2^E, where q is the fp32
+ * value nearest the exact quotient (a power-of-two scaling: exact unless q is
+ * subnormal).  Magnitudes in [6, 8) * 2^E saturate to 6. */
+void orc_mx_quantize_block(const float* xb, uint8_t* scode, uint8_t* ecodes) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; ++i) {
+    float a = f32_abs(xb[i]);
+    if (a > amax) amax = a;
+  }
+  int E;
+  if (amax == 0.0f) {
+    E = -127;
+  } else {
+    int p;
+    frexp((double)amax, &p); /* amax = m * 2^p, m in [0.5, 1): floor(log2 amax) = p - 1 */
+    E = (p - 1) - 2;
+  }
+  if (E < -127) E = -127;
+  if (E > 127) E = 127;
+  *scode = (uint8_t)(E + 127);
+  for (int i = 0; i < 32; ++i) {
+    float q = (float)ldexp((double)xb[i], -E); /* exact in fp64, one rounding to fp32 */
+    ecodes[i] = (uint8_t)orc_e2m1_encode(q);
+  }
+}
+
+/* Quantise x [rows, cols] (row stride ld) to MXFP4: codes [rows, cols/2]
+ * (low nibble = even element), scales [rows, cols/32].  cols must be a
+ * multiple of 32. */
+void orc_mx_quantize(const float* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes, uint8_t* scales) {
+  int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      uint8_t ec[32];
+      uint8_t sc;
+      orc_mx_quantize_block(x + r * ld + b * 32, &sc, ec);
+      scales[r * nb + b] = sc;
+      for (int i = 0; i < 16; ++i)
+        codes[r * (cols / 2) + b * 16 + i] = (uint8_t)(ec[2 * i] | (ec[2 * i + 1] << 4));
+    }
+  }
+}
+
+/* Decoded MXFP4 element (r, c): e2m1(code) * 2^(scale - 127).  Exact in
+ * fp64. */
+static double dec_elem_mx(const uint8_t* codes, const uint8_t* scales, int64_t cols, int64_t r, int64_t c) {
+  uint8_t byte = codes[r * (cols / 2) + c / 2];
+  int code = (c & 1) ? (byte >> 4) : (byte & 15);
+  return orc_e2m1_value(code) * orc_ue8m0_value(scales[r * (cols / 32) + c / 32]);
+}
+
+void orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols, double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) out[r * cols + c] = dec_elem_mx(codes, scales, cols, r, c);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Router and permutation                                                   */
 /* ------------------------------------------------------------------------ */
 
@@ -333,6 +415,35 @@ void orc_grouped_gemm_w4a16(const float* a, const uint8_t* w_codes, const uint8_
   }
 }
 
+/* MXFP4 x MXFP4: out[r, n] = sum_k dec(a[r,k]) * dec(w[e(r), n, k]), fp64
+ * accumulation, no per-tensor coefficient.  a: codes [R, K/2], scales
+ * [R, K/32]; w: codes [E, N, K/2], scales [E, N, K/32]; out fp64 [R, N]. */
+void orc_grouped_gemm_mx(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
+                         const uint8_t* w_scales, const int32_t* offsets, int E, int N, int K, double* out) {
+  int R = offsets[E];
+  double* adq = (double*)malloc(sizeof(double) * (size_t)R * (size_t)K);
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t c = 0; c < K; ++c) adq[r * K + c] = dec_elem_mx(a_codes, a_scales, K, r, c);
+  for (int e = 0; e < E; ++e) {
+    int r0 = offsets[e], r1 = offsets[e + 1];
+    if (r1 <= r0) continue;
+    const uint8_t* wc = w_codes + (int64_t)e * N * (K / 2);
+    const uint8_t* ws = w_scales + (int64_t)e * N * (K / 32);
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+      double* wrow = (double*)malloc(sizeof(double) * (size_t)K);
+      for (int64_t c = 0; c < K; ++c) wrow[c] = dec_elem_mx(wc, ws, K, n, c);
+      for (int r = r0; r < r1; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < K; ++c) acc += adq[(int64_t)r * K + c] * wrow[c];
+        out[(int64_t)r * N + n] = acc;
+      }
+      free(wrow);
+    }
+  }
+  free(adq);
+}
+
 /* ------------------------------------------------------------------------ */
 /* SwiGLU, requantisation, combine                                          */
 /* ------------------------------------------------------------------------ */
@@ -367,7 +478,11 @@ void orc_combine(const float* Y, const int32_t* inv, const double* w, int T, int
  *   gate_up grouped GEMM (G stored fp32) -> SwiGLU (h stored fp32) ->
  *   (W4A4: requantise h with the static S_h | W4A16: round h to bf16) ->
  *   down grouped GEMM (Y stored fp32) -> weighted combine (out fp64).
- * mode 0 = W4A4, 1 = W4A16.  x is [T, H] (bf16 values widened to fp32).
+ * mode 0 = W4A4, 1 = W4A16, 2 = MXFP4 weights and activations (x quantised
+ * and h requantised per 32-element block with UE8M0 scales; the per-tensor
+ * scales w13_S, w2_S, S_h and S_x do not exist in this format and are not
+ * read; hq_scales_o then holds R * I/32 bytes).
+ * x is [T, H] (bf16 values widened to fp32).
  * S_x_in: NULL = the dynamic per-tensor scale of these T rows; otherwise the
  * scale of a larger tensor these rows were taken from (to check a sample of
  * tokens of a big batch, the scale must be the whole batch's).
@@ -394,7 +509,19 @@ void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, 
   orc_route(logits, T, E, k, ids, w);
   orc_permute(ids, T, E, k, offsets, perm, inv);
 
-  if (mode == 0) {
+  if (mode == 2) {
+    uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
+    uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 32);
+    uint8_t* ac = (uint8_t*)malloc((size_t)R * H / 2);
+    uint8_t* as = (uint8_t*)malloc((size_t)R * H / 32);
+    orc_mx_quantize(x, T, H, H, xc, xs);
+    for (int r = 0; r < R; ++r) {
+      memcpy(ac + (int64_t)r * H / 2, xc + (int64_t)perm[r] * H / 2, (size_t)H / 2);
+      memcpy(as + (int64_t)r * H / 32, xs + (int64_t)perm[r] * H / 32, (size_t)H / 32);
+    }
+    orc_grouped_gemm_mx(ac, as, w13_codes, w13_scales, offsets, E, 2 * I, H, G64);
+    free(xc); free(xs); free(ac); free(as);
+  } else if (mode == 0) {
     uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
     uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 16);
     uint8_t* ac = (uint8_t*)malloc((size_t)R * H / 2);
@@ -417,7 +544,15 @@ void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, 
   orc_swiglu(G32, R, I, h64);
   for (int64_t i = 0; i < (int64_t)R * I; ++i) h32[i] = (float)h64[i];
 
-  if (mode == 0) {
+  if (mode == 2) {
+    uint8_t* hc = (uint8_t*)malloc((size_t)R * I / 2);
+    uint8_t* hs = (uint8_t*)malloc((size_t)R * I / 32);
+    orc_mx_quantize(h32, R, I, I, hc, hs);
+    orc_grouped_gemm_mx(hc, hs, w2_codes, w2_scales, offsets, E, H, I, Y64);
+    if (hq_codes_o) memcpy(hq_codes_o, hc, (size_t)R * I / 2);
+    if (hq_scales_o) memcpy(hq_scales_o, hs, (size_t)R * I / 32);
+    free(hc); free(hs);
+  } else if (mode == 0) {
     uint8_t* hc = (uint8_t*)malloc((size_t)R * I / 2);
     uint8_t* hs = (uint8_t*)malloc((size_t)R * I / 16);
     float sh = S_h;
@@ -458,7 +593,13 @@ void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, i
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
   orc_route(logits, T, E, k, ids, w);
   double* xd = (double*)malloc(sizeof(double) * (size_t)T * H);
-  if (mode == 0) {
+  if (mode == 2) {
+    uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
+    uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 32);
+    orc_mx_quantize(x, T, H, H, xc, xs);
+    orc_mx_dequantize(xc, xs, T, H, xd);
+    free(xc); free(xs);
+  } else if (mode == 0) {
     uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
     uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 16);
     float S_x = S_x_in ? *S_x_in : 0.0f;
@@ -475,21 +616,34 @@ void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, i
     double* hd = (double*)malloc(sizeof(double) * (size_t)I);
     for (int j = 0; j < k; ++j) {
       int e = ids[t * k + j];
+      const int mx = mode == 2;
+      const int sb = mx ? 32 : 16; /* elements per block scale */
       const uint8_t* c13 = w13_codes + (int64_t)e * 2 * I * (H / 2);
-      const uint8_t* s13 = w13_scales + (int64_t)e * 2 * I * (H / 16);
+      const uint8_t* s13 = w13_scales + (int64_t)e * 2 * I * (H / sb);
       const uint8_t* c2 = w2_codes + (int64_t)e * H * (I / 2);
-      const uint8_t* s2 = w2_scales + (int64_t)e * H * (I / 16);
+      const uint8_t* s2 = w2_scales + (int64_t)e * H * (I / sb);
+      const double S13 = mx ? 1.0 : (double)w13_S[e];
+      const double S2 = mx ? 1.0 : (double)w2_S[e];
       for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int c = 0; c < H; ++c) {
-          g += xd[(int64_t)t * H + c] * dec_elem(c13, s13, H, i, c) * (double)w13_S[e];
-          u += xd[(int64_t)t * H + c] * dec_elem(c13, s13, H, I + i, c) * (double)w13_S[e];
+          const double wg = mx ? dec_elem_mx(c13, s13, H, i, c) : dec_elem(c13, s13, H, i, c);
+          const double wu = mx ? dec_elem_mx(c13, s13, H, I + i, c) : dec_elem(c13, s13, H, I + i, c);
+          g += xd[(int64_t)t * H + c] * wg * S13;
+          u += xd[(int64_t)t * H + c] * wu * S13;
         }
         float g32 = (float)g, u32 = (float)u;
         double hv = (double)g32 / (1.0 + exp(-(double)g32)) * (double)u32;
         h32[i] = (float)hv;
       }
-      if (mode == 0) {
+      if (mx) {
+        uint8_t hsc;
+        uint8_t ec[32];
+        for (int b = 0; b < I / 32; ++b) {
+          orc_mx_quantize_block(h32 + b * 32, &hsc, ec);
+          for (int q = 0; q < 32; ++q) hd[b * 32 + q] = orc_e2m1_value(ec[q]) * orc_ue8m0_value(hsc);
+        }
+      } else if (mode == 0) {
         uint8_t hsc;
         uint8_t ec[16];
         for (int b = 0; b < I / 16; ++b) {
@@ -502,7 +656,7 @@ void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, i
       }
       for (int n = 0; n < H; ++n) {
         double y = 0.0;
-        for (int i = 0; i < I; ++i) y += hd[i] * dec_elem(c2, s2, I, n, i) * (double)w2_S[e];
+        for (int i = 0; i < I; ++i) y += hd[i] * (mx ? dec_elem_mx(c2, s2, I, n, i) : dec_elem(c2, s2, I, n, i)) * S2;
         float y32 = (float)y;
         out[(int64_t)t * H + n] += w[t * k + j] * (double)y32;
       }

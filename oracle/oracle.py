@@ -65,6 +65,16 @@ def _declare(L):
     L.orc_moe_layer_naive.argtypes = layer_args
     L.orc_num_threads.restype = C.c_int
     L.orc_num_threads.argtypes = []
+    L.orc_ue8m0_value.restype = C.c_double
+    L.orc_ue8m0_value.argtypes = [C.c_int]
+    L.orc_mx_quantize_block.restype = None
+    L.orc_mx_quantize_block.argtypes = [_P, _P, _P]
+    L.orc_mx_quantize.restype = None
+    L.orc_mx_quantize.argtypes = [_P, _I64, _I64, _I64, _P, _P]
+    L.orc_mx_dequantize.restype = None
+    L.orc_mx_dequantize.argtypes = [_P, _P, _I64, _I64, _P]
+    L.orc_grouped_gemm_mx.restype = None
+    L.orc_grouped_gemm_mx.argtypes = [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, _P]
 
 
 def _c(a, dtype):
@@ -98,6 +108,10 @@ def e2m1_encode(q: float) -> int:
 
 def round_bf16(v: float) -> float:
     return float(lib().orc_round_bf16(float(np.float32(v))))
+
+
+def ue8m0_value(code: int) -> float:
+    return lib().orc_ue8m0_value(int(code))
 
 
 def num_threads() -> int:
@@ -145,6 +159,49 @@ def dequantize(codes, scales, S, cols):
     out = np.zeros((rows, cols), np.float64)
     lib().orc_dequantize(_p(codes), _p(scales), float(np.float32(S)), rows, cols, _p(out))
     return out
+
+
+def mx_quantize(x):
+    """MXFP4-quantise x [rows, cols] (cols a multiple of 32).  Returns
+    (codes uint8 [rows, cols/2], scales uint8 [rows, cols/32])."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 32), np.uint8)
+    lib().orc_mx_quantize(_p(x), rows, cols, cols, _p(codes), _p(scales))
+    return codes, scales
+
+
+def mx_quantize_block(xb):
+    xb = _c(xb, np.float32)
+    assert xb.shape == (32,)
+    sc = np.zeros(1, np.uint8)
+    ec = np.zeros(32, np.uint8)
+    lib().orc_mx_quantize_block(_p(xb), _p(sc), _p(ec))
+    return int(sc[0]), ec
+
+
+def mx_dequantize(codes, scales, cols):
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    rows = codes.shape[0]
+    out = np.zeros((rows, cols), np.float64)
+    lib().orc_mx_dequantize(_p(codes), _p(scales), rows, cols, _p(out))
+    return out
+
+
+def mx_quantize_experts(w):
+    """MXFP4-quantise a stack of expert weight matrices w [E, N, K].  Returns
+    (codes [E, N, K/2], scales [E, N, K/32], None) -- the format has no
+    per-tensor scale."""
+    w = np.asarray(w, np.float32)
+    E, N, K = w.shape
+    codes = np.zeros((E, N, K // 2), np.uint8)
+    scales = np.zeros((E, N, K // 32), np.uint8)
+    for e in range(E):
+        codes[e], scales[e] = mx_quantize(w[e])
+    return codes, scales, None
 
 
 def route(logits, k):
@@ -196,6 +253,20 @@ def grouped_gemm_w4a16(a, w_codes, w_scales, w_S, offsets):
     return out
 
 
+def grouped_gemm_mx(a_codes, a_scales, w_codes, w_scales, offsets):
+    a_codes = _c(a_codes, np.uint8)
+    a_scales = _c(a_scales, np.uint8)
+    w_codes = _c(w_codes, np.uint8)
+    w_scales = _c(w_scales, np.uint8)
+    offsets = _c(offsets, np.int32)
+    E, N, Kh = w_codes.shape
+    K = 2 * Kh
+    R = int(offsets[E])
+    out = np.zeros((R, N), np.float64)
+    lib().orc_grouped_gemm_mx(_p(a_codes), _p(a_scales), _p(w_codes), _p(w_scales), _p(offsets), E, N, K, _p(out))
+    return out
+
+
 def swiglu(G):
     G = _c(G, np.float32)
     R, I2 = G.shape
@@ -215,12 +286,26 @@ def combine(Y, inv, w):
     return out
 
 
+_MODES = {"w4a4": 0, "w4a16": 1, "mxw4a4": 2}
+
+
+def _weights(w13, w2):
+    """Contiguous (codes, scales, S) of both projections; a missing S (MXFP4)
+    becomes ones, which the oracle does not read in that mode."""
+    def one(w):
+        c = _c(w[0], np.uint8)
+        S = np.ones(c.shape[0], np.float32) if w[2] is None else _c(w[2], np.float32)
+        return c, _c(w[1], np.uint8), S
+    return one(w13) + one(w2)
+
+
 def _sx(S_x):
     return None if S_x is None else np.array([S_x], np.float32)
 
 
 def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False, S_x=None):
-    """Full layer.  mode: 'w4a4' | 'w4a16'.  w13 / w2: (codes, scales, S[E]).
+    """Full layer.  mode: 'w4a4' | 'w4a16' | 'mxw4a4'.  w13 / w2: (codes, scales,
+    S[E]); for 'mxw4a4' the scales are UE8M0 per 32 and S is None.
     S_x: None = dynamic activation scale of x; else the given scale (for a
     sample of rows of a larger batch).  Returns out fp64 [T, H] (and a dict
     of intermediates if asked)."""
@@ -228,12 +313,11 @@ def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False, S_x=None):
     logits = _c(logits, np.float32)
     T, H = x.shape
     E = logits.shape[1]
-    c13, s13, S13 = (_c(w13[0], np.uint8), _c(w13[1], np.uint8), _c(w13[2], np.float32))
-    c2, s2, S2 = (_c(w2[0], np.uint8), _c(w2[1], np.uint8), _c(w2[2], np.float32))
+    c13, s13, S13, c2, s2, S2 = _weights(w13, w2)
     I = c2.shape[2] * 2
     R = T * k
     out = np.zeros((T, H), np.float64)
-    m = 0 if mode == "w4a4" else 1
+    m = _MODES[mode]
     ids = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float64)
     offsets = np.zeros(E + 1, np.int32)
@@ -241,7 +325,7 @@ def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False, S_x=None):
     inv = np.zeros(R, np.int32)
     S_x_out = np.zeros(1, np.float32)
     hq_c = np.zeros((R, I // 2), np.uint8)
-    hq_s = np.zeros((R, I // 16), np.uint8)
+    hq_s = np.zeros((R, I // (32 if m == 2 else 16)), np.uint8)
     h32 = np.zeros((R, I), np.float32)
     sx = _sx(S_x)
     lib().orc_moe_layer(m, _p(x), _p(logits), T, H, I, E, k, _p(c13), _p(s13), _p(S13), _p(c2), _p(s2), _p(S2),
@@ -258,11 +342,10 @@ def moe_layer_naive(mode, x, logits, k, w13, w2, S_h, S_x=None):
     logits = _c(logits, np.float32)
     T, H = x.shape
     E = logits.shape[1]
-    c13, s13, S13 = (_c(w13[0], np.uint8), _c(w13[1], np.uint8), _c(w13[2], np.float32))
-    c2, s2, S2 = (_c(w2[0], np.uint8), _c(w2[1], np.uint8), _c(w2[2], np.float32))
+    c13, s13, S13, c2, s2, S2 = _weights(w13, w2)
     I = c2.shape[2] * 2
     out = np.zeros((T, H), np.float64)
-    m = 0 if mode == "w4a4" else 1
+    m = _MODES[mode]
     sx = _sx(S_x)
     lib().orc_moe_layer_naive(m, _p(x), _p(logits), T, H, I, E, k, _p(c13), _p(s13), _p(S13), _p(c2), _p(s2),
                               _p(S2), float(np.float32(S_h)), _p(sx), _p(out))
