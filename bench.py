@@ -1,7 +1,7 @@
 """Benchmark of the NVFP4 MoE layer (decode) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_c16|decode_b512|wide] [--mode w4a4|w4a16]
+                    [--workload decode_c16|decode_b512|wide] [--mode w4a4|w4a16|mxw4a4]
 
 Prints ONE JSON line (rank 0).  A step is one full MoE layer forward over the
 workload's batch: quantise -> route/permute/gather -> gate_up grouped GEMM ->
@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WEIGHT_BYTES_PER_ELEM = 0.5 + 1.0 / 16  # E2M1 codes + one E4M3 scale per 16
+MX_WEIGHT_BYTES_PER_ELEM = 0.5 + 1.0 / 32  # MXFP4: E2M1 codes + one UE8M0 scale per 32
 
 
 def _load_peaks():
@@ -108,7 +109,7 @@ def _kernel_hash(mode="w4a4"):
     """Hash of the sources of the dominant kernel of a mode (staleness check
     of the committed DRAM-traffic figure)."""
     h = hashlib.sha256()
-    for fn in ("gemm_%s.cu" % mode, "common.cuh"):
+    for fn in ("gemm_%s.cu" % ("w4a4" if mode == "mxw4a4" else mode), "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -128,8 +129,10 @@ def _traffic(workload, mode):
     return e.get("dram_bytes_per_launch")
 
 
-def gpu_weights(cfg, dev, B, wl, seed=0):
+def gpu_weights(cfg, dev, B, wl, seed=0, mx=False):
     import torch
+    if mx:
+        return gpu_mx_weights(cfg, dev, B, wl, seed)
     out = []
     for which, N, K in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
         codes = torch.empty(cfg.E, N, K // 2, dtype=torch.uint8, device=dev)
@@ -146,6 +149,23 @@ def gpu_weights(cfg, dev, B, wl, seed=0):
     return out
 
 
+def gpu_mx_weights(cfg, dev, B, wl, seed=0):
+    import torch
+    out = []
+    for which, N, K in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
+        codes = torch.empty(cfg.E, N, K // 2, dtype=torch.uint8, device=dev)
+        lin = torch.empty(cfg.E, N, K // 32, dtype=torch.uint8, device=dev)
+        for e in range(cfg.E):
+            wf = wl.expert_weight_fp32(which, e, N, K, seed, device=dev)
+            _, s = B.mxfp4_quantize(wf, codes=codes[e])
+            lin[e].copy_(s[:, : K // 32])
+        del wf
+        packed = B.mxfp4_pack_weight_scales(lin, cfg.E, N, K)
+        del lin
+        out.append((codes, packed, None))
+    return out
+
+
 def oracle_sample(cfg, mode, ntok, seed=0):
     """Prepare the oracle's inputs for the first `ntok` tokens of the
     workload (weights of the experts they use, quantised by the oracle; the
@@ -158,10 +178,9 @@ def oracle_sample(cfg, mode, ntok, seed=0):
     toks = list(range(ntok))
     ids, _ = orc.route(logits[toks], cfg.k)
     used = np.unique(ids)
-    w13 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed).numpy()
-                                         for e in used]))
-    w2 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed).numpy()
-                                        for e in used]))
+    q = orc.mx_quantize_experts if mode == "mxw4a4" else orc.quantize_experts
+    w13 = q(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed).numpy() for e in used]))
+    w2 = q(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed).numpy() for e in used]))
     S_x = orc.tensor_scale(x) if mode == "w4a4" else None
     xs, ls = x[toks], logits[toks][:, used]
 
@@ -302,7 +321,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_c16",
                     choices=["decode_c16", "decode_b512", "wide", "tiny", "gemm_sweep"])
-    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16"])
+    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16", "mxw4a4"])
     ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
     ap.add_argument("--baseline-tokens", type=int, default=4, help="tokens of the in-run CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -318,7 +337,8 @@ def main():
     cfg = wl.CONFIGS[args.workload]
     if args.experts:
         cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)
-    metric = "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name)
+    metric = ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if args.mode == "mxw4a4"
+              else "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name))
     unit = "tokens/s"
     if args.impl == "reference":
         return run_reference(args, cfg, metric, unit)
@@ -334,9 +354,11 @@ def main():
     torch.cuda.set_device(dev)
     B.load()
     B.nvfp4_device_check()
-    mode = B.MOE_W4A4 if args.mode == "w4a4" else B.MOE_W4A16
+    mode = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4}[args.mode]
+    mx = mode == B.MOE_MXW4A4
+    bpe = MX_WEIGHT_BYTES_PER_ELEM if mx else WEIGHT_BYTES_PER_ELEM
 
-    (w13, w2) = gpu_weights(cfg, dev, B, wl)
+    (w13, w2) = gpu_weights(cfg, dev, B, wl, mx=mx)
     x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
     logits = wl.router_logits(cfg, device=dev)
     S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
@@ -353,11 +375,11 @@ def main():
     perm = torch.empty(R, dtype=torch.int32, device=dev)
     inv = torch.empty(R, dtype=torch.int32, device=dev)
     a_c = torch.empty(R, H // 2, dtype=torch.uint8, device=dev)
-    a_s = torch.empty(R, H // 16, dtype=torch.uint8, device=dev)
+    a_s = torch.empty(R, B.mxfp4_scale_pitch(H) if mx else H // 16, dtype=torch.uint8, device=dev)
     a_b = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
     G = torch.empty(R, 2 * I, dtype=torch.float32, device=dev)
     h_c = torch.empty(R, I // 2, dtype=torch.uint8, device=dev)
-    h_s = torch.empty(R, I // 16, dtype=torch.uint8, device=dev)
+    h_s = torch.empty(R, B.mxfp4_scale_pitch(I) if mx else I // 16, dtype=torch.uint8, device=dev)
     h_b = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
     Y = torch.empty(R, H, dtype=torch.float32, device=dev)
     out = torch.empty(T, H, dtype=torch.float32, device=dev)
@@ -370,7 +392,20 @@ def main():
 
     def step(ev_pair=None):
         st = torch.cuda.current_stream().cuda_stream
-        if mode == B.MOE_W4A4:
+        if mx:
+            # routing + MXFP4 quantisation straight into permuted rows
+            chk(L.moe_route_quantize_mxfp4(P(x), P(logits), T, H, cfg.E, k, P(ids), P(tw), P(offs), P(perm),
+                                           P(inv), P(a_c), P(a_s), P(status), P(ws_route), ws_route.numel(), st))
+            if ev_pair:
+                ev_pair[0].record()
+            chk(L.moe_grouped_gemm_nvfp4(2, P(a_c), P(a_s), None, P(w13[0]), P(w13[1]), None, P(offs),
+                                         cfg.E, 2 * I, H, R, P(G), P(status), st))
+            if ev_pair:
+                ev_pair[1].record()
+            chk(L.moe_swiglu_requant(P(G), R, I, 2, None, P(h_c), P(h_s), None, st))
+            chk(L.moe_grouped_gemm_nvfp4(2, P(h_c), P(h_s), None, P(w2[0]), P(w2[1]), None, P(offs),
+                                         cfg.E, H, I, R, P(Y), P(status), st))
+        elif mode == B.MOE_W4A4:
             # routing + activation quantisation straight into permuted rows
             # (the kernels moe_layer_forward runs)
             chk(L.moe_route_quantize_nvfp4(P(x), P(logits), T, H, cfg.E, k, P(ids), P(tw), P(offs), P(perm),
@@ -418,9 +453,9 @@ def main():
     # touched experts -> algorithmic bytes
     counts = np.diff(offs.cpu().numpy())
     touched = int((counts > 0).sum())
-    w13_bytes = touched * 2 * I * H * WEIGHT_BYTES_PER_ELEM
-    w2_bytes = touched * H * I * WEIGHT_BYTES_PER_ELEM
-    act_in = R * H * (WEIGHT_BYTES_PER_ELEM if mode == B.MOE_W4A4 else 2.0)
+    w13_bytes = touched * 2 * I * H * bpe
+    w2_bytes = touched * H * I * bpe
+    act_in = R * H * (2.0 if mode == B.MOE_W4A16 else bpe)
     gemm1_bytes = w13_bytes + act_in + R * 2 * I * 4
     layer_weight_bytes = w13_bytes + w2_bytes
 
@@ -508,7 +543,8 @@ def main():
     result = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp4(e2m1)xfp4, fp32 accumulate" if mode == B.MOE_W4A4 else "fp4(e2m1)xbf16, fp32 accumulate",
+        "dtype": {B.MOE_W4A4: "fp4(e2m1)xfp4, fp32 accumulate", B.MOE_W4A16: "fp4(e2m1)xbf16, fp32 accumulate",
+                  B.MOE_MXW4A4: "fp4(e2m1)xfp4 (UE8M0 scales), fp32 accumulate"}[mode],
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised on the GPU)",
         "config": {"workload": cfg.name, "mode": args.mode, "T": T, "hidden": H, "intermediate": I,
                    "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,

@@ -61,7 +61,7 @@ typedef enum nvfp4_status {
 
 enum { NVFP4_DT_BF16 = 0, NVFP4_DT_F32 = 1 };
 enum { NVFP4_SCALE_STATIC = 0, NVFP4_SCALE_DYNAMIC = 1 };
-enum { MOE_W4A4 = 0, MOE_W4A16 = 1 };
+enum { MOE_W4A4 = 0, MOE_W4A16 = 1, MOE_MXW4A4 = 2 };
 enum { MOE_ACT_NONE = 0, MOE_ACT_NVFP4 = 1, MOE_ACT_BF16 = 2 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -112,6 +112,42 @@ int nvfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, 
                              nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * MXFP4 -- the group-32 format with UE8M0 (power-of-two) block scales that
+ * "The Benchmark That Confirmed the Ceiling", sections "Introduction" and
+ * "The NVFP4 Pivot", names as the stock checkpoint's.  The pages define only
+ * the block size and the scale type; the conversion follows the OCP MX rule:
+ *   per 32-element block: E = floor(log2(amax)) - 2, clamped to [-127, 127]
+ *   (an all-zero block takes -127); scale code E + 127 (UE8M0, value
+ *   2^(code-127)); element code = E2M1(RNE, satfinite, sign kept) of
+ *   x * 2^-E.  No per-tensor scale.
+ * Layouts: codes as NVFP4 (two per byte, element 2i in the low nibble);
+ * activation scales [rows, mxfp4_scale_pitch(cols)] bytes, the row pitch
+ * being cols/32 rounded up to a multiple of 16 (padding written as zero) so
+ * that the grouped GEMM can fetch them with TMA.
+ * Mode MOE_MXW4A4 of the grouped GEMM, SwiGLU/requant and layer calls runs
+ * both operands in MXFP4 on tcgen05.mma kind::mxf4nvf4 .scale_vec::2X.
+ * ------------------------------------------------------------------------ */
+int64_t mxfp4_scale_pitch(int64_t cols);
+
+/* mxfp4_quantize -- x [rows, cols] (bf16 or fp32, row stride ld_x elements)
+ * to codes [rows, cols/2] and scales [rows, mxfp4_scale_pitch(cols)].
+ * Constraints: cols % 32 == 0; ld_x >= cols, ld_x % 8 == 0 (bf16) or % 4 == 0
+ * (fp32); x and codes 16-byte aligned. */
+int mxfp4_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* codes,
+                   uint8_t* scales, nvfp4_stream_t stream);
+
+/* mxfp4_pack_weight_scales -- one-time reshuffle of MXFP4 expert weight
+ * scales from the linear layout [E, N, K/32] into the layout the grouped
+ * GEMM reads (weight preparation, no counterpart on the pages).  For expert
+ * e, 128-row tile nt = n / 128 and 64-column block kb = k / 64, a 256-byte
+ * block at ((e*N/128 + nt)*K/64 + kb)*256; inside it, row r = n % 128 and
+ * scale j = (k % 64) / 32 sit at byte (r % 32) * 8 + (r / 32) * 2 + j.
+ *   scales_linear  [E, N, K/32];  scales_packed  out, E*N*K/32 bytes.
+ * Constraints: N % 128 == 0, K % 256 == 0. */
+int mxfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, uint8_t* scales_packed,
+                             nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_align_permute -- router top-k plus the expert permutation.
  * Routing: "The 2x Gap", section "The Investigation So Far" (top-8 of 256
  * experts); "Native FP4 Is Slower ...", section 1 (22 of 512).  Per token t:
@@ -156,6 +192,16 @@ int moe_route_quantize_nvfp4(const void* x, const float* logits, int T, int H, i
                              uint8_t* a_codes, uint8_t* a_scales, int32_t* dev_status, void* workspace,
                              size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* moe_route_quantize_mxfp4 -- the same front half for MOE_MXW4A4: routing
+ * and permutation as moe_align_permute, and x quantised to MXFP4 (as
+ * mxfp4_quantize) straight into permuted order: a_codes [T*k, H/2], a_scales
+ * [T*k, mxfp4_scale_pitch(H)].  Identical to mxfp4_quantize followed by a
+ * row gather.  Constraints: as moe_route_quantize_nvfp4. */
+int moe_route_quantize_mxfp4(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                             float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, uint8_t* a_codes,
+                             uint8_t* a_scales, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                             nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * moe_grouped_gemm_nvfp4 -- ragged grouped GEMM over experts.
  * "The 2x Gap", sections "The Investigation So Far" and "Discovering the
@@ -165,11 +211,15 @@ int moe_route_quantize_nvfp4(const void* x, const float* logits, int T, int H, i
  * permuted row r of expert e (expert_offsets[e] <= r < expert_offsets[e+1]):
  *   W4A4 : out[r, n] = a_S * w_S[e] * sum_k dec(a[r,k]) * dec(w[e,n,k])
  *   W4A16: out[r, n] =        w_S[e] * sum_k a[r,k]      * dec(w[e,n,k])
- * with dec(.) = e2m1(code) * e4m3(block scale), fp32 accumulation.
+ *   MXW4A4: out[r, n] =              sum_k dec(a[r,k]) * dec(w[e,n,k])
+ * with dec(.) = e2m1(code) * e4m3(block scale) (MXFP4: * 2^(scale-127) per
+ * 32 elements), fp32 accumulation.
  *   W4A4 : a = codes [R, K/2], a_scales = [R, K/16], a_S = device fp32 scalar
  *   W4A16: a = bf16 [R, K], a_scales = NULL, a_S = NULL
+ *   MXW4A4: a = codes [R, K/2], a_scales [R, mxfp4_scale_pitch(K)], a_S and
+ *          w_S unused (may be NULL)
  *   w_codes        [E, N, K/2]
- *   w_scales_packed  from nvfp4_pack_weight_scales
+ *   w_scales_packed  from nvfp4_pack_weight_scales (mxfp4_pack_weight_scales)
  *   w_S            fp32 [E]
  *   expert_offsets int32 [E+1], expert_offsets[E] must equal R (checked on
  *                  the device; a violation sets dev_status to
@@ -191,6 +241,9 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
  *          [R, I/16]; h_bf16 unused (NULL).
  *   W4A16: h is rounded to bf16 (RNE) into h_bf16 [R, I]; the NVFP4 outputs
  *          and S_h are unused (NULL).
+ *   MXW4A4: h is quantised to MXFP4 (as mxfp4_quantize): h_codes [R, I/2],
+ *          h_scales [R, mxfp4_scale_pitch(I)]; S_h and h_bf16 unused.  The
+ *          block scales come from h itself, so no calibration is needed.
  *   G fp32 [R, 2I] (gate columns 0..I-1, up columns I..2I-1).
  * Constraints: I % 16 == 0.
  * ------------------------------------------------------------------------ */
@@ -211,10 +264,11 @@ int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, 
  * moe_layer_forward -- the whole layer in one call: every step above,
  * enqueued in order on `stream` with no host synchronisation, so the call
  * can be captured in a CUDA graph.
- *   mode        MOE_W4A4 or MOE_W4A16
+ *   mode        MOE_W4A4, MOE_W4A16 or MOE_MXW4A4
  *   x           bf16 [T, H]; logits fp32 [T, E]
  *   w13_*       gate_up weights: codes [E, 2I, H/2], packed scales, S [E]
  *   w2_*        down weights:    codes [E, H, I/2],  packed scales, S [E]
+ *               (MXW4A4: MXFP4 packed scales; w13_S, w2_S unused, may be NULL)
  *   S_h         device fp32 scalar, static decode scale of h (W4A4 only)
  *   out         fp32 [T, H]
  *   workspace   >= moe_layer_workspace_bytes(mode, T, H, I, E, k); holds

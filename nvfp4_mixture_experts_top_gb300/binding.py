@@ -17,7 +17,7 @@ from . import build as _build
 NVFP4_OK = 0
 NVFP4_DT_BF16, NVFP4_DT_F32 = 0, 1
 NVFP4_SCALE_STATIC, NVFP4_SCALE_DYNAMIC = 0, 1
-MOE_W4A4, MOE_W4A16 = 0, 1
+MOE_W4A4, MOE_W4A16, MOE_MXW4A4 = 0, 1, 2
 MOE_ACT_NONE, MOE_ACT_NVFP4, MOE_ACT_BF16 = 0, 1, 2
 STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4_E_ALIGN", 4: "NVFP4_E_WORKSPACE",
                 5: "NVFP4_E_ARCH", 6: "NVFP4_E_CUDA", 7: "NVFP4_E_DEVICE_TIMEOUT", 8: "NVFP4_E_BAD_ROUTING"}
@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4
 EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspace_bytes", "nvfp4_quantize",
            "nvfp4_pack_weight_scales", "moe_align_permute_workspace_bytes", "moe_align_permute",
            "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine", "moe_layer_workspace_bytes",
-           "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4")
+           "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4", "mxfp4_scale_pitch",
+           "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4")
 
 
 class Nvfp4Error(RuntimeError):
@@ -83,6 +84,14 @@ def load(build_if_missing: bool = True):
     L.moe_route_quantize_nvfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_align_permute_noalloc.restype = _I
     L.moe_align_permute_noalloc.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P, _P]
+    L.mxfp4_scale_pitch.restype = _I64
+    L.mxfp4_scale_pitch.argtypes = [_I64]
+    L.mxfp4_quantize.restype = _I
+    L.mxfp4_quantize.argtypes = [_P, _I, _I64, _I64, _I64, _P, _P, _P]
+    L.mxfp4_pack_weight_scales.restype = _I
+    L.mxfp4_pack_weight_scales.argtypes = [_P, _I, _I, _I, _P, _P]
+    L.moe_route_quantize_mxfp4.restype = _I
+    L.moe_route_quantize_mxfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     _lib = L
     return L
 
@@ -151,6 +160,37 @@ def nvfp4_pack_weight_scales(scales_linear, E, N, K, out=None):
     return out
 
 
+def mxfp4_scale_pitch(cols):
+    return int(load().mxfp4_scale_pitch(cols))
+
+
+def mxfp4_quantize(x, codes=None, scales=None):
+    """Quantise x [rows, cols] (bf16 or fp32, CUDA) to MXFP4.  Returns (codes
+    [rows, cols/2], scales [rows, mxfp4_scale_pitch(cols)])."""
+    L = load()
+    rows, cols = x.shape
+    dev = x.device
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be bf16 or fp32")
+    dt = NVFP4_DT_BF16 if x.dtype == torch.bfloat16 else NVFP4_DT_F32
+    if codes is None:
+        codes = _empty((rows, cols // 2), torch.uint8, dev)
+    if scales is None:
+        scales = _empty((rows, mxfp4_scale_pitch(cols)), torch.uint8, dev)
+    _check("mxfp4_quantize", L.mxfp4_quantize(_ptr(x), dt, rows, cols, x.stride(0), _ptr(codes), _ptr(scales),
+                                              _stream()))
+    return codes, scales
+
+
+def mxfp4_pack_weight_scales(scales_linear, E, N, K, out=None):
+    L = load()
+    if out is None:
+        out = _empty(E * N * (K // 32), torch.uint8, scales_linear.device)
+    _check("mxfp4_pack_weight_scales",
+           L.mxfp4_pack_weight_scales(_ptr(scales_linear), E, N, K, _ptr(out), _stream()))
+    return out
+
+
 def moe_align_permute(logits, k, act=None, act_kind=MOE_ACT_NONE, dev_status=None):
     """Route + permute.  act: None, (codes, scales) for NVFP4 rows, or a bf16
     [T, H] tensor.  Returns dict(ids, w, offsets, perm, inv[, act_codes,
@@ -211,10 +251,34 @@ def moe_route_quantize_nvfp4(x, logits, k, dev_status=None):
     return out
 
 
+def moe_route_quantize_mxfp4(x, logits, k, dev_status=None):
+    """Routing + MXFP4 quantisation of x [T, H] bf16 written in permuted order.
+    Returns dict(ids, w, offsets, perm, inv, act_codes, act_scales)."""
+    L = load()
+    T, H = x.shape
+    E = logits.shape[1]
+    dev = x.device
+    R = T * k
+    out = dict(ids=_empty((T, k), torch.int32, dev), w=_empty((T, k), torch.float32, dev),
+               offsets=_empty((E + 1,), torch.int32, dev), perm=_empty((max(R, 1),), torch.int32, dev),
+               inv=_empty((max(R, 1),), torch.int32, dev),
+               act_codes=_empty((max(R, 1), H // 2), torch.uint8, dev),
+               act_scales=_empty((max(R, 1), mxfp4_scale_pitch(H)), torch.uint8, dev))
+    ws = _empty(max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256), torch.uint8, dev)
+    _check("moe_route_quantize_mxfp4",
+           L.moe_route_quantize_mxfp4(_ptr(x), _ptr(logits), T, H, E, k, _ptr(out["ids"]), _ptr(out["w"]),
+                                      _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv"]),
+                                      _ptr(out["act_codes"]), _ptr(out["act_scales"]), _ptr(dev_status), _ptr(ws),
+                                      ws.numel(), _stream()))
+    for key in ("perm", "inv", "act_codes", "act_scales"):
+        out[key] = out[key][:R]
+    return out
+
+
 def moe_grouped_gemm_nvfp4(mode, a, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, N, K, out=None,
                            dev_status=None):
     L = load()
-    E = w_S.shape[0]
+    E = offsets.numel() - 1
     R = a.shape[0]
     if out is None:
         out = _empty((max(R, 1), N), torch.float32, a.device)[:R]
@@ -229,9 +293,9 @@ def moe_swiglu_requant(G, mode, S_h=None):
     R, I2 = G.shape
     I = I2 // 2
     dev = G.device
-    if mode == MOE_W4A4:
+    if mode in (MOE_W4A4, MOE_MXW4A4):
         hc = _empty((max(R, 1), I // 2), torch.uint8, dev)
-        hs = _empty((max(R, 1), I // 16), torch.uint8, dev)
+        hs = _empty((max(R, 1), I // 16 if mode == MOE_W4A4 else mxfp4_scale_pitch(I)), torch.uint8, dev)
         _check("moe_swiglu_requant",
                L.moe_swiglu_requant(_ptr(G), R, I, mode, _ptr(S_h), _ptr(hc), _ptr(hs), None, _stream()))
         return hc[:R], hs[:R]
@@ -255,7 +319,8 @@ def moe_layer_workspace_bytes(mode, T, H, I, E, k):
 
 
 def moe_layer_forward(mode, x, logits, k, w13, w2, S_h, out=None, workspace=None, dev_status=None):
-    """Whole layer.  w13 / w2: (codes, packed scales, S[E]) on the GPU."""
+    """Whole layer.  w13 / w2: (codes, packed scales, S[E]) on the GPU (S is
+    None for MOE_MXW4A4)."""
     L = load()
     T, H = x.shape
     E = logits.shape[1]

@@ -198,6 +198,12 @@ __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);    // M / 16
 }
 
+// The same for MXFP4 operands: E2M1 x E2M1 with UE8M0 scales, one scale per
+// 32 elements (used with .scale_vec::2X: two scales per row per K=64 MMA).
+__host__ __device__ constexpr uint32_t idesc_mxf4_ue8m0(uint32_t M, uint32_t N) {
+  return idesc_mxf4nvf4(M, N) | (1u << 23);  // scale type: UE8M0
+}
+
 // Instruction descriptor, kind::f16 with BF16 inputs and fp32 accumulate.
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
   return (1u << 4)              // D format: F32
@@ -306,6 +312,20 @@ __device__ __forceinline__ void ew_mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc,
       "setp.ne.b32 p, %6, 0;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// MXFP4: two UE8M0 scales per row per MMA, read from bytes 0 and 1 of the
+// row's 32-bit scale cell (scale-factor data id 0).
+__device__ __forceinline__ void ew_mma_mxf4_2x(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
@@ -469,6 +489,53 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&v)[16], float
   w0 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
   w1 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
   return sc;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP4 encoding (32-element blocks, UE8M0 power-of-two scales)
+// ---------------------------------------------------------------------------
+
+// fp32 2^n for n in [-127, 127] (2^-127 is subnormal); built from the bits.
+__device__ __forceinline__ float exp2_int(int n) {
+  return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// floor(log2(a)) of a finite fp32 a > 0, subnormals included, from the bits.
+__device__ __forceinline__ int floor_log2(float a) {
+  const uint32_t u = __float_as_uint(a);
+  const int e = (int)(u >> 23);
+  return e > 0 ? e - 127 : (31 - __clz((int)u)) - 149;  // subnormal: value = u * 2^-149
+}
+
+// Quantise one 32-element block to MXFP4: shared exponent E = floor(log2
+// amax) - 2 (E2M1's largest magnitude is 1.5 * 2^2), clamped to [-127, 127],
+// an all-zero block taking -127; elements E2M1(RN, satfinite) of x * 2^-E,
+// one correctly rounded fp32 multiply (exact unless subnormal), sign kept.
+// Returns the UE8M0 code E + 127; writes 16 bytes of packed element codes.
+__device__ __forceinline__ uint32_t mx_quantize_block32(const float (&v)[32], uint4& codes) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int E = amax == 0.0f ? -127 : floor_log2(amax) - 2;
+  E = E < -127 ? -127 : (E > 127 ? 127 : E);
+  const float inv = exp2_int(-E);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float q0 = __fmul_rn(v[8 * q + 2 * i], inv);
+      const float q1 = __fmul_rn(v[8 * q + 2 * i + 1], inv);
+      uint32_t byte = e2m1x2_from_abs(fabsf(q0), fabsf(q1));
+      byte |= (__float_as_uint(q0) >> 31) << 3;
+      byte |= (__float_as_uint(q1) >> 31) << 7;
+      word |= byte << (8 * i);
+    }
+    w[q] = word;
+  }
+  codes = make_uint4(w[0], w[1], w[2], w[3]);
+  return (uint32_t)(E + 127);
 }
 
 }  // namespace nvfp4moe

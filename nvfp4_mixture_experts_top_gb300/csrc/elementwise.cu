@@ -1,6 +1,6 @@
 // elementwise.cu -- HBM-bound kernels of the NVFP4 MoE path: quantiser
 // (with the warp-shuffle tensor amax), weight-scale packing, SwiGLU +
-// requantisation, and the weighted combine.
+// requantisation, and the weighted combine; and their MXFP4 counterparts.
 //
 // All of them are one-pass streaming kernels: coalesced 16-byte loads and
 // stores, grids sized in multiples of the SM count, no shared-memory staging
@@ -220,6 +220,101 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
+// MXFP4: quantiser, quantise-scatter, weight-scale packing, SwiGLU + requant
+// (one thread per 32-element block; scale rows padded to mx_scale_pitch)
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(256) mx_quantize_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+                                                          int64_t ld, uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  const int64_t nb = cols / 32, pitch = mx_scale_pitch(cols);
+  const int64_t total = rows * pitch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / pitch, b = i % pitch;
+    if (b >= nb) {
+      scales[i] = 0;  // row padding
+      continue;
+    }
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) load8<T>(x + r * ld + b * 32 + 8 * q, v + 8 * q);
+    uint4 c;
+    const uint32_t sc = mx_quantize_block32(v, c);
+    *reinterpret_cast<uint4*>(codes + r * (cols / 2) + b * 16) = c;
+    scales[i] = (uint8_t)sc;
+  }
+}
+
+__global__ void __launch_bounds__(256) mx_quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T,
+                                                                  int64_t H, int k, const int32_t* __restrict__ inv,
+                                                                  uint8_t* __restrict__ codes,
+                                                                  uint8_t* __restrict__ scales) {
+  const int64_t nb = H / 32, pitch = mx_scale_pitch(H);
+  const int64_t total = (int64_t)T * pitch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / pitch, b = i % pitch;
+    if (b >= nb) {
+      for (int j = 0; j < k; ++j) scales[(int64_t)__ldg(inv + t * k + j) * pitch + b] = 0;
+      continue;
+    }
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) load8<__nv_bfloat16>(x + t * H + b * 32 + 8 * q, v + 8 * q);
+    uint4 c;
+    const uint8_t sc = (uint8_t)mx_quantize_block32(v, c);
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = __ldg(inv + t * k + j);
+      *reinterpret_cast<uint4*>(codes + r * (H / 2) + b * 16) = c;
+      scales[r * pitch + b] = sc;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t* __restrict__ in, int64_t E, int64_t N,
+                                                             int64_t K, uint8_t* __restrict__ out) {
+  const int64_t kb_n = K / 64;  // scale pairs per row
+  const int64_t total = E * N * kb_n;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / kb_n, kb = i % kb_n;  // row = e*N + n
+    const int64_t e = row / N, n = row % N;
+    const uint16_t pair = *reinterpret_cast<const uint16_t*>(in + row * (K / 32) + kb * 2);
+    const int64_t nt = n / 128, r = n % 128;
+    const int64_t blk = (e * (N / 128) + nt) * kb_n + kb;
+    *reinterpret_cast<uint16_t*>(out + blk * 256 + (r % 32) * 8 + (r / 32) * 2) = pair;
+  }
+}
+
+__global__ void __launch_bounds__(256) swiglu_requant_mx_kernel(const float* __restrict__ G, int64_t R, int64_t I,
+                                                                uint8_t* __restrict__ h_codes,
+                                                                uint8_t* __restrict__ h_scales) {
+  const int64_t nb = I / 32, pitch = mx_scale_pitch(I);
+  const int64_t total = R * pitch;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / pitch, b = i % pitch;
+    if (b >= nb) {
+      h_scales[i] = 0;
+      continue;
+    }
+    const float4* gp = reinterpret_cast<const float4*>(G + r * 2 * I + b * 32);
+    const float4* up = reinterpret_cast<const float4*>(G + r * 2 * I + I + b * 32);
+    float h[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 g = __ldg(gp + q), u = __ldg(up + q);
+      h[4 * q + 0] = silu_mul(g.x, u.x);
+      h[4 * q + 1] = silu_mul(g.y, u.y);
+      h[4 * q + 2] = silu_mul(g.z, u.z);
+      h[4 * q + 3] = silu_mul(g.w, u.w);
+    }
+    uint4 c;
+    const uint32_t sc = mx_quantize_block32(h, c);
+    *reinterpret_cast<uint4*>(h_codes + r * (I / 2) + b * 16) = c;
+    h_scales[i] = (uint8_t)sc;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 
@@ -287,6 +382,43 @@ cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, i
   const int64_t total = (int64_t)T * (H / 4);
   if (total == 0) return cudaSuccess;
   combine_kernel<<<grid_for(total, 256), 256, 0, st>>>(Y, inv, w, T, k, H, out_dtype, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t st) {
+  const int64_t total = rows * mx_scale_pitch(cols);
+  if (total == 0) return cudaSuccess;
+  const int g = grid_for(total, 256);
+  if (x_dtype == NVFP4_DT_BF16)
+    mx_quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, codes,
+                                                         scales);
+  else
+    mx_quantize_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv, uint8_t* codes,
+                                       uint8_t* scales, cudaStream_t st) {
+  const int64_t total = (int64_t)T * mx_scale_pitch(H);
+  if (total == 0) return cudaSuccess;
+  mx_quantize_scatter_kernel<<<grid_for(total, 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x_bf16), T, H,
+                                                                   k, inv, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st) {
+  const int64_t total = (int64_t)E * N * (K / 64);
+  if (total == 0) return cudaSuccess;
+  mx_pack_scales_kernel<<<grid_for(total, 256), 256, 0, st>>>(in, E, N, K, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_requant_mx(const float* G, int R, int I, uint8_t* h_codes, uint8_t* h_scales,
+                                     cudaStream_t st) {
+  const int64_t total = (int64_t)R * mx_scale_pitch(I);
+  if (total == 0) return cudaSuccess;
+  swiglu_requant_mx_kernel<<<grid_for(total, 256), 256, 0, st>>>(G, R, I, h_codes, h_scales);
   return cudaGetLastError();
 }
 

@@ -57,7 +57,7 @@ constexpr int TOK_PER_PASS = TG * MAXG;
 
 constexpr uint32_t W_BYTES = BM * KC / 2;    // 16384
 constexpr uint32_t A_BYTES = TG * KC / 2;    // 4096
-constexpr uint32_t WS_BYTES = BM * KC / 16;  // 2048
+constexpr uint32_t WS_BYTES = BM * KC / 16;  // 2048: scale cells in shared memory
 constexpr uint32_t AS_BYTES = TG * KC / 16;  // 512
 constexpr uint32_t OFF_A = W_BYTES;                        // 16384
 constexpr uint32_t OFF_WS = OFF_A + MAXG * A_BYTES;         // 32768
@@ -89,10 +89,19 @@ struct Params {
 };
 
 
+// MX = false: NVFP4 (E4M3 scale per 16 elements, per-tensor fp32 scales,
+// kind::mxf4nvf4 .scale_vec::4X).  MX = true: MXFP4 (UE8M0 scale per 32
+// elements, no per-tensor scales, .scale_vec::2X); the weight scales arrive
+// as 1 KB per stage (two bytes per row per MMA) and the activation scales as
+// rows of mx_scale_pitch(K) bytes, and warp 6 widens both into the 4-byte
+// per-row cells that tcgen05.cp copies to TMEM (bytes 2-3 zero).
+template <bool MX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_as, const __grid_constant__ CUtensorMap tm_a4,
                      const __grid_constant__ CUtensorMap tm_as4, const Params p) {
+  // bytes of weight scales fetched per stage (MXFP4: two per row per MMA)
+  constexpr uint32_t WS_SRC_BYTES = MX ? WS_BYTES / 2 : WS_BYTES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t sf_ready[STAGES];
@@ -160,9 +169,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const int e = it.e, nt = it.nt, r0 = it.r0, ng = it.ng;
-      const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * 512;
+      const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * (MX ? 256 : 512);
       {
-        const uint32_t bytes = W_BYTES + WS_BYTES + (ng == 1 ? 1 : MAXG) * (A_BYTES + AS_BYTES);
+        const uint32_t bytes = W_BYTES + WS_SRC_BYTES + (ng == 1 ? 1 : MAXG) * (A_BYTES + AS_BYTES);
         for (int kc = kc0; kc < kc1; ++kc) {
           if (!warp_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
             ok = false;
@@ -182,17 +191,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           ew_arrive_expect_tx(&full_bar[stage], bytes);
           ew_tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
-          ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * 4 * 512, WS_BYTES, &full_bar[stage], pol_w);
+          // NVFP4: the 2 KB of packed scale cells; MXFP4: 1 KB of scale pairs,
+          // staged in the upper half and widened in place by warp 6
+          ew_bulk_load(sb + OFF_WS + (MX ? WS_BYTES - WS_SRC_BYTES : 0), wsc + (size_t)kc * WS_SRC_BYTES,
+                       WS_SRC_BYTES, &full_bar[stage], pol_w);
+          // token scales: NVFP4 16 B per row per stage; MXFP4 8 B, so the
+          // 16-byte box covers two stages and warp 6 picks its half
+          const int as_x = MX ? (kc >> 1) * 16 : kc * (KC / 16);
           // one copy per operand whatever the token count: a 32-row box for a
           // single group, a 128-row box (all groups) otherwise -- TMA issue
           // costs ~100 cycles per copy, so per-group copies would bound the
           // stage rate of many-token passes
           if (ng == 1) {
             ew_tma_load_2d(sb + OFF_A, &tm_a, &full_bar[stage], kc * (KC / 2), r0, pol_a);
-            ew_tma_load_2d(sb + OFF_AS, &tm_as, &full_bar[stage], kc * (KC / 16), r0, pol_a);
+            ew_tma_load_2d(sb + OFF_AS, &tm_as, &full_bar[stage], as_x, r0, pol_a);
           } else {
             ew_tma_load_2d(sb + OFF_A, &tm_a4, &full_bar[stage], kc * (KC / 2), r0, pol_a);
-            ew_tma_load_2d(sb + OFF_AS, &tm_as4, &full_bar[stage], kc * (KC / 16), r0, pol_a);
+            ew_tma_load_2d(sb + OFF_AS, &tm_as4, &full_bar[stage], as_x, r0, pol_a);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -228,9 +243,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint4 v[MAXG];
 #pragma unroll
           for (int g = 0; g < MAXG; ++g) v[g] = *reinterpret_cast<const uint4*>(as_tile + g * AS_BYTES + lane * 16);
+          uint32_t w[MAXG][4];
+          if constexpr (MX) {
+            // this stage's 8 scale bytes of token (32g + lane): half kc & 1 of
+            // the 16-byte row; the pair for MMA kk widens to one cell
+#pragma unroll
+            for (int g = 0; g < MAXG; ++g) {
+              const uint32_t a = (kc & 1) ? v[g].z : v[g].x, b = (kc & 1) ? v[g].w : v[g].y;
+              w[g][0] = a & 0xFFFFu;
+              w[g][1] = a >> 16;
+              w[g][2] = b & 0xFFFFu;
+              w[g][3] = b >> 16;
+            }
+            // weight scales: pairs [kk][lane][row quarter c] at the upper 1 KB
+            // -> cells [kk][lane][c] over the whole 2 KB
+            uint8_t* ws_tile = smem + stage * STAGE_BYTES + OFF_WS;
+            uint2 pr[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              pr[kk] = *reinterpret_cast<const uint2*>(ws_tile + (WS_BYTES - WS_SRC_BYTES) + kk * 256 + lane * 8);
+            __syncwarp();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              *reinterpret_cast<uint4*>(ws_tile + kk * 512 + lane * 16) =
+                  make_uint4(pr[kk].x & 0xFFFFu, pr[kk].x >> 16, pr[kk].y & 0xFFFFu, pr[kk].y >> 16);
+          } else {
+#pragma unroll
+            for (int g = 0; g < MAXG; ++g) {
+              w[g][0] = v[g].x;
+              w[g][1] = v[g].y;
+              w[g][2] = v[g].z;
+              w[g][3] = v[g].w;
+            }
+          }
           __syncwarp();
-          const uint32_t w[MAXG][4] = {{v[0].x, v[0].y, v[0].z, v[0].w}, {v[1].x, v[1].y, v[1].z, v[1].w},
-                                       {v[2].x, v[2].y, v[2].z, v[2].w}, {v[3].x, v[3].y, v[3].z, v[3].w}};
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             *reinterpret_cast<uint4*>(as_tile + kk * AS_BYTES + lane * 16) =
@@ -260,7 +306,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       const int ng = decode_item<TOK_PER_PASS>(w, s_base, NT, xr).ng;
       {
-        const uint32_t idesc = idesc_mxf4nvf4(BM, TG * ng);
+        const uint32_t idesc = MX ? idesc_mxf4_ue8m0(BM, TG * ng) : idesc_mxf4nvf4(BM, TG * ng);
         if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
           break;
@@ -287,7 +333,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ew_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
             ew_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
             // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
-            ew_mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
+            if constexpr (MX)
+              ew_mma_mxf4_2x(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
+                             (kc != kc0 || kk != 0));
+            else
+              ew_mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
                             (kc != kc0 || kk != 0));
           }
           ew_commit(&empty_bar[stage]);
@@ -322,7 +372,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
       const int r0 = it.r0, m1 = it.m1, ng = it.ng;
-      const float alpha = __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
+      const float alpha = MX ? 1.0f : __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
       const int n = it.nt * BM + q * 32 + lane;
       {
         if (!warp_wait(&acc_full[acc], acc_phase, &abort_flag, p.dev_status)) {
@@ -369,15 +419,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace w4a4
 
-cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
-                             const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
-                             const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
-                             cudaStream_t st) {
+template <bool MX>
+static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
+                               const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                               const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
+                               cudaStream_t st) {
   using namespace w4a4;
   if (R == 0 || E == 0) return cudaSuccess;
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_w4a4_kernel<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -389,13 +442,15 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   // token codes: [R rows, K/2 bytes], box 128 B x 32 rows, 128-byte swizzle
   err = make_tmap_2d_u8(&tm_a, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TG, 128);
   if (err != cudaSuccess) return err;
-  // token scales: [R rows, K/16 bytes], box 16 B x 32 rows, no swizzle
-  err = make_tmap_2d_u8(&tm_as, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TG, 0);
+  // token scales: NVFP4 [R rows, K/16 bytes]; MXFP4 [R rows, mx_scale_pitch(K)
+  // bytes]; box 16 B x 32 rows, no swizzle
+  const uint64_t as_pitch = MX ? (uint64_t)mx_scale_pitch(K) : (uint64_t)K / 16;
+  err = make_tmap_2d_u8(&tm_as, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, TG, 0);
   if (err != cudaSuccess) return err;
   // the same two tensors with 128-row boxes (all token groups of a pass)
   err = make_tmap_2d_u8(&tm_a4, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TOK_PER_PASS, 128);
   if (err != cudaSuccess) return err;
-  err = make_tmap_2d_u8(&tm_as4, a_scales, (uint64_t)K / 16, (uint64_t)R, (uint64_t)K / 16, KC / 16, TOK_PER_PASS, 0);
+  err = make_tmap_2d_u8(&tm_as4, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, TOK_PER_PASS, 0);
   if (err != cudaSuccess) return err;
   Params p;
   p.w_scales = w_scales_packed;
@@ -409,7 +464,6 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
   p.K = K;
   p.R = R;
   p.drop_stage = fault_injection_drop_stage();
-  if (E > kMaxExperts) return cudaErrorInvalidValue;
   // the number of work items depends on the routing, which lives on the
   // device: launch one persistent CTA per SM and let each find its items
   // Split K in two when even the largest possible number of work items,
@@ -421,8 +475,23 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
-  gemm_w4a4_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4, p);
+  gemm_w4a4_kernel<MX><<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
+                             const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                             const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
+                             cudaStream_t st) {
+  return launch_impl<false>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                            dev_status, st);
+}
+
+cudaError_t launch_gemm_mxw4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
+                               const uint8_t* w_scales_packed, const int32_t* offsets, int E, int N, int K, int R,
+                               float* out, int32_t* dev_status, cudaStream_t st) {
+  return launch_impl<true>(a_codes, a_scales, nullptr, w_codes, w_scales_packed, nullptr, offsets, E, N, K, R, out,
+                           dev_status, st);
 }
 
 }  // namespace nvfp4moe

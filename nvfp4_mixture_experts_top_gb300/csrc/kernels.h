@@ -54,4 +54,28 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
                               const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
                               int32_t* dev_status, cudaStream_t st);
 
+// ---------------------------------------------------------------------------
+// MXFP4 (32-element blocks, UE8M0 scales)
+// ---------------------------------------------------------------------------
+
+// Row pitch in bytes of an MXFP4 scale tensor with `cols` columns: cols/32
+// rounded up to a multiple of 16 (TMA rows start on 16-byte boundaries); the
+// padding bytes are written as zero.
+__host__ __device__ constexpr int64_t mx_scale_pitch(int64_t cols) { return ((cols / 32 + 15) / 16) * 16; }
+
+cudaError_t launch_mx_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t st);
+// Quantise x [T, H] bf16 to MXFP4 and write each token's row to its k
+// permuted rows inv[t*k + j].
+cudaError_t launch_mx_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv, uint8_t* codes,
+                                       uint8_t* scales, cudaStream_t st);
+// linear [E, N, K/32] -> per (expert, 128-row tile, K/64 step) 256-byte
+// blocks: row r's two scales at (r % 32) * 8 + (r / 32) * 2.
+cudaError_t launch_mx_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st);
+cudaError_t launch_swiglu_requant_mx(const float* G, int R, int I, uint8_t* h_codes, uint8_t* h_scales,
+                                     cudaStream_t st);
+cudaError_t launch_gemm_mxw4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
+                               const uint8_t* w_scales_packed, const int32_t* offsets, int E, int N, int K, int R,
+                               float* out, int32_t* dev_status, cudaStream_t st);
+
 }  // namespace nvfp4moe

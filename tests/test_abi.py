@@ -59,3 +59,26 @@ def test_host_validation_without_gpu():
     # routing with k > 32 -> E_SHAPE
     assert L.moe_align_permute(None, 4, 64, 33, None, None, ctypes.c_void_p(16), None, None, 0, None, None, 0,
                                None, None, None, None, 0, None) == 2
+
+
+def test_mxfp4_host_side_without_gpu():
+    """The MXFP4 scale pitch (a host computation) and the MXFP4 argument
+    checks, which run before any device call."""
+    from nvfp4_mixture_experts_top_gb300 import binding
+    L = binding.load()
+    # cols/32 rounded up to a multiple of 16 bytes
+    assert [L.mxfp4_scale_pitch(c) for c in (32, 256, 512, 768, 2048, 4096, 6144)] == [16, 16, 16, 32, 64, 128, 192]
+    # cols not a multiple of 32 -> E_SHAPE; null outputs -> E_INVAL; bad dtype -> E_INVAL
+    assert L.mxfp4_quantize(None, 0, 4, 48, 48, None, None, None) == 2
+    assert L.mxfp4_quantize(None, 0, 4, 64, 64, None, None, None) == 1
+    assert L.mxfp4_quantize(None, 5, 4, 64, 64, None, None, None) == 1
+    # MXFP4 grouped GEMM needs activation scales but no per-tensor scales
+    assert L.moe_grouped_gemm_nvfp4(2, ctypes.c_void_p(16), None, None, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                    None, ctypes.c_void_p(16), 4, 128, 256, 8, ctypes.c_void_p(16), None,
+                                    None) == 1
+    # MXFP4 weight-scale packing shape rule
+    assert L.mxfp4_pack_weight_scales(None, 2, 100, 256, None, None) == 2
+    # SwiGLU/requant in MXFP4 needs I % 32 == 0
+    assert L.moe_swiglu_requant(ctypes.c_void_p(16), 4, 48, 2, None, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                None, None) == 2
+    assert L.moe_layer_workspace_bytes(2, 16, 4096, 2048, 256, 8) > 16 * 8 * 2 * 2048 * 4
