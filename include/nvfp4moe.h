@@ -113,7 +113,7 @@ int nvfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, 
 
 /* ------------------------------------------------------------------------
  * MXFP4 -- the group-32 format with UE8M0 (power-of-two) block scales that
- * "The Benchmark That Confirmed the Ceiling", sections "Introduction" and
+ * "The Benchmark That Confirmed the Ceiling", sections "The Optimization Hierarchy" and
  * "The NVFP4 Pivot", names as the stock checkpoint's.  The pages define only
  * the block size and the scale type; the conversion follows the OCP MX rule:
  *   per 32-element block: E = floor(log2(amax)) - 2, clamped to [-127, 127]

@@ -19,7 +19,7 @@
  *    both operands plus one per-tensor coefficient; section "The Investigation
  *    So Far": routed top-8 of 256 experts, ~16 tokens per expert.
  *  - "The Benchmark That Confirmed the Ceiling: NVFP4 Cutlass on sm_120",
- *    sections "Introduction" and "The NVFP4 Pivot": the stock checkpoint is
+ *    sections "The Optimization Hierarchy" and "The NVFP4 Pivot": the stock checkpoint is
  *    MXFP4 -- group-32 blocks with UE8M0 (power-of-two) scales.
  *  - "The 24% Ceiling: Diagnosing the Limits of NVFP4 Quantization on
  *    Blackwell SM120 GPUs", section "The Core Insight": W4A16 keeps the
