@@ -114,6 +114,14 @@ def router_logits(cfg: MoEConfig, seed: int = 0, device="cpu") -> torch.Tensor:
     return z.contiguous()
 
 
+def router_weight_bf16(E: int, H: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Router weight [E, H] ~ N(0, 1/H) rounded to bf16, so that the logits of
+    N(0, 1) activations are about N(0, 1) (the scale of router_logits)."""
+    g = _gen(device, "router", seed, E, H)
+    w = torch.randn(E, H, generator=g, device=device, dtype=torch.float32) / float(np.sqrt(H))
+    return w.to(torch.bfloat16)
+
+
 def expert_weight_fp32(which: str, e: int, N: int, K: int, seed: int = 0, device="cpu") -> torch.Tensor:
     """One expert's weight matrix [N, K] ~ N(0, 0.02) in fp32.  which is
     'w13' (gate rows 0..I-1 then up rows I..2I-1, K = hidden) or 'w2'

@@ -314,6 +314,22 @@ void orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows
 /* Router and permutation                                                   */
 /* ------------------------------------------------------------------------ */
 
+/* Router logits, the step before routing ("The 2x Gap: Diagnosing Suboptimal
+ * FP4 GEMM Kernels on Blackwell SM120", section "The Investigation So Far":
+ * each token goes to 8 of 256 experts chosen from these scores):
+ *   logits[t, e] = sum_h x[t, h] * w[e, h]
+ * x [T, H] and w [E, H] hold bf16 values widened to fp32; the sum is fp64
+ * and the result is stored as fp32 (the GPU's storage type). */
+void orc_router_logits(const float* x, const float* w, int T, int H, int E, float* logits) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h) acc += (double)x[(int64_t)t * H + h] * (double)w[(int64_t)e * H + h];
+      logits[(int64_t)t * E + e] = (float)acc;
+    }
+}
+
 /* Top-k selection by repeated arg-max (strict >, so ties go to the lower
  * expert id), then softmax over the k selected logits in fp64. */
 void orc_route(const float* logits, int T, int E, int k, int32_t* ids, double* w) {

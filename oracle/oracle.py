@@ -73,6 +73,8 @@ def _declare(L):
     L.orc_mx_quantize.argtypes = [_P, _I64, _I64, _I64, _P, _P]
     L.orc_mx_dequantize.restype = None
     L.orc_mx_dequantize.argtypes = [_P, _P, _I64, _I64, _P]
+    L.orc_router_logits.restype = None
+    L.orc_router_logits.argtypes = [_P, _P, C.c_int, C.c_int, C.c_int, _P]
     L.orc_grouped_gemm_mx.restype = None
     L.orc_grouped_gemm_mx.argtypes = [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, _P]
 
@@ -202,6 +204,17 @@ def mx_quantize_experts(w):
     for e in range(E):
         codes[e], scales[e] = mx_quantize(w[e])
     return codes, scales, None
+
+
+def router_logits(x, w):
+    """logits [T, E] (fp32) = x [T, H] . w [E, H]^T, summed in fp64."""
+    x = _c(x, np.float32)
+    w = _c(w, np.float32)
+    T, H = x.shape
+    E = w.shape[0]
+    out = np.zeros((T, E), np.float32)
+    lib().orc_router_logits(_p(x), _p(w), T, H, E, _p(out))
+    return out
 
 
 def route(logits, k):

@@ -287,3 +287,21 @@ def test_layer_token_subset_with_batch_scale(orc):
     sub = orc.moe_layer("w4a4", x[toks], logits[toks][:, used], cfg.k,
                         tuple(a[used] for a in w13), tuple(a[used] for a in w2), cfg.S_h, S_x=S_x)
     assert np.array_equal(sub, full[toks])
+
+
+def test_router_logits_vs_numpy_and_one_hot(orc):
+    """The oracle's router-logits loop against numpy's fp64 matmul (an
+    independent implementation), and one-hot activations that must pick out
+    router-weight columns exactly."""
+    T, H, E = 9, 320, 40
+    x = wl.activations_bf16(T, H, seed=3).float().numpy()
+    w = wl.router_weight_bf16(E, H, seed=3).float().numpy()
+    got = orc.router_logits(x, w)
+    ref = (x.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32)
+    # both sum in fp64 and round once to fp32; only the fp64 summation order
+    # differs, which can move a rare result by one fp32 ulp
+    assert np.allclose(got, ref, rtol=2e-7, atol=1e-9) and (got == ref).mean() > 0.99
+    assert 0.5 < got.std() < 2.0     # logits of the expected scale
+    oh = np.zeros((3, H), np.float32)
+    oh[0, 0] = oh[1, 77] = oh[2, H - 1] = 1.0
+    assert np.array_equal(orc.router_logits(oh, w), w[:, [0, 77, H - 1]].T)
