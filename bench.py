@@ -313,6 +313,74 @@ def run_gemm_sweep(args, wl):
     print(json.dumps(result), flush=True)
 
 
+def run_router(args, cfg, wl):
+    """Router logits (moe_router_logits) for the workload's T, H, E: a CUDA
+    graph of back-to-back calls rotating over copies of x and W_router whose
+    total exceeds twice the L2, so every call reads its operands from HBM.
+    value = tokens/s of the router step alone."""
+    import torch
+
+    from nvfp4_mixture_experts_top_gb300 import binding as B
+    dev = torch.device("cuda", _dist()[2])
+    torch.cuda.set_device(dev)
+    L = B.load()
+    B.nvfp4_device_check()
+    hbm, _, peak_kind = _load_peaks()
+    T, H, E = cfg.T, cfg.H, cfg.E
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = E * H * 2 + T * H * 2 + T * E * 4
+    copies = int(max(2, np.ceil(2 * l2 / per_copy)))
+    x = wl.activations_bf16(T, H, device=dev)
+    w = wl.router_weight_bf16(E, H, device=dev)
+    Xs = [x.clone() for _ in range(copies)]
+    Ws = [w.clone() for _ in range(copies)]
+    outs = [torch.empty(T, E, device=dev) for _ in range(copies)]
+    ws = torch.empty(int(L.moe_router_logits_workspace_bytes(T, H, E)), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch(i):
+        r = L.moe_router_logits(Xs[i].data_ptr(), Ws[i].data_ptr(), T, H, E, outs[i].data_ptr(), status.data_ptr(),
+                                ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+        if r != 0:
+            raise B.Nvfp4Error("moe_router_logits", r)
+
+    for i in range(args.warmup):
+        launch(i % copies)
+    reps = max(args.steps, copies)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(reps):
+                launch(i % copies)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d" % int(status.item()))
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    gbs = per_copy / (us * 1e-6) / 1e9
+    splits = int(L.moe_router_logits_workspace_bytes(T, H, E)) // max(1, T * E * 4)
+    result = {"metric": "router-logits tokens/s (%s: T=%d, H=%d, E=%d)" % (cfg.name, T, H, E),
+              "value": T / (us * 1e-6), "unit": "tokens/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+              "ms_per_step": us / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "bf16xbf16, fp32 accumulate", "data": "synthetic",
+              "config": {"workload": cfg.name + "_router", "T": T, "hidden": H, "experts": E,
+                         "k_splits": max(1, splits),
+                         "l2": "rotating %d operand copies > 2x L2" % copies},
+              "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                           "peak_kind": peak_kind, "algorithmic_bytes_per_launch": per_copy, "avg_launch_us": us,
+                           "traffic": None},
+              "gpu_launches": reps * (2 if splits > 1 else 1)}
+    print(json.dumps(result), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -326,6 +394,8 @@ def main():
     ap.add_argument("--baseline-tokens", type=int, default=4, help="tokens of the in-run CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--router", action="store_true",
+                    help="time the router-logits GEMM for the workload's T, H, E instead of the layer")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profiler captures)")
     args = ap.parse_args()
@@ -337,6 +407,8 @@ def main():
     cfg = wl.CONFIGS[args.workload]
     if args.experts:
         cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)
+    if args.router:
+        return run_router(args, cfg, wl)
     metric = ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if args.mode == "mxw4a4"
               else "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name))
     unit = "tokens/s"

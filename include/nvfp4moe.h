@@ -148,6 +148,26 @@ int mxfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, 
                              nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_router_logits -- the router scores that the routing step ranks ("The
+ * 2x Gap", section "The Investigation So Far": each token goes to 8 of 256
+ * experts by these scores):
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h]
+ * bf16 inputs, fp32 accumulation on the tensor cores, fp32 output.  K is
+ * split over the SMs and the partial sums are added in a fixed order, so
+ * the result is reproducible bit for bit.  Its output feeds
+ * moe_align_permute / moe_route_quantize_nvfp4 / _mxfp4 directly.
+ *   x bf16 [T, H]; w_router bf16 [E, H]; logits fp32 [T, E]
+ *   workspace >= moe_router_logits_workspace_bytes(T, H, E) (for the current
+ *   device: the split depends on its SM count)
+ *   dev_status: optional; a bounded device wait that runs out sets
+ *   NVFP4_E_DEVICE_TIMEOUT.
+ * Constraints: H % 64 == 0, T >= 0, E >= 1; pointers 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t moe_router_logits_workspace_bytes(int T, int H, int E);
+int moe_router_logits(const void* x, const void* w_router, int T, int H, int E, float* logits,
+                      int32_t* dev_status, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_align_permute -- router top-k plus the expert permutation.
  * Routing: "The 2x Gap", section "The Investigation So Far" (top-8 of 256
  * experts); "Native FP4 Is Slower ...", section 1 (22 of 512).  Per token t:

@@ -27,7 +27,8 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspac
            "nvfp4_pack_weight_scales", "moe_align_permute_workspace_bytes", "moe_align_permute",
            "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine", "moe_layer_workspace_bytes",
            "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4", "mxfp4_scale_pitch",
-           "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4")
+           "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4",
+           "moe_router_logits_workspace_bytes", "moe_router_logits")
 
 
 class Nvfp4Error(RuntimeError):
@@ -84,6 +85,10 @@ def load(build_if_missing: bool = True):
     L.moe_route_quantize_nvfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_align_permute_noalloc.restype = _I
     L.moe_align_permute_noalloc.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P, _P]
+    L.moe_router_logits_workspace_bytes.restype = _SZ
+    L.moe_router_logits_workspace_bytes.argtypes = [_I, _I, _I]
+    L.moe_router_logits.restype = _I
+    L.moe_router_logits.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _SZ, _P]
     L.mxfp4_scale_pitch.restype = _I64
     L.mxfp4_scale_pitch.argtypes = [_I64]
     L.mxfp4_quantize.restype = _I
@@ -188,6 +193,20 @@ def mxfp4_pack_weight_scales(scales_linear, E, N, K, out=None):
         out = _empty(E * N * (K // 32), torch.uint8, scales_linear.device)
     _check("mxfp4_pack_weight_scales",
            L.mxfp4_pack_weight_scales(_ptr(scales_linear), E, N, K, _ptr(out), _stream()))
+    return out
+
+
+def moe_router_logits(x, w_router, out=None, workspace=None, dev_status=None):
+    """logits [T, E] fp32 = x [T, H] bf16 . w_router [E, H] bf16 ^T."""
+    L = load()
+    T, H = x.shape
+    E = w_router.shape[0]
+    if out is None:
+        out = _empty((T, E), torch.float32, x.device)
+    if workspace is None:
+        workspace = _empty(int(L.moe_router_logits_workspace_bytes(T, H, E)), torch.uint8, x.device)
+    _check("moe_router_logits", L.moe_router_logits(_ptr(x), _ptr(w_router), T, H, E, _ptr(out), _ptr(dev_status),
+                                                    _ptr(workspace), workspace.numel(), _stream()))
     return out
 
 

@@ -159,6 +159,27 @@ int mxfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, 
       launch_mx_pack_scales(scales_linear, E, N, K, scales_packed, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_router_logits_workspace_bytes(int T, int H, int E) {
+  if (T < 0 || H < 0 || E < 0) return 0;
+  // at least 256 bytes, so that a non-null, aligned workspace always exists
+  const size_t b = router_workspace_bytes(T, H, E);
+  return b > 256 ? b : 256;
+}
+
+int moe_router_logits(const void* x, const void* w_router, int T, int H, int E, float* logits, int32_t* dev_status,
+                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0) return NVFP4_E_INVAL;
+  if (H % 64 != 0) return NVFP4_E_SHAPE;
+  if (T == 0) return NVFP4_OK;
+  if (x == nullptr || w_router == nullptr || logits == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return NVFP4_E_ALIGN;
+  if (workspace == nullptr || workspace_bytes < moe_router_logits_workspace_bytes(T, H, E)) return NVFP4_E_WORKSPACE;
+  if (!aligned16(workspace)) return NVFP4_E_ALIGN;
+  CHECK_ARCH();
+  return cuda_status(launch_router_logits(x, w_router, T, H, E, logits, workspace, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_align_permute_workspace_bytes(int T, int E, int k) {
   (void)k;
   if (T < 0 || E < 0) return 0;

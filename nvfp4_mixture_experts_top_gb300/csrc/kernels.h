@@ -54,6 +54,13 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
                               const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
                               int32_t* dev_status, cudaStream_t st);
 
+// Router logits [T, E] = x [T, H] . W [E, H]^T (bf16 in, fp32 out) on the
+// tensor cores, K split over the SMs; workspace holds the fp32 partials
+// (router_workspace_bytes; 0 when the problem is not split).
+size_t router_workspace_bytes(int T, int H, int E);
+cudaError_t launch_router_logits(const void* x_bf16, const void* w_bf16, int T, int H, int E, float* logits,
+                                 void* workspace, int32_t* dev_status, cudaStream_t st);
+
 // ---------------------------------------------------------------------------
 // MXFP4 (32-element blocks, UE8M0 scales)
 // ---------------------------------------------------------------------------
