@@ -122,8 +122,8 @@ int nvfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, 
  *   x * 2^-E.  No per-tensor scale.
  * Layouts: codes as NVFP4 (two per byte, element 2i in the low nibble);
  * activation scales [rows, mxfp4_scale_pitch(cols)] bytes, the row pitch
- * being cols/32 rounded up to a multiple of 16 (padding written as zero) so
- * that the grouped GEMM can fetch them with TMA.
+ * being cols/32 rounded up to a multiple of 16 and at least 128 (padding
+ * written as zero) so that the grouped GEMM fetches them efficiently with TMA.
  * Mode MOE_MXW4A4 of the grouped GEMM, SwiGLU/requant and layer calls runs
  * both operands in MXFP4 on tcgen05.mma kind::mxf4nvf4 .scale_vec::2X.
  * ------------------------------------------------------------------------ */

@@ -66,9 +66,14 @@ cudaError_t launch_router_logits(const void* x_bf16, const void* w_bf16, int T, 
 // ---------------------------------------------------------------------------
 
 // Row pitch in bytes of an MXFP4 scale tensor with `cols` columns: cols/32
-// rounded up to a multiple of 16 (TMA rows start on 16-byte boundaries); the
-// padding bytes are written as zero.
-__host__ __device__ constexpr int64_t mx_scale_pitch(int64_t cols) { return ((cols / 32 + 15) / 16) * 16; }
+// rounded up to a multiple of 16 (TMA rows start on 16-byte boundaries), and
+// at least 128: the grouped GEMM fetches 16 bytes of every row per two K
+// stages, and with rows narrower than a 128-byte line those fetches slowed
+// the whole kernel by a fifth (K = 2048) to a third (K = 1024) on GB300.
+// The padding bytes are written as zero.
+__host__ __device__ constexpr int64_t mx_scale_pitch(int64_t cols) {
+  return ((cols / 32 + 15) / 16) * 16 < 128 ? 128 : ((cols / 32 + 15) / 16) * 16;
+}
 
 cudaError_t launch_mx_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
                                uint8_t* scales, cudaStream_t st);

@@ -66,8 +66,9 @@ def test_mxfp4_host_side_without_gpu():
     checks, which run before any device call."""
     from nvfp4_mixture_experts_top_gb300 import binding
     L = binding.load()
-    # cols/32 rounded up to a multiple of 16 bytes
-    assert [L.mxfp4_scale_pitch(c) for c in (32, 256, 512, 768, 2048, 4096, 6144)] == [16, 16, 16, 32, 64, 128, 192]
+    # cols/32 rounded up to a multiple of 16 bytes, at least 128
+    assert [L.mxfp4_scale_pitch(c) for c in (32, 256, 2048, 4096, 4608, 6144, 8192)] == [128, 128, 128, 128, 144,
+                                                                                         192, 256]
     # cols not a multiple of 32 -> E_SHAPE; null outputs -> E_INVAL; bad dtype -> E_INVAL
     assert L.mxfp4_quantize(None, 0, 4, 48, 48, None, None, None) == 2
     assert L.mxfp4_quantize(None, 0, 4, 64, 64, None, None, None) == 1
