@@ -89,6 +89,40 @@ struct Params {
 };
 
 
+// Work unit u = (item, K split): the item and its K-chunk range [kc0, kc1).
+struct Unit {
+  WorkItem it;
+  int kc0, kc1;
+};
+__device__ __forceinline__ Unit unit_at(int u, int splits, int kch, const ItemTable& tab, int NT, int E) {
+  const int w = u / splits, split = u % splits;
+  Unit r;
+  r.it = decode_item<TOK_PER_PASS>(w, tab, NT, E);
+  r.kc0 = split * kch / splits;
+  r.kc1 = (split + 1) * kch / splits;
+  return r;
+}
+
+// A CTA's units, decoded once in the prologue (32 at a time, one per lane):
+// decoding costs ~1000 cycles of dependent latency (binary search, integer
+// divisions), which at a unit boundary stalled the producer and the MMA
+// issuer for a whole stage.  Units beyond the table are decoded on the fly.
+constexpr int kUnitTable = 256;
+__device__ __forceinline__ int4 pack_unit(const Unit& u) {
+  return make_int4(u.it.e | (u.it.nt << 16), u.it.r0, u.it.m1, u.kc0 | (u.kc1 << 12) | (u.it.ng << 24));
+}
+__device__ __forceinline__ Unit unpack_unit(int4 v) {
+  Unit u;
+  u.it.e = v.x & 0xFFFF;
+  u.it.nt = v.x >> 16;
+  u.it.r0 = v.y;
+  u.it.m1 = v.z;
+  u.kc0 = v.w & 0xFFF;
+  u.kc1 = (v.w >> 12) & 0xFFF;
+  u.it.ng = v.w >> 24;
+  return u;
+}
+
 // MX = false: NVFP4 (E4M3 scale per 16 elements, per-tensor fp32 scales,
 // kind::mxf4nvf4 .scale_vec::4X).  MX = true: MXFP4 (UE8M0 scale per 32
 // elements, no per-tensor scales, .scale_vec::2X); the weight scales arrive
@@ -111,7 +145,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
-  __shared__ int s_base[kMaxExperts + 1];
+  __shared__ ItemTable tab;
+  __shared__ int4 s_units[kUnitTable];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -142,14 +177,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   const ExpertRows xr{p.offsets, p.E, p.R};
-  if (warp == 2) build_item_prefix<TOK_PER_PASS>(xr, NT, s_base, lane);
+  if (warp == 2) {
+    build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
+    __syncwarp();
+    const int n_units = tab.base[p.E] * p.splits;
+    for (int j = lane; j < kUnitTable; j += 32) {
+      const int u = blockIdx.x + j * gridDim.x;
+      if (u >= n_units) break;
+      s_units[j] = pack_unit(unit_at(u, p.splits, KCH, tab, NT, p.E));
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   // work unit = (item, K split); splits is 1, or 2 when the items alone
   // cannot fill the GPU (the two K halves then add into a zeroed output)
-  const int units = s_base[p.E] * p.splits;
+  const int units = tab.base[p.E] * p.splits;
+  // unit number j of this CTA (u = blockIdx.x + j * gridDim.x)
+  auto unit_j = [&](int j, int u) -> Unit {
+    return j < kUnitTable ? unpack_unit(s_units[j]) : unit_at(u, p.splits, KCH, tab, NT, p.E);
+  };
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(p.offsets + p.E) != p.R || __ldg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
@@ -164,11 +212,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
     int it_p = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int w = u / p.splits, split = u % p.splits;
-      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
-      const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
-      const int e = it.e, nt = it.nt, r0 = it.r0, ng = it.ng;
+    for (int u = blockIdx.x, j = 0; ok && u < units; u += gridDim.x, ++j) {
+      const Unit cur = unit_j(j, u);
+      const int kc0 = cur.kc0, kc1 = cur.kc1;
+      const int e = cur.it.e, nt = cur.it.nt, r0 = cur.it.r0, ng = cur.it.ng;
       const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * (MX ? 256 : 512);
       {
         const uint32_t bytes = W_BYTES + WS_SRC_BYTES + (ng == 1 ? 1 : MAXG) * (A_BYTES + AS_BYTES);
@@ -231,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int w = u / p.splits, split = u % p.splits;
+      const int split = u % p.splits;
       const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
       {
         for (int kc = kc0; kc < kc1; ++kc) {
@@ -301,10 +348,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int it_c = 0;
     const uint32_t smem_base = smem_u32(smem);
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int w = u / p.splits, split = u % p.splits;
-      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
-      const int ng = decode_item<TOK_PER_PASS>(w, s_base, NT, xr).ng;
+    for (int u = blockIdx.x, j = 0; ok && u < units; u += gridDim.x, ++j) {
+      const Unit cur = unit_j(j, u);
+      const int kc0 = cur.kc0, kc1 = cur.kc1;
+      const int ng = cur.it.ng;
       {
         const uint32_t idesc = MX ? idesc_mxf4_ue8m0(BM, TG * ng) : idesc_mxf4nvf4(BM, TG * ng);
         if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
@@ -367,10 +414,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     int it_e = 0;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int w = u / p.splits, split = u % p.splits;
-      const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
-      const WorkItem it = decode_item<TOK_PER_PASS>(w, s_base, NT, xr);
+    for (int u = blockIdx.x, j = 0; ok && u < units; u += gridDim.x, ++j) {
+      const WorkItem it = unit_j(j, u).it;
       const int r0 = it.r0, m1 = it.m1, ng = it.ng;
       const float alpha = MX ? 1.0f : __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
       const int n = it.nt * BM + q * 32 + lane;

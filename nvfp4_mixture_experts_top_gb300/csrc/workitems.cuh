@@ -3,9 +3,10 @@
 // A work item is (expert e, 128-row weight tile nt, pass over up to TOK
 // tokens of the expert).  Items are numbered expert-major, then tile, then
 // pass, so the passes of one weight tile run on neighbouring CTAs at the same
-// time and share the tile through L2.  Each CTA builds s_base[e] (the number
-// of items of experts < e; s_base[E] = all items) from expert_offsets in
-// shared memory and finds an item's expert by binary search.
+// time and share the tile through L2.  Each CTA builds an ItemTable (the
+// number of items of experts < e, and each expert's rows) from
+// expert_offsets in shared memory and finds an item's expert by binary
+// search.
 #pragma once
 
 #include "common.cuh"
@@ -30,9 +31,20 @@ struct WorkItem {
   int e, nt, r0, m1, ng;  // expert, weight tile, first row, end row of the expert, token groups of 32
 };
 
-// One warp: s_base[0..E] (exclusive prefix of items per expert).
+// Shared-memory table of the routing, built once per CTA: the item prefix
+// and every expert's validated row range, so that finding an item's expert
+// and rows costs shared-memory reads only (two dependent global loads per
+// item cost ~1000 cycles at a work-item boundary, in every warp that decodes
+// the item).
+struct ItemTable {
+  int base[kMaxExperts + 1];  // items of experts < e; base[E] = all items
+  int m0[kMaxExperts];        // first row of expert e (validated)
+  int m1[kMaxExperts];        // end row of expert e (validated)
+};
+
+// One warp: fills the table from expert_offsets.
 template <int TOK>
-__device__ __forceinline__ void build_item_prefix(const ExpertRows& x, int NT, int* s_base, int lane) {
+__device__ __forceinline__ void build_item_table(const ExpertRows& x, int NT, ItemTable& tab, int lane) {
   int carry = 0;
   for (int e0 = 0; e0 < x.E; e0 += 32) {
     const int e = e0 + lane;
@@ -40,6 +52,8 @@ __device__ __forceinline__ void build_item_prefix(const ExpertRows& x, int NT, i
     if (e < x.E) {
       int m0, m1;
       expert_rows(x, e, m0, m1);
+      tab.m0[e] = m0;
+      tab.m1[e] = m1;
       cnt = NT * ((m1 - m0 + TOK - 1) / TOK);
     }
     int v = cnt;
@@ -48,25 +62,25 @@ __device__ __forceinline__ void build_item_prefix(const ExpertRows& x, int NT, i
       const int y = __shfl_up_sync(0xFFFFFFFFu, v, o);
       if (lane >= o) v += y;
     }
-    if (e < x.E) s_base[e] = carry + v - cnt;
+    if (e < x.E) tab.base[e] = carry + v - cnt;
     carry += __shfl_sync(0xFFFFFFFFu, v, 31);
   }
-  if (lane == 0) s_base[x.E] = carry;
+  if (lane == 0) tab.base[x.E] = carry;
 }
 
+// Item w -> (expert by binary search over the prefix, tile, pass, rows).
 template <int TOK>
-__device__ __forceinline__ WorkItem decode_item(int w, const int* s_base, int NT, const ExpertRows& x) {
-  int lo = 0, hi = x.E;  // s_base[lo] <= w < s_base[hi]
+__device__ __forceinline__ WorkItem decode_item(int w, const ItemTable& tab, int NT, int E) {
+  int lo = 0, hi = E;  // base[lo] <= w < base[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s_base[mid] <= w) lo = mid;
+    if (tab.base[mid] <= w) lo = mid;
     else hi = mid;
   }
   WorkItem it;
-  int m0, m1;
-  expert_rows(x, lo, m0, m1);
+  const int m0 = tab.m0[lo], m1 = tab.m1[lo];
   const int passes = (m1 - m0 + TOK - 1) / TOK;
-  const int local = w - s_base[lo];
+  const int local = w - tab.base[lo];
   it.e = lo;
   it.nt = local / passes;
   it.r0 = m0 + (local % passes) * TOK;
