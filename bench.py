@@ -109,7 +109,7 @@ def _kernel_hash(mode="w4a4"):
     """Hash of the sources of the dominant kernel of a mode (staleness check
     of the committed DRAM-traffic figure)."""
     h = hashlib.sha256()
-    for fn in ("gemm_%s.cu" % ("w4a4" if mode == "mxw4a4" else mode), "common.cuh"):
+    for fn in ("gemm_%s.cu" % ("w4a4" if mode == "mxw4a4" else mode), "common.cuh", "workitems.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

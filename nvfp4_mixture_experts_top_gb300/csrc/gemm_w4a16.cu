@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
   __shared__ ItemTable tab;
+  __shared__ int4 s_items[kItemSlots];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,12 +141,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&tmem_base_s, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
+  if (warp == 2) {
+    build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
+    __syncwarp();
+    for (int j = lane; j < kItemSlots; j += 32) {
+      const int w = blockIdx.x + j * gridDim.x;
+      if (w >= tab.base[p.E]) break;
+      s_items[j] = pack_item(decode_item<TOK_PER_PASS>(w, tab, NT, p.E));
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const int items = tab.base[p.E];
+  // item number j of this CTA (w = blockIdx.x + j * gridDim.x)
+  auto item_j = [&](int j, int w) -> WorkItem {
+    return j < kItemSlots ? unpack_item(s_items[j]) : decode_item<TOK_PER_PASS>(w, tab, NT, p.E);
+  };
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(p.offsets + p.E) != p.R || __ldg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
   }
@@ -158,8 +171,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0, issued_mask = 0, issued_par = 0;
     bool ok = true;
     int it_p = 0;
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const WorkItem it = decode_item<TOK_PER_PASS>(w, tab, NT, p.E);
+    for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
+      const WorkItem it = item_j(j, w);
       const uint8_t* wsc = p.w_scales + ((size_t)(it.e * NT + it.nt) * (p.K / 64)) * 512;
       const uint32_t bytes = W_BYTES + WS_BYTES + it.ng * NATOM * B_GROUP;
       for (int kc = 0; kc < KCH; ++kc) {
@@ -199,8 +212,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     int it_m = 0;
     const uint32_t smem_base = smem_u32(smem);
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const int ng = decode_item<TOK_PER_PASS>(w, tab, NT, p.E).ng;
+    for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
+      const int ng = item_j(j, w).ng;
       const uint32_t idesc = idesc_bf16(BM, TG * ng);
       if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
         ok = false;
@@ -253,8 +266,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const WorkItem it = decode_item<TOK_PER_PASS>(w, tab, NT, p.E);
+    for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
+      const WorkItem it = item_j(j, w);
       const float alpha = __ldg(p.w_S + it.e);
       const int n = it.nt * BM + q * 32 + lane;
       if (!warp_wait(&acc_full[acc], acc_phase, &abort_flag, p.dev_status)) {

@@ -89,4 +89,21 @@ __device__ __forceinline__ WorkItem decode_item(int w, const ItemTable& tab, int
   return it;
 }
 
+// A CTA's items decoded once in the prologue (decoding costs ~1000 cycles of
+// dependent latency, which at an item boundary stalls the warp that needs
+// it); packed as {e | nt << 16, r0, m1, ng}.
+constexpr int kItemSlots = 256;
+__device__ __forceinline__ int4 pack_item(const WorkItem& it) {
+  return make_int4(it.e | (it.nt << 16), it.r0, it.m1, it.ng);
+}
+__device__ __forceinline__ WorkItem unpack_item(int4 v) {
+  WorkItem it;
+  it.e = v.x & 0xFFFF;
+  it.nt = v.x >> 16;
+  it.r0 = v.y;
+  it.m1 = v.z;
+  it.ng = v.w;
+  return it;
+}
+
 }  // namespace nvfp4moe
