@@ -584,30 +584,23 @@ def main():
         ms_step = float(tt.item())
     value = world * T / (ms_step / 1e3)
 
-    # end to end through the one-call API with host buffers
-    x_h = x.cpu().pin_memory()
-    lg_h = logits.cpu().pin_memory()
-    out_h = torch.empty(T, H, dtype=torch.float32).pin_memory()
-    x_d = torch.empty_like(x)
-    lg_d = torch.empty_like(logits)
-    out_d = torch.empty_like(out)
-    wsl = torch.empty(B.moe_layer_workspace_bytes(mode, T, H, I, cfg.E, k), dtype=torch.uint8, device=dev)
-
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        lg_d.copy_(lg_h, non_blocking=True)
-        B.moe_layer_forward(mode, x_d, lg_d, k, w13, w2, S_h, out=out_d, workspace=wsl)
-        out_h.copy_(out_d, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-
+    # end to end through the public API with host buffers: MoELayerGraph
+    # replays the host->device copies of x and logits, moe_layer_forward and
+    # the device->host copy of the output as one graph; each step also waits
+    # for the result on the host
+    lg_graph = B.MoELayerGraph(mode, T, H, cfg.E, k, w13, w2, S_h, device=dev)
+    lg_graph.x_host.copy_(x.cpu())
+    lg_graph.logits_host.copy_(logits.cpu())
     for _ in range(args.warmup):
-        e2e_step()
+        lg_graph.run()
     te0 = time.perf_counter()
     for _ in range(K):
-        e2e_step()
+        res = lg_graph.run()
     e2e_s = (time.perf_counter() - te0) / K
-    if not torch.equal(out_h, out.cpu()):
+    if not torch.equal(res, out.cpu()):
         raise RuntimeError("e2e result differs from the device-timed step")
+    if int(lg_graph.dev_status.item()) != 0:
+        raise RuntimeError("device status %d in the e2e run" % int(lg_graph.dev_status.item()))
 
     hbm, _, peak_kind = _load_peaks()
     gemm_avg_ms = statistics.mean(gemm_ms)

@@ -167,3 +167,24 @@ def test_layer_decode_b512_full_size(orc):
 def test_layer_wide_full_size(orc, mode):
     dev = cuda_or_skip()
     _sampled_check(orc, wl.CONFIGS["wide"], mode, [5], dev)
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+def test_layer_graph_matches_one_call(orc, mode):
+    """MoELayerGraph (host copies + layer + copy back, replayed as one CUDA
+    graph) gives exactly moe_layer_forward's output, on two different
+    inputs in a row."""
+    dev = cuda_or_skip()
+    cfg = wl.CONFIGS["decode_c16"]
+    m = MODES[mode]
+    (g13, _), (g2, _) = gpu_weights(cfg, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    graph = B.MoELayerGraph(m, cfg.T, cfg.H, cfg.E, cfg.k, g13, g2, S_h, device=dev)
+    for seed in (0, 1):
+        x = wl.activations_bf16(cfg.T, cfg.H, seed=seed, device=dev)
+        logits = wl.router_logits(cfg, seed=seed, device=dev)
+        ref = B.moe_layer_forward(m, x, logits, cfg.k, g13, g2, S_h)
+        torch.cuda.synchronize()
+        got = graph.run(x.cpu(), logits.cpu())
+        assert torch.equal(got, ref.cpu()), seed
+        assert int(graph.dev_status.item()) == 0
