@@ -46,6 +46,23 @@ def _load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(v, world, device="cpu"):
+    """The largest value of v over the ranks of the job (the slowest replica
+    sets the job's step time); v itself when there is one rank."""
+    if world <= 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds_per_step):
+    """Whole-job throughput: every rank processes its own units (replicas)."""
+    return world * units_per_rank / seconds_per_step
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -577,12 +594,8 @@ def main():
     gemm_ms = [a.elapsed_time(b) for a, b in evs]
     if int(status.item()) != 0:
         raise RuntimeError("device status %d" % int(status.item()))
-    ms_step = ms_total / K
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    value = world * T / (ms_step / 1e3)
+    ms_step = max_over_ranks(ms_total / K, world, dev)
+    value = job_throughput(T, world, ms_step / 1e3)
 
     # end to end through the public API with host buffers: MoELayerGraph
     # replays the host->device copies of x and logits, moe_layer_forward and
@@ -596,7 +609,7 @@ def main():
     te0 = time.perf_counter()
     for _ in range(K):
         res = lg_graph.run()
-    e2e_s = (time.perf_counter() - te0) / K
+    e2e_s = max_over_ranks((time.perf_counter() - te0) / K, world, dev)
     if not torch.equal(res, out.cpu()):
         raise RuntimeError("e2e result differs from the device-timed step")
     if int(lg_graph.dev_status.item()) != 0:
@@ -623,7 +636,7 @@ def main():
         "layer_hbm": {"weight_bytes_per_step": layer_weight_bytes,
                       "achieved_gbs": layer_weight_bytes / (ms_step / 1e3) / 1e9,
                       "frac_of_peak": layer_weight_bytes / (ms_step / 1e3) / 1e9 / hbm},
-        "e2e": {"value": world * T / e2e_s, "unit": unit, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+        "e2e": {"value": job_throughput(T, world, e2e_s), "unit": unit, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 4},
         "gpu_launches": launches_per_step * K,
     }
