@@ -395,6 +395,20 @@ __device__ __forceinline__ void ew_tma_load_2d(void* smem_dst, const void* tmap,
       : "memory");
 }
 
+// TMA reduce-add of an fp32 shared-memory box into global memory (the add is
+// done in L2), tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* smem_src, int32_t x, int32_t y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   tmap),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's bulk groups have been read
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk groups have completed (their global writes are done)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void ew_bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
                                              uint64_t cache_policy) {
   asm volatile(

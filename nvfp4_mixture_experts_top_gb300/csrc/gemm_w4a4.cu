@@ -133,7 +133,8 @@ template <bool MX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_as, const __grid_constant__ CUtensorMap tm_a4,
-                     const __grid_constant__ CUtensorMap tm_as4, const Params p) {
+                     const __grid_constant__ CUtensorMap tm_as4, const __grid_constant__ CUtensorMap tm_out,
+                     const Params p) {
   // bytes of weight scales fetched per stage (MXFP4: two per row per MMA)
   constexpr uint32_t WS_SRC_BYTES = MX ? WS_BYTES / 2 : WS_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -147,6 +148,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ volatile int abort_flag;
   __shared__ ItemTable tab;
   __shared__ int4 s_units[kUnitTable];
+  // split-K epilogue staging: per epilogue warp a [32 tokens][32 rows] fp32 box
+  __shared__ __align__(128) float s_red[4][TG * 32];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -431,14 +434,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS + g * TG, r);
           tmem_ld_wait();
           const int tb = r0 + g * TG;
+          if (p.splits == 2 && tb + TG <= m1) {
+            // a full group of a K half: stage it as [token][row] and let TMA add
+            // it into the output in L2 (two halves onto zero: 0 + a + b == 0 +
+            // b + a, so the sum does not depend on their order)
+            float* box = s_red[q];
+            if (lane == 0) bulk_wait_read_all();  // the previous box has been read
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (tb + j < m1) {
-              float* dst = p.out + (size_t)(tb + j) * p.N + n;
-              const float v = __fmul_rn(__uint_as_float(r[j]), alpha);
-              // two K halves: 0 + a + b == 0 + b + a, so the sum is the same in either order
-              if (p.splits == 1) *dst = v;
-              else atomicAdd(dst, v);
+            for (int i = 0; i < 32; ++i) box[i * 32 + lane] = __fmul_rn(__uint_as_float(r[i]), alpha);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tm_out, box, it.nt * BM + q * 32, tb);
+              bulk_commit_group();
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (tb + i < m1) {
+                float* dst = p.out + (size_t)(tb + i) * p.N + n;
+                const float v = __fmul_rn(__uint_as_float(r[i]), alpha);
+                if (p.splits == 1) *dst = v;
+                else atomicAdd(dst, v);  // ragged group of a K half: same order argument
+              }
             }
           }
         }
@@ -453,6 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // reduce-adds complete before the CTA (and its boxes) go away
     __syncwarp();
   }
 
@@ -497,6 +517,10 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
   if (err != cudaSuccess) return err;
   err = make_tmap_2d_u8(&tm_as4, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, TOK_PER_PASS, 0);
   if (err != cudaSuccess) return err;
+  // output [R rows, N fp32]: destination of the split-K reduce-adds, box 32 x 32
+  CUtensorMap tm_out;
+  err = make_tmap_2d_f32(&tm_out, out, (uint64_t)N, (uint64_t)R, (uint64_t)N * 4, 32, TG);
+  if (err != cudaSuccess) return err;
   Params p;
   p.w_scales = w_scales_packed;
   p.w_S = w_S;
@@ -520,7 +544,7 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
-  gemm_w4a4_kernel<MX><<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4, p);
+  gemm_w4a4_kernel<MX><<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4, tm_out, p);
   return cudaGetLastError();
 }
 

@@ -14,4 +14,10 @@ namespace nvfp4moe {
 cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch,
                             uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
 
+// 2-D fp32 tensor [rows, inner] with row pitch `pitch_bytes`; box of
+// box_inner x box_rows elements, no swizzle (used as the destination of TMA
+// reduce-add; box elements outside the tensor are neither read nor written).
+cudaError_t make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                             uint32_t box_inner, uint32_t box_rows);
+
 }  // namespace nvfp4moe
