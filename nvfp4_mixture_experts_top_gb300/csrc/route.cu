@@ -14,7 +14,9 @@
 //       row = offsets[e] + (rows of expert e in earlier chunks)
 //                        + popcount(mask bits of earlier tokens in the chunk)
 //     which is stable by (expert, token) by construction; then it resets the
-//     counter.
+//     counter.  With a single chunk (T <= 32, decode) the one CTA does this
+//     straight from shared memory, without the round trips through global
+//     memory and the counter.
 // gather_kernel: one warp per permuted row, 16-byte vector copies.
 #include <math.h>
 
@@ -90,6 +92,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   __shared__ uint32_t mask[kMaxE];
   __shared__ int32_t base[kMaxE];
   __shared__ int32_t warp_tot[32];
+  __shared__ int32_t s_ids[kChunk * 32];  // this chunk's expert ids (k <= 32)
   __shared__ bool last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -121,24 +124,33 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     if (lane < k) {
       ids[(int64_t)t * k + lane] = my_id;
       w[(int64_t)t * k + lane] = my_w;
+      s_ids[warp * k + lane] = my_id;
       atomicOr(&mask[my_id], 1u << warp);
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = mask[e];
+  // a single chunk (T <= 32, the decode case) keeps everything in shared
+  // memory: no mask round trip through global memory, no counter
+  const bool single = (C == 1);
+  if (!single) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = mask[e];
 
-  // 3: the last chunk to finish does the scan and the scatter
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(counter, 1u) == (uint32_t)(C - 1));
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
+    // 3: the last chunk to finish does the scan and the scatter
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = (atomicAdd(counter, 1u) == (uint32_t)(C - 1));
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+  }
 
   const int e = threadIdx.x;
   int cnt = 0;
-  if (e < E)
-    for (int cc = 0; cc < C; ++cc) cnt += __popc(__ldcg(masks + (int64_t)cc * E + e));
+  if (e < E) {
+    if (single) cnt = __popc(mask[e]);
+    else
+      for (int cc = 0; cc < C; ++cc) cnt += __popc(__ldcg(masks + (int64_t)cc * E + e));
+  }
   int incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -173,18 +185,18 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
       const int tl = pidx / k, j = pidx % k;
       const int tt = cc * kChunk + tl;
       if (tt < T) {
-        const int ee = __ldcg(ids + (int64_t)tt * k + j);
-        const uint32_t m = __ldcg(masks + (int64_t)cc * E + ee);
+        const int ee = single ? s_ids[tl * k + j] : __ldcg(ids + (int64_t)tt * k + j);
+        const uint32_t m = single ? mask[ee] : __ldcg(masks + (int64_t)cc * E + ee);
         const int row = base[ee] + __popc(m & ((1u << tl) - 1u));
         perm[row] = tt;
         inv[(int64_t)tt * k + j] = row;
       }
     }
     __syncthreads();
-    if (e < E) base[e] += __popc(__ldcg(masks + (int64_t)cc * E + e));
+    if (e < E && !single) base[e] += __popc(__ldcg(masks + (int64_t)cc * E + e));
     __syncthreads();
   }
-  if (threadIdx.x == 0) *counter = 0;
+  if (threadIdx.x == 0 && !single) *counter = 0;
 }
 
 // One warp per permuted row: copy `row_bytes` (and `sc_bytes` of scales).
