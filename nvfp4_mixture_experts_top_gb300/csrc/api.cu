@@ -40,6 +40,24 @@ int num_sms() {
   return g_sms[d];
 }
 
+// cudaFuncAttributeMaxDynamicSharedMemorySize for `func` on the current
+// device, set once per (kernel, device): a process may drive several GPUs.
+cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
+  constexpr int kFuncs = 16;
+  static const void* funcs[kFuncs];
+  static bool done[kFuncs][kMaxDevices];
+  const int d = current_device();
+  if (d < 0) return cudaErrorInvalidDevice;
+  int i = 0;
+  while (i < kFuncs && funcs[i] != nullptr && funcs[i] != func) ++i;
+  if (i == kFuncs) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (funcs[i] == nullptr) funcs[i] = func;
+  if (done[i][d]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[i][d] = true;
+  return e;
+}
+
 static int device_check_impl() {
   const int d = current_device();
   if (d < 0) return NVFP4_E_CUDA;

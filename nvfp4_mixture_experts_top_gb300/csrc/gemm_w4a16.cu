@@ -72,6 +72,7 @@ struct Params {
   float* out;
   int32_t* dev_status;
   int E, N, K, R;
+  int drop_stage;  // fault injection for tests: producer stage index never armed (-1: none)
 };
 
 // 8 packed E2M1 codes (4 bytes, element 2i in the low nibble of byte i) times
@@ -182,6 +183,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         uint8_t* sb = smem + stage * RSTAGE_BYTES;
         if (lane == 0) W4A16_TRACE(0, it_p);
+        if (it_p == p.drop_stage) {
+          // fault injection (tests only): this stage is never armed, so the
+          // consumers' bounded waits run out and the kernel aborts cleanly
+          ++it_p;
+          if (++stage == RSTAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          continue;
+        }
         ew_arrive_expect_tx(&raw_full[stage], bytes);
         ew_tma_load_2d(sb + OFF_W, &tm_w, &raw_full[stage], kc * (KC / 2), it.e * p.N + it.nt * BM, pol_w);
         ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * NATOM * 512, WS_BYTES, &raw_full[stage], pol_w);
@@ -370,12 +381,9 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
   using namespace w4a16;
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a16_kernel), SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   CUtensorMap tm_w, tm_b;
   // raw weight codes: [E*N rows, K/2 bytes], box 128 B x 128 rows, 128-byte swizzle
@@ -395,6 +403,7 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
   p.N = N;
   p.K = K;
   p.R = R;
+  p.drop_stage = fault_injection_drop_stage();
   gemm_w4a16_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_b, p);
   return cudaGetLastError();
 }

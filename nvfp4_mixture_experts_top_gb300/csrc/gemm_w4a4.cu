@@ -492,12 +492,9 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
   using namespace w4a4;
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_w4a4_kernel<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a4_kernel<MX>), SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   CUtensorMap tm_w, tm_a, tm_as, tm_a4, tm_as4;
   cudaError_t err;

@@ -8,11 +8,16 @@ namespace nvfp4moe {
 
 int num_sms();  // SM count of the current device (cached)
 
+// Opt a kernel into `bytes` of dynamic shared memory on the current device
+// (once per kernel and device).
+cudaError_t ensure_dynamic_smem(const void* func, int bytes);
+
 // Fault injection for the failure-detection tests: the value of the
 // environment variable NVFP4MOE_TEST_DROP_STAGE (read at every launch), or -1
-// when it is unset.  A grouped GEMM launched with it set never arms that
-// pipeline stage, so its bounded waits run out: it reports
-// NVFP4_E_DEVICE_TIMEOUT in dev_status, drains, frees TMEM and returns.
+// when it is unset.  A grouped GEMM (W4A4, MXFP4, W4A16) or router GEMM
+// launched with it set never arms that pipeline stage, so its bounded waits
+// run out: it reports NVFP4_E_DEVICE_TIMEOUT in dev_status, drains, frees
+// TMEM and returns.
 int fault_injection_drop_stage();
 
 cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,

@@ -47,6 +47,7 @@ struct Params {
   int32_t* dev_status;
   int T, E, H;
   int mt, nt, splits;  // expert tiles, token tiles, K ranges
+  int drop_stage;      // fault injection for tests: stage index (per CTA) never armed (-1: none)
 };
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -102,6 +103,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       uint8_t* sb = smem + stage * STAGE_BYTES;
+      if (kc - kc0 == p.drop_stage) {
+        // fault injection (tests only): never armed; the MMA warp's bounded wait runs out
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        continue;
+      }
       ew_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
       // x coordinates are bytes: chunk kc = 64 bf16 = 128 bytes
       ew_tma_load_2d(sb, &tm_w, &full_bar[stage], kc * KC * 2, m * BM, pol_w);
@@ -207,11 +216,9 @@ cudaError_t launch_router_logits(const void* x_bf16, const void* w_bf16, int T, 
                                  void* workspace, int32_t* dev_status, cudaStream_t st) {
   using namespace router;
   if (T == 0 || E == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(router_gemm_kernel), SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   CUtensorMap tm_w, tm_x;
   // bf16 rows viewed as bytes: [rows, 2H], box 128 B x 128 rows, 128-byte swizzle
@@ -228,6 +235,7 @@ cudaError_t launch_router_logits(const void* x_bf16, const void* w_bf16, int T, 
   p.splits = choose_splits(T, H, E);
   p.out = p.splits > 1 ? static_cast<float*>(workspace) : logits;
   p.dev_status = dev_status;
+  p.drop_stage = fault_injection_drop_stage();
   router_gemm_kernel<<<p.mt * p.nt * p.splits, NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_x, p);
   err = cudaGetLastError();
   if (err != cudaSuccess || p.splits == 1) return err;

@@ -1,6 +1,6 @@
 """Failure detection on the GPU without faulting it.
 
-The grouped GEMM's waits are bounded.  With the test-only fault injection
+The grouped GEMMs' (W4A4 and W4A16) and the router GEMM's waits are bounded.  With the test-only fault injection
 (NVFP4MOE_TEST_DROP_STAGE: the producer never arms one pipeline stage) the
 consumers' waits run out: the kernel must report NVFP4_E_DEVICE_TIMEOUT in
 the status word, drain its copies and MMAs, free its tensor memory and
@@ -53,3 +53,49 @@ def test_gemm_bounded_wait_times_out_and_context_survives(orc):
     assert int(status.item()) == 0
     assert_close(out.cpu().numpy(), orc.grouped_gemm_w4a4(ac, as_, aS, w[0], w[1], w[2], offs), "after timeout")
     assert sum(counts) == 8
+
+
+def _drop_stage_zero(fn):
+    os.environ["NVFP4MOE_TEST_DROP_STAGE"] = "0"
+    try:
+        t0 = time.time()
+        fn()
+        torch.cuda.synchronize()
+        return time.time() - t0
+    finally:
+        del os.environ["NVFP4MOE_TEST_DROP_STAGE"]
+
+
+def test_w4a16_gemm_bounded_wait_times_out_and_context_survives(orc):
+    dev = cuda_or_skip()
+    E, N, K = 2, 128, 512
+    offs = np.array([0, 5, 8], np.int32)
+    w = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, N, K).numpy() for e in range(E)]))
+    a = wl.random_fp32((8, K), seed=2, tag="fail16").to(torch.bfloat16).float().numpy()
+    wd = upload_weights(w, E, N, K, dev)
+    args = (to_dev(a, dev, torch.bfloat16), None, None, *wd, to_dev(offs, dev), N, K)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    elapsed = _drop_stage_zero(lambda: B.moe_grouped_gemm_nvfp4(B.MOE_W4A16, *args, dev_status=status))
+    assert int(status.item()) == NVFP4_E_DEVICE_TIMEOUT
+    assert elapsed < 30.0
+    status.zero_()
+    out = B.moe_grouped_gemm_nvfp4(B.MOE_W4A16, *args, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(out.cpu().numpy(), orc.grouped_gemm_w4a16(a, w[0], w[1], w[2], offs), "w4a16 after timeout")
+
+
+def test_router_gemm_bounded_wait_times_out_and_context_survives(orc):
+    dev = cuda_or_skip()
+    T, H, E = 16, 1024, 256
+    x = wl.activations_bf16(T, H, seed=4)
+    wr = wl.router_weight_bf16(E, H, seed=4)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    elapsed = _drop_stage_zero(lambda: B.moe_router_logits(x.to(dev), wr.to(dev), dev_status=status))
+    assert int(status.item()) == NVFP4_E_DEVICE_TIMEOUT
+    assert elapsed < 30.0
+    status.zero_()
+    got = B.moe_router_logits(x.to(dev), wr.to(dev), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(got.cpu().numpy(), orc.router_logits(x.float().numpy(), wr.float().numpy()), "router after timeout")
