@@ -51,28 +51,37 @@ namespace w4a4 {
 constexpr int BM = 128;     // weight rows per tile
 constexpr int KC = 256;     // K elements per stage (= one 128-byte swizzle row)
 constexpr int TG = 32;      // tokens per group
-constexpr int MAXG = 4;     // token groups per pass
-constexpr int STAGES = 5;
-constexpr int TOK_PER_PASS = TG * MAXG;
 
 constexpr uint32_t W_BYTES = BM * KC / 2;    // 16384
-constexpr uint32_t A_BYTES = TG * KC / 2;    // 4096
+constexpr uint32_t A_BYTES = TG * KC / 2;    // 4096 per token group
 constexpr uint32_t WS_BYTES = BM * KC / 16;  // 2048: scale cells in shared memory
-constexpr uint32_t AS_BYTES = TG * KC / 16;  // 512
-constexpr uint32_t OFF_A = W_BYTES;                        // 16384
-constexpr uint32_t OFF_WS = OFF_A + MAXG * A_BYTES;         // 32768
-constexpr uint32_t OFF_AS = OFF_WS + WS_BYTES;              // 34816
-constexpr uint32_t STAGE_BYTES = OFF_AS + MAXG * AS_BYTES;  // 36864
-static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr uint32_t AS_BYTES = TG * KC / 16;  // 512 per token group
 
-// TMEM columns: two accumulators of 128 fp32 columns, then per stage 16
-// columns of weight scales and 16 of token scales (4 per K step each).
+// Ring geometry for passes of at most G token groups.  G = 4 (128 tokens per
+// pass, 36 KB stages, 5 stages) serves batches where experts see many tokens;
+// G = 1 (32 tokens per pass, 24 KB stages, 8 stages) serves sparse decode,
+// where a deeper ring keeps more weight bytes in flight per SM.  The token-
+// scale area always holds 4 groups: warp 6 transposes in place into 4 K-step
+// blocks of 4 cells.
+template <int G>
+struct Geo {
+  static constexpr int MAXG = G;
+  static constexpr int STAGES = G == 1 ? 8 : 5;
+  static constexpr int TOK_PER_PASS = TG * G;
+  static constexpr uint32_t OFF_A = W_BYTES;
+  static constexpr uint32_t OFF_WS = OFF_A + G * A_BYTES;
+  static constexpr uint32_t OFF_AS = OFF_WS + WS_BYTES;
+  static constexpr uint32_t STAGE_BYTES = OFF_AS + 4 * AS_BYTES;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  // TMEM columns: two accumulators of 32*G fp32 columns, then per stage 16
+  // columns of weight scales and 16 of token scales (4 per K step each)
+  static constexpr uint32_t ACC_COLS = TOK_PER_PASS;
+  static constexpr uint32_t SF_BASE = 2 * ACC_COLS;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(SF_BASE + STAGES * 32 <= 512, "TMEM budget");
+};
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = TOK_PER_PASS;  // 128
-constexpr uint32_t SF_BASE = 2 * ACC_COLS;   // 256
 constexpr uint32_t SF_STAGE = 32;
-static_assert(SF_BASE + STAGES * SF_STAGE <= TMEM_COLS, "TMEM budget");
 
 constexpr int NUM_THREADS = 224;  // 7 warps, roles above
 
@@ -94,10 +103,11 @@ struct Unit {
   WorkItem it;
   int kc0, kc1;
 };
+template <int TOK>
 __device__ __forceinline__ Unit unit_at(int u, int splits, int kch, const ItemTable& tab, int NT, int E) {
   const int w = u / splits, split = u % splits;
   Unit r;
-  r.it = decode_item<TOK_PER_PASS>(w, tab, NT, E);
+  r.it = decode_item<TOK>(w, tab, NT, E);
   r.kc0 = split * kch / splits;
   r.kc1 = (split + 1) * kch / splits;
   return r;
@@ -129,12 +139,18 @@ __device__ __forceinline__ Unit unpack_unit(int4 v) {
 // as 1 KB per stage (two bytes per row per MMA) and the activation scales as
 // rows of mx_scale_pitch(K) bytes, and warp 6 widens both into the 4-byte
 // per-row cells that tcgen05.cp copies to TMEM (bytes 2-3 zero).
-template <bool MX>
+template <bool MX, int G>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_as, const __grid_constant__ CUtensorMap tm_a4,
                      const __grid_constant__ CUtensorMap tm_as4, const __grid_constant__ CUtensorMap tm_out,
                      const Params p) {
+  using GE = Geo<G>;
+  constexpr int MAXG = GE::MAXG;
+  constexpr int STAGES = GE::STAGES;
+  constexpr int TOK_PER_PASS = GE::TOK_PER_PASS;
+  constexpr uint32_t OFF_A = GE::OFF_A, OFF_WS = GE::OFF_WS, OFF_AS = GE::OFF_AS, STAGE_BYTES = GE::STAGE_BYTES;
+  constexpr uint32_t ACC_COLS = GE::ACC_COLS, SF_BASE = GE::SF_BASE;
   // bytes of weight scales fetched per stage (MXFP4: two per row per MMA)
   constexpr uint32_t WS_SRC_BYTES = MX ? WS_BYTES / 2 : WS_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -187,7 +203,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int j = lane; j < kUnitTable; j += 32) {
       const int u = blockIdx.x + j * gridDim.x;
       if (u >= n_units) break;
-      s_units[j] = pack_unit(unit_at(u, p.splits, KCH, tab, NT, p.E));
+      s_units[j] = pack_unit(unit_at<TOK_PER_PASS>(u, p.splits, KCH, tab, NT, p.E));
     }
   }
   tc_fence_before();
@@ -199,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int units = tab.base[p.E] * p.splits;
   // unit number j of this CTA (u = blockIdx.x + j * gridDim.x)
   auto unit_j = [&](int j, int u) -> Unit {
-    return j < kUnitTable ? unpack_unit(s_units[j]) : unit_at(u, p.splits, KCH, tab, NT, p.E);
+    return j < kUnitTable ? unpack_unit(s_units[j]) : unit_at<TOK_PER_PASS>(u, p.splits, KCH, tab, NT, p.E);
   };
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint4 v[MAXG];
 #pragma unroll
           for (int g = 0; g < MAXG; ++g) v[g] = *reinterpret_cast<const uint4*>(as_tile + g * AS_BYTES + lane * 16);
-          uint32_t w[MAXG][4];
+          uint32_t w[4][4] = {};  // [group][K step]; groups beyond MAXG stay zero
           if constexpr (MX) {
             // this stage's 8 scale bytes of token (32g + lane): half kc & 1 of
             // the 16-byte row; the pair for MMA kk widens to one cell
@@ -484,8 +500,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace w4a4
 
-template <bool MX>
-static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
+template <bool MX, int G>
+static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
                                const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                                const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
                                cudaStream_t st) {
@@ -493,7 +509,7 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   {
-    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a4_kernel<MX>), SMEM_BYTES);
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a4_kernel<MX, G>), Geo<G>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tm_w, tm_a, tm_as, tm_a4, tm_as4;
@@ -510,9 +526,9 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
   err = make_tmap_2d_u8(&tm_as, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, TG, 0);
   if (err != cudaSuccess) return err;
   // the same two tensors with 128-row boxes (all token groups of a pass)
-  err = make_tmap_2d_u8(&tm_a4, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, TOK_PER_PASS, 128);
+  err = make_tmap_2d_u8(&tm_a4, a_codes, (uint64_t)K / 2, (uint64_t)R, (uint64_t)K / 2, KC / 2, Geo<G>::TOK_PER_PASS, 128);
   if (err != cudaSuccess) return err;
-  err = make_tmap_2d_u8(&tm_as4, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, TOK_PER_PASS, 0);
+  err = make_tmap_2d_u8(&tm_as4, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, Geo<G>::TOK_PER_PASS, 0);
   if (err != cudaSuccess) return err;
   // output [R rows, N fp32]: destination of the split-K reduce-adds, box 32 x 32
   CUtensorMap tm_out;
@@ -535,13 +551,31 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
   // Split K in two when even the largest possible number of work items,
   // tiles x (experts + R/128) passes, cannot fill every SM once.  Exactly two
   // partial sums keep the result independent of their arrival order.
-  const long long max_items = (long long)(N / BM) * ((long long)E + (R + TOK_PER_PASS - 1) / TOK_PER_PASS);
+  constexpr int TOK = Geo<G>::TOK_PER_PASS;
+  const long long max_items = (long long)(N / BM) * ((long long)E + (R + TOK - 1) / TOK);
   p.splits = (max_items < num_sms() && (K / KC) >= 2) ? 2 : 1;
   if (p.splits == 2) {
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
-  gemm_w4a4_kernel<MX><<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4, tm_out, p);
+  gemm_w4a4_kernel<MX, G><<<num_sms(), NUM_THREADS, Geo<G>::SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4,
+                                                                            tm_out, p);
+  return cudaGetLastError();
+}
+
+// Passes of 32 tokens and the 8-stage ring when the experts see few tokens on
+// average (sparse decode: every expert's weights stream once per 32 tokens,
+// which at <= 4 tokens per expert is almost always once), else passes of 128.
+template <bool MX>
+static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
+                               const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                               const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
+                               cudaStream_t st) {
+  if ((long long)R <= 4LL * E)
+    return launch_geo<MX, 1>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                             dev_status, st);
+  return launch_geo<MX, 4>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                           dev_status, st);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,10 @@ CASES = [
     ([0, 31, 32, 33, 64, 1, 0, 65], 384, 256),
     ([129, 0, 200, 5], 128, 1024),
     ([16] * 12, 512, 768),
+    # few tokens per expert on average (the 32-token-pass, 8-stage geometry),
+    # with a 40-token expert taking two passes, and a K-split case
+    ([40, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1], 256, 512),
+    ([2, 0, 3], 128, 1024),
 ]
 
 
