@@ -548,7 +548,10 @@ def main():
     gemm1_bytes = w13_bytes + act_in + R * 2 * I * 4
     layer_weight_bytes = w13_bytes + w2_bytes
 
-    # capture K steps with per-step events around the gate_up GEMM
+    # two graphs of K steps: the layer as it runs (kernels back to back, each
+    # a programmatic dependent of the one before), and the same steps with
+    # event nodes around every gate_up GEMM for its own duration (an event
+    # node between two kernels makes the second wait for the first's end)
     K = args.steps
     def timing_event():
         # recorded inside the captured graph: must be an external event node
@@ -558,12 +561,17 @@ def main():
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
+    graph_ev = torch.cuda.CUDAGraph()
     with torch.cuda.stream(side):
         with torch.cuda.graph(graph, stream=side):
             for i in range(K):
+                step()
+        with torch.cuda.graph(graph_ev, stream=side):
+            for i in range(K):
                 step(evs[i])
     torch.cuda.synchronize()
-    graph.replay()  # one untimed replay (graph upload)
+    graph.replay()  # one untimed replay of each (graph upload)
+    graph_ev.replay()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -586,6 +594,8 @@ def main():
     t1.record()
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
+    graph_ev.replay()  # the gate_up GEMM durations (second timed pass)
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     if not args.no_clocks:
@@ -628,7 +638,8 @@ def main():
                    "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "no flush: %.2f GB of touched weights per step >> 129 MB L2" % (layer_weight_bytes / 1e9),
-                   "timing": "CUDA graph of %d steps, CUDA events" % K},
+                   "timing": "CUDA graph of %d steps, CUDA events; gate_up duration from a second replay of "
+                             "the %d steps with events around each gate_up launch" % (K, K)},
         "roofline": {"kernel": "moe_grouped_gemm_nvfp4 gate_up (%s)" % args.mode, "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gemm1_bytes,

@@ -138,6 +138,18 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait: block until the grid this one
+// depends on (the preceding kernel on the stream) has completed and its
+// memory operations are visible; a no-op when the kernel was launched without
+// the programmatic-serialization attribute.  pdl_trigger: let the next grid
+// on the stream begin launching once every CTA of this grid has triggered or
+// exited.  Kernels of this library touch no global memory before pdl_wait
+// and trigger only after it (and after their TMEM allocation), so at most two
+// grids of a chain are resident and a waiting grid never holds TMEM that its
+// predecessor still has to allocate.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, copies
 // ---------------------------------------------------------------------------

@@ -42,6 +42,8 @@ __device__ __forceinline__ void load8<float>(const float* p, float* v) {
 template <typename T>
 __global__ void __launch_bounds__(256) amax_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
                                                    int64_t ld, uint32_t* __restrict__ amax_bits) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t vec_per_row = cols / 8;
   const int64_t nvec = rows * vec_per_row;
   float m = 0.0f;
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ x, 
                                                        int64_t ld, float* __restrict__ S, int dynamic,
                                                        const uint32_t* __restrict__ amax_bits,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_trigger();
   float s;
   if (dynamic) {
     s = __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f);
@@ -100,6 +104,8 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
                                                                const uint32_t* __restrict__ amax_bits,
                                                                float* __restrict__ S, uint8_t* __restrict__ codes,
                                                                uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_trigger();
   const float s = __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *S = s;
   const int64_t nb_row = H / 16;
@@ -150,6 +156,8 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
                                                              uint8_t* __restrict__ h_codes,
                                                              uint8_t* __restrict__ h_scales,
                                                              __nv_bfloat16* __restrict__ h_bf16) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nb_row = I / 16;
   const int64_t nblk = R * nb_row;
   const float s = (mode == MOE_W4A4) ? *S_h : 0.0f;
@@ -192,6 +200,8 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ Y, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int T, int k, int64_t H,
                                                       int out_dtype, void* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t q_per_row = H / 4;
   const int64_t total = (int64_t)T * q_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -228,6 +238,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) mx_quantize_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
                                                           int64_t ld, uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nb = cols / 32, pitch = mx_scale_pitch(cols);
   const int64_t total = rows * pitch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -250,6 +262,8 @@ __global__ void __launch_bounds__(256) mx_quantize_scatter_kernel(const __nv_bfl
                                                                   int64_t H, int k, const int32_t* __restrict__ inv,
                                                                   uint8_t* __restrict__ codes,
                                                                   uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nb = H / 32, pitch = mx_scale_pitch(H);
   const int64_t total = (int64_t)T * pitch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -288,6 +302,8 @@ __global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t* __re
 __global__ void __launch_bounds__(256) swiglu_requant_mx_kernel(const float* __restrict__ G, int64_t R, int64_t I,
                                                                 uint8_t* __restrict__ h_codes,
                                                                 uint8_t* __restrict__ h_scales) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nb = I / 32, pitch = mx_scale_pitch(I);
   const int64_t total = R * pitch;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -335,20 +351,18 @@ cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t co
     if (e != cudaSuccess) return e;
     const int g = grid_for(rows * cols / 8, 256);
     if (x_dtype == NVFP4_DT_BF16)
-      amax_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, amax_ws);
+      e = launch_pdl(amax_kernel<__nv_bfloat16>, g, 256, 0, st, static_cast<const __nv_bfloat16*>(x), rows, cols, ld,
+                     amax_ws);
     else
-      amax_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, amax_ws);
-    e = cudaGetLastError();
+      e = launch_pdl(amax_kernel<float>, g, 256, 0, st, static_cast<const float*>(x), rows, cols, ld, amax_ws);
     if (e != cudaSuccess) return e;
   }
   const int g = grid_for(rows * cols / 16, 256);
   if (x_dtype == NVFP4_DT_BF16)
-    quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, S,
-                                                      dynamic, amax_ws, codes, scales);
-  else
-    quantize_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, S, dynamic, amax_ws,
-                                              codes, scales);
-  return cudaGetLastError();
+    return launch_pdl(quantize_kernel<__nv_bfloat16>, g, 256, 0, st, static_cast<const __nv_bfloat16*>(x), rows,
+                      cols, ld, S, dynamic, static_cast<const uint32_t*>(amax_ws), codes, scales);
+  return launch_pdl(quantize_kernel<float>, g, 256, 0, st, static_cast<const float*>(x), rows, cols, ld, S, dynamic,
+                    static_cast<const uint32_t*>(amax_ws), codes, scales);
 }
 
 cudaError_t launch_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
@@ -356,9 +370,8 @@ cudaError_t launch_quantize_scatter(const void* x_bf16, int T, int H, int k, con
                                     cudaStream_t st) {
   const int64_t nblk = (int64_t)T * (H / 16);
   if (nblk == 0) return cudaSuccess;
-  quantize_scatter_kernel<<<grid_for(nblk, 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x_bf16), T, H, k,
-                                                               inv, amax_bits, S, codes, scales);
-  return cudaGetLastError();
+  return launch_pdl(quantize_scatter_kernel, grid_for(nblk, 256), 256, 0, st, static_cast<const __nv_bfloat16*>(x_bf16),
+                    T, (int64_t)H, k, inv, amax_bits, S, codes, scales);
 }
 
 cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st) {
@@ -372,17 +385,15 @@ cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const 
                                   uint8_t* h_scales, void* h_bf16, cudaStream_t st) {
   const int64_t nblk = (int64_t)R * (I / 16);
   if (nblk == 0) return cudaSuccess;
-  swiglu_requant_kernel<<<grid_for(nblk, 256), 256, 0, st>>>(G, R, I, mode, S_h, h_codes, h_scales,
-                                                             static_cast<__nv_bfloat16*>(h_bf16));
-  return cudaGetLastError();
+  return launch_pdl(swiglu_requant_kernel, grid_for(nblk, 256), 256, 0, st, G, (int64_t)R, (int64_t)I, mode, S_h,
+                    h_codes, h_scales, static_cast<__nv_bfloat16*>(h_bf16));
 }
 
 cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H, int out_dtype,
                            void* out, cudaStream_t st) {
   const int64_t total = (int64_t)T * (H / 4);
   if (total == 0) return cudaSuccess;
-  combine_kernel<<<grid_for(total, 256), 256, 0, st>>>(Y, inv, w, T, k, H, out_dtype, out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid_for(total, 256), 256, 0, st, Y, inv, w, T, k, (int64_t)H, out_dtype, out);
 }
 
 cudaError_t launch_mx_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,
@@ -391,20 +402,18 @@ cudaError_t launch_mx_quantize(const void* x, int x_dtype, int64_t rows, int64_t
   if (total == 0) return cudaSuccess;
   const int g = grid_for(total, 256);
   if (x_dtype == NVFP4_DT_BF16)
-    mx_quantize_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, codes,
-                                                         scales);
-  else
-    mx_quantize_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), rows, cols, ld, codes, scales);
-  return cudaGetLastError();
+    return launch_pdl(mx_quantize_kernel<__nv_bfloat16>, g, 256, 0, st, static_cast<const __nv_bfloat16*>(x), rows,
+                      cols, ld, codes, scales);
+  return launch_pdl(mx_quantize_kernel<float>, g, 256, 0, st, static_cast<const float*>(x), rows, cols, ld, codes,
+                    scales);
 }
 
 cudaError_t launch_mx_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv, uint8_t* codes,
                                        uint8_t* scales, cudaStream_t st) {
   const int64_t total = (int64_t)T * mx_scale_pitch(H);
   if (total == 0) return cudaSuccess;
-  mx_quantize_scatter_kernel<<<grid_for(total, 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x_bf16), T, H,
-                                                                   k, inv, codes, scales);
-  return cudaGetLastError();
+  return launch_pdl(mx_quantize_scatter_kernel, grid_for(total, 256), 256, 0, st,
+                    static_cast<const __nv_bfloat16*>(x_bf16), T, (int64_t)H, k, inv, codes, scales);
 }
 
 cudaError_t launch_mx_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st) {
@@ -418,8 +427,8 @@ cudaError_t launch_swiglu_requant_mx(const float* G, int R, int I, uint8_t* h_co
                                      cudaStream_t st) {
   const int64_t total = (int64_t)R * mx_scale_pitch(I);
   if (total == 0) return cudaSuccess;
-  swiglu_requant_mx_kernel<<<grid_for(total, 256), 256, 0, st>>>(G, R, I, h_codes, h_scales);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_requant_mx_kernel, grid_for(total, 256), 256, 0, st, G, (int64_t)R, (int64_t)I, h_codes,
+                    h_scales);
 }
 
 }  // namespace nvfp4moe

@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&tmem_base_s, TMEM_COLS);
     tmem_relinquish();
   }
+  // nothing above reads or writes global memory: launched as a programmatic
+  // dependent, this prologue overlaps the preceding kernel's tail
+  pdl_wait();
   if (warp == 2) {
     build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
     __syncwarp();
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();  // after this CTA's TMEM allocation
   const uint32_t tmem = tmem_base_s;
   const int items = tab.base[p.E];
   // item number j of this CTA (w = blockIdx.x + j * gridDim.x)
@@ -404,8 +408,7 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
   p.K = K;
   p.R = R;
   p.drop_stage = fault_injection_drop_stage();
-  gemm_w4a16_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_b, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_w4a16_kernel, num_sms(), NUM_THREADS, SMEM_BYTES, st, tm_w, tm_b, p);
 }
 
 }  // namespace nvfp4moe

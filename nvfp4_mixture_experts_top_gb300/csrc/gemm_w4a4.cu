@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&tmem_base_s, TMEM_COLS);
     tmem_relinquish();
   }
+  // nothing above reads or writes global memory: launched as a programmatic
+  // dependent, this prologue overlaps the preceding kernel's tail
+  pdl_wait();
   const ExpertRows xr{p.offsets, p.E, p.R};
   if (warp == 2) {
     build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();  // after this CTA's TMEM allocation
   const uint32_t tmem = tmem_base_s;
   // work unit = (item, K split); splits is 1, or 2 when the items alone
   // cannot fill the GPU (the two K halves then add into a zeroed output)
@@ -558,9 +562,8 @@ static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, c
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
-  gemm_w4a4_kernel<MX, G><<<num_sms(), NUM_THREADS, Geo<G>::SMEM_BYTES, st>>>(tm_w, tm_a, tm_as, tm_a4, tm_as4,
-                                                                            tm_out, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_w4a4_kernel<MX, G>, num_sms(), NUM_THREADS, Geo<G>::SMEM_BYTES, st, tm_w, tm_a, tm_as, tm_a4,
+                    tm_as4, tm_out, p);
 }
 
 // Passes of 32 tokens and the 8-stage ring when the experts see few tokens on
@@ -576,7 +579,6 @@ static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, 
                              dev_status, st);
   return launch_geo<MX, 4>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
                            dev_status, st);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,

@@ -4,9 +4,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace nvfp4moe {
 
 int num_sms();  // SM count of the current device (cached)
+
+// Launch `kernel` with programmatic stream serialization: it may begin while
+// the preceding kernel on the stream drains, and runs its global-memory-free
+// prologue (barrier setup, TMEM allocation, descriptor prefetch) in that
+// window; pdl_wait() inside the kernel orders everything else after the
+// predecessor.  Returns the launch status.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Opt a kernel into `bytes` of dynamic shared memory on the current device
 // (once per kernel and device).

@@ -94,10 +94,18 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t s_ids[kChunk * 32];  // this chunk's expert ids (k <= 32)
   __shared__ bool last;
+  __shared__ uint32_t s_amax;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const int C = gridDim.x;
+  // a single chunk (T <= 32, the decode case) keeps everything in shared
+  // memory: no mask round trip through global memory, no counter, and the
+  // activation amax is stored, not accumulated into a zeroed word
+  const bool single = (C == 1);
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0;
+  if (threadIdx.x == 0) s_amax = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
   // 1-2: top-k of this chunk's tokens, chunk mask (and, when x is given, the
@@ -115,7 +123,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) atomicMax(amax_bits, __float_as_uint(m));
+    if (lane == 0) atomicMax(single ? &s_amax : amax_bits, __float_as_uint(m));
   }
   if (t < T) {
     int my_id;
@@ -129,9 +137,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     }
   }
   __syncthreads();
-  // a single chunk (T <= 32, the decode case) keeps everything in shared
-  // memory: no mask round trip through global memory, no counter
-  const bool single = (C == 1);
+  if (single && x != nullptr && threadIdx.x == 0) *amax_bits = s_amax;
   if (!single) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = mask[e];
 
@@ -204,6 +210,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ in, const uint8_t* __restrict__ in_sc,
                                                      int64_t row_bytes, int64_t sc_bytes, uint8_t* __restrict__ out,
                                                      uint8_t* __restrict__ out_sc) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
@@ -226,20 +234,22 @@ cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t*
   const int C = (T + kChunk - 1) / kChunk;
   uint32_t* counter = static_cast<uint32_t*>(ws);      // word 0: chunk counter, word 1: activation amax
   uint32_t* masks = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
-  cudaError_t e = cudaMemsetAsync(counter, 0, 2 * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return e;
+  if (C > 1) {
+    // several chunks meet through the counter and accumulate the amax
+    const cudaError_t e = cudaMemsetAsync(counter, 0, 2 * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+  }
   const int nper = (E + 31) / 32;
-#define NVFP4MOE_ROUTE(NP)                                                                                   \
-  route_kernel<NP><<<C, 1024, 0, st>>>(logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, counter, masks, \
-                                       dev_status, static_cast<const __nv_bfloat16*>(x_bf16), H, counter + 1)
+#define NVFP4MOE_ROUTE(NP)                                                                                        \
+  return launch_pdl(route_kernel<NP>, C, 1024, 0, st, logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, counter, \
+                    masks, dev_status, static_cast<const __nv_bfloat16*>(x_bf16), (int64_t)H, counter + 1)
   if (nper <= 1) NVFP4MOE_ROUTE(1);
-  else if (nper <= 2) NVFP4MOE_ROUTE(2);
-  else if (nper <= 4) NVFP4MOE_ROUTE(4);
-  else if (nper <= 8) NVFP4MOE_ROUTE(8);
-  else if (nper <= 16) NVFP4MOE_ROUTE(16);
-  else NVFP4MOE_ROUTE(32);
+  if (nper <= 2) NVFP4MOE_ROUTE(2);
+  if (nper <= 4) NVFP4MOE_ROUTE(4);
+  if (nper <= 8) NVFP4MOE_ROUTE(8);
+  if (nper <= 16) NVFP4MOE_ROUTE(16);
+  NVFP4MOE_ROUTE(32);
 #undef NVFP4MOE_ROUTE
-  return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* act_in, const uint8_t* act_in_scales,
@@ -250,9 +260,8 @@ cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* 
   int blocks = (R + 7) / 8;
   const int cap = num_sms() * 8;
   if (blocks > cap) blocks = cap;
-  gather_kernel<<<blocks, 256, 0, st>>>(perm, R, static_cast<const uint8_t*>(act_in), act_in_scales, row_bytes,
-                                        sc_bytes, static_cast<uint8_t*>(act_out), act_out_scales);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, blocks, 256, 0, st, perm, R, static_cast<const uint8_t*>(act_in), act_in_scales,
+                    row_bytes, sc_bytes, static_cast<uint8_t*>(act_out), act_out_scales);
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,

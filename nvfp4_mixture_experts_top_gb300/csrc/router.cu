@@ -85,9 +85,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&tmem_base_s, TMEM_COLS);
     tmem_relinquish();
   }
+  // no global memory is touched above: as a programmatic dependent this
+  // prologue overlaps the preceding kernel's tail
+  pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();  // after this CTA's TMEM allocation
   const uint32_t tmem = tmem_base_s;
 
   if (warp == 0) {
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // logits[i] = sum over ranges s (in order) of partial[s][i]
 __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ partial, int64_t n,
                                                             int splits, float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     float acc = __ldg(partial + i);
     for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, __ldg(partial + (int64_t)s * n + i));
@@ -236,15 +242,13 @@ cudaError_t launch_router_logits(const void* x_bf16, const void* w_bf16, int T, 
   p.out = p.splits > 1 ? static_cast<float*>(workspace) : logits;
   p.dev_status = dev_status;
   p.drop_stage = fault_injection_drop_stage();
-  router_gemm_kernel<<<p.mt * p.nt * p.splits, NUM_THREADS, SMEM_BYTES, st>>>(tm_w, tm_x, p);
-  err = cudaGetLastError();
+  err = launch_pdl(router_gemm_kernel, p.mt * p.nt * p.splits, NUM_THREADS, SMEM_BYTES, st, tm_w, tm_x, p);
   if (err != cudaSuccess || p.splits == 1) return err;
   const int64_t n = (int64_t)T * E;
   int64_t blocks = (n + 255) / 256;
   const int64_t cap = (int64_t)num_sms() * 8;
-  router_reduce_kernel<<<(int)(blocks < cap ? blocks : cap), 256, 0, st>>>(static_cast<const float*>(workspace), n,
-                                                                          p.splits, logits);
-  return cudaGetLastError();
+  return launch_pdl(router_reduce_kernel, (int)(blocks < cap ? blocks : cap), 256, 0, st,
+                    static_cast<const float*>(workspace), n, p.splits, logits);
 }
 
 }  // namespace nvfp4moe
