@@ -534,9 +534,16 @@ def main():
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after warm-up" % int(status.item()))
     # the staged step and the one-call layer agree bit for bit
-    ref_out = B.moe_layer_forward(mode, x, logits, k, w13, w2, S_h)
+    layer_out = torch.empty(T, H, dtype=torch.float32, device=dev)
+    layer_ws = torch.empty(B.moe_layer_workspace_bytes(mode, T, H, I, cfg.E, k), dtype=torch.uint8, device=dev)
+
+    def layer_step():
+        B.moe_layer_forward(mode, x, logits, k, w13, w2, S_h, out=layer_out, workspace=layer_ws, dev_status=status)
+
+    for _ in range(args.warmup):
+        layer_step()
     torch.cuda.synchronize()
-    if not torch.equal(ref_out, out):
+    if not torch.equal(layer_out, out):
         raise RuntimeError("staged step and moe_layer_forward disagree")
 
     # touched experts -> algorithmic bytes
@@ -548,10 +555,11 @@ def main():
     gemm1_bytes = w13_bytes + act_in + R * 2 * I * 4
     layer_weight_bytes = w13_bytes + w2_bytes
 
-    # two graphs of K steps: the layer as it runs (kernels back to back, each
-    # a programmatic dependent of the one before), and the same steps with
-    # event nodes around every gate_up GEMM for its own duration (an event
-    # node between two kernels makes the second wait for the first's end)
+    # two graphs of K steps: the layer as a user runs it (K moe_layer_forward
+    # calls: kernels back to back, each a programmatic dependent of the one
+    # before), and the staged entry points with event nodes around every
+    # gate_up GEMM for its own duration (an event node between two kernels
+    # makes the second wait for the first's end)
     K = args.steps
     def timing_event():
         # recorded inside the captured graph: must be an external event node
@@ -565,7 +573,7 @@ def main():
     with torch.cuda.stream(side):
         with torch.cuda.graph(graph, stream=side):
             for i in range(K):
-                step()
+                layer_step()
         with torch.cuda.graph(graph_ev, stream=side):
             for i in range(K):
                 step(evs[i])
@@ -604,6 +612,8 @@ def main():
     gemm_ms = [a.elapsed_time(b) for a, b in evs]
     if int(status.item()) != 0:
         raise RuntimeError("device status %d" % int(status.item()))
+    if not torch.equal(layer_out, out):
+        raise RuntimeError("timed layer output differs from the staged step")
     ms_step = max_over_ranks(ms_total / K, world, dev)
     value = job_throughput(T, world, ms_step / 1e3)
 
@@ -638,8 +648,9 @@ def main():
                    "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "no flush: %.2f GB of touched weights per step >> 129 MB L2" % (layer_weight_bytes / 1e9),
-                   "timing": "CUDA graph of %d steps, CUDA events; gate_up duration from a second replay of "
-                             "the %d steps with events around each gate_up launch" % (K, K)},
+                   "timing": "CUDA graph of %d moe_layer_forward calls, CUDA events; gate_up duration from a "
+                             "second graph of the %d steps through the staged entry points with events around "
+                             "each gate_up launch" % (K, K)},
         "roofline": {"kernel": "moe_grouped_gemm_nvfp4 gate_up (%s)" % args.mode, "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gemm1_bytes,

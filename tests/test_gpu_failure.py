@@ -99,3 +99,43 @@ def test_router_gemm_bounded_wait_times_out_and_context_survives(orc):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert_close(got.cpu().numpy(), orc.router_logits(x.float().numpy(), wr.float().numpy()), "router after timeout")
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+@pytest.mark.parametrize("drop", [0, 3])
+def test_layer_bounded_wait_times_out_and_context_survives(orc, mode, drop):
+    """The whole layer (its kernels chained as programmatic dependents): a GEMM
+    stage that is never armed -- the first one, or one inside the first ring
+    lap (H = 2048: four K stages per gate_up work unit after the split) --
+    ends in a reported timeout, the kernels after it still run and return,
+    and the next layer call gives the oracle's result."""
+    dev = cuda_or_skip()
+    cfg = wl.MoEConfig("fail_layer", T=8, H=2048, I=512, E=4, k=2, routing="uniform")
+    m = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16}[mode]
+    xt = wl.activations_bf16(cfg.T, cfg.H, seed=5)
+    logits = wl.router_logits(cfg, seed=5)
+    w13 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, 5).numpy()
+                                         for e in range(cfg.E)]))
+    w2 = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, 5).numpy()
+                                        for e in range(cfg.E)]))
+    g13 = upload_weights(w13, cfg.E, 2 * cfg.I, cfg.H, dev)
+    g2 = upload_weights(w2, cfg.E, cfg.H, cfg.I, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    x, lg = xt.to(dev), logits.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    os.environ["NVFP4MOE_TEST_DROP_STAGE"] = str(drop)
+    try:
+        t0 = time.time()
+        B.moe_layer_forward(m, x, lg, cfg.k, g13, g2, S_h, dev_status=status)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["NVFP4MOE_TEST_DROP_STAGE"]
+    assert int(status.item()) == NVFP4_E_DEVICE_TIMEOUT
+    assert elapsed < 30.0
+    status.zero_()
+    out = B.moe_layer_forward(m, x, lg, cfg.k, g13, g2, S_h, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = orc.moe_layer(mode, xt.float().numpy(), logits.numpy(), cfg.k, w13, w2, cfg.S_h)
+    assert_close(out.cpu().numpy(), ref, "layer %s after timeout (drop %d)" % (mode, drop))
