@@ -303,6 +303,33 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
                       size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_layer_forward_host -- moe_layer_forward from and to page-locked host
+ * memory, for a caller whose step inputs arrive on the host and whose result
+ * is read there (one decode step end to end).  An interface convenience of
+ * this library: the computation is moe_layer_forward's.
+ *   x_host       bf16 [T, H], page-locked (cudaHostAlloc / registered)
+ *   logits_host  fp32 [T, E], page-locked
+ *   out_host     fp32 [T, H], page-locked; written by the device
+ *   other arguments as for moe_layer_forward
+ *   workspace    >= moe_layer_host_workspace_bytes(mode, T, H, I, E, k):
+ *                moe_layer_workspace_bytes plus device copies of x and logits
+ * The copies are kernels, not DMA transfers: a staging kernel reads x and
+ * logits over the host link into the workspace, and the combine kernel
+ * writes each output row straight into out_host, so the whole step is one
+ * chain of programmatically dependent kernels (no copy-engine nodes when
+ * captured in a graph).  The result is bitwise that of moe_layer_forward.
+ * out_host is complete once the stream's work up to this call has finished.
+ * Errors: NVFP4_E_INVAL if a buffer is not page-locked host memory; the
+ * other codes as for moe_layer_forward.
+ * ------------------------------------------------------------------------ */
+size_t moe_layer_host_workspace_bytes(int mode, int T, int H, int I, int E, int k);
+int moe_layer_forward_host(int mode, const void* x_host, const float* logits_host, int T, int H, int I, int E, int k,
+                           const uint8_t* w13_codes, const uint8_t* w13_scales_packed, const float* w13_S,
+                           const uint8_t* w2_codes, const uint8_t* w2_scales_packed, const float* w2_S,
+                           const float* S_h, float* out_host, int32_t* dev_status, void* workspace,
+                           size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_align_permute_noalloc -- moe_align_permute for callers that cannot
  * give the library scratch memory.  (The reference pages have no counterpart:
  * this is an interface convenience of this library, not a step of the method.)

@@ -28,7 +28,8 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspac
            "moe_grouped_gemm_nvfp4", "moe_swiglu_requant", "moe_combine", "moe_layer_workspace_bytes",
            "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4", "mxfp4_scale_pitch",
            "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4",
-           "moe_router_logits_workspace_bytes", "moe_router_logits")
+           "moe_router_logits_workspace_bytes", "moe_router_logits", "moe_layer_host_workspace_bytes",
+           "moe_layer_forward_host")
 
 
 class Nvfp4Error(RuntimeError):
@@ -81,6 +82,11 @@ def load(build_if_missing: bool = True):
     L.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
     L.moe_layer_forward.restype = _I
     L.moe_layer_forward.argtypes = [_I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_layer_host_workspace_bytes.restype = _SZ
+    L.moe_layer_host_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+    L.moe_layer_forward_host.restype = _I
+    L.moe_layer_forward_host.argtypes = [_I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                         _P]
     L.moe_route_quantize_nvfp4.restype = _I
     L.moe_route_quantize_nvfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.moe_align_permute_noalloc.restype = _I
@@ -106,6 +112,12 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
+    return C.c_void_p(t.data_ptr())
+
+
+def _hptr(t):
+    if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+        raise ValueError("expected a contiguous page-locked (pinned) CPU tensor")
     return C.c_void_p(t.data_ptr())
 
 
@@ -356,13 +368,42 @@ def moe_layer_forward(mode, x, logits, k, w13, w2, S_h, out=None, workspace=None
     return out
 
 
+def moe_layer_host_workspace_bytes(mode, T, H, I, E, k):
+    return int(load().moe_layer_host_workspace_bytes(mode, T, H, I, E, k))
+
+
+def moe_layer_forward_host(mode, x_host, logits_host, k, w13, w2, S_h, out_host=None, workspace=None,
+                           dev_status=None):
+    """Whole layer from and to page-locked host memory: x_host bf16 [T, H]
+    and logits_host fp32 [T, E] pinned CPU tensors; returns out_host, a
+    pinned fp32 [T, H] CPU tensor the device writes (valid once the current
+    stream has reached this point).  w13 / w2 as for moe_layer_forward."""
+    for t in (x_host, logits_host) + (() if out_host is None else (out_host,)):
+        _hptr(t)  # rejects device, pageable or strided tensors before any work
+    L = load()
+    T, H = x_host.shape
+    E = logits_host.shape[1]
+    I = w2[0].shape[2] * 2
+    dev = w13[0].device
+    if out_host is None:
+        out_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    if workspace is None:
+        workspace = _empty(moe_layer_host_workspace_bytes(mode, T, H, I, E, k), torch.uint8, dev)
+    _check("moe_layer_forward_host",
+           L.moe_layer_forward_host(mode, _hptr(x_host), _hptr(logits_host), T, H, I, E, k, _ptr(w13[0]),
+                                    _ptr(w13[1]), _ptr(w13[2]), _ptr(w2[0]), _ptr(w2[1]), _ptr(w2[2]), _ptr(S_h),
+                                    _hptr(out_host), _ptr(dev_status), _ptr(workspace), workspace.numel(),
+                                    _stream()))
+    return out_host
+
+
 class MoELayerGraph:
-    """moe_layer_forward for fixed shapes and weights, replayed as one CUDA
-    graph together with its host transfers: the copy of x and logits from
-    pinned host buffers, the whole layer, and the copy of the output back to
-    a pinned host buffer.  A decode step of many small kernels is dominated
-    by launch overhead otherwise (the CUDA-graph lesson of "Native FP4 Is
-    Slower Than Emulated FP4", section 3).
+    """moe_layer_forward_host for fixed shapes and weights, replayed as one
+    CUDA graph: x and logits are read from pinned host buffers and the output
+    is written to a pinned host buffer by the layer's own kernels, so the
+    graph is one chain of kernels.  A decode step of many small kernels is
+    dominated by launch overhead otherwise (the CUDA-graph lesson of "Native
+    FP4 Is Slower Than Emulated FP4", section 3).
 
     Usage: g = MoELayerGraph(mode, T, H, E, k, w13, w2, S_h); write the step's
     inputs into g.x_host / g.logits_host (or pass them to run()); g.run()
@@ -374,19 +415,13 @@ class MoELayerGraph:
         self.x_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
         self.logits_host = torch.empty(T, E, dtype=torch.float32).pin_memory()
         self.out_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
-        self._x = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-        self._lg = torch.empty(T, E, dtype=torch.float32, device=dev)
-        self._out = torch.empty(T, H, dtype=torch.float32, device=dev)
-        self._ws = torch.empty(moe_layer_workspace_bytes(mode, T, H, I, E, k), dtype=torch.uint8, device=dev)
+        self._ws = torch.empty(moe_layer_host_workspace_bytes(mode, T, H, I, E, k), dtype=torch.uint8, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         args = (mode, k, w13, w2, S_h)
 
         def body():
-            self._x.copy_(self.x_host, non_blocking=True)
-            self._lg.copy_(self.logits_host, non_blocking=True)
-            moe_layer_forward(args[0], self._x, self._lg, args[1], args[2], args[3], args[4], out=self._out,
-                              workspace=self._ws, dev_status=self.dev_status)
-            self.out_host.copy_(self._out, non_blocking=True)
+            moe_layer_forward_host(args[0], self.x_host, self.logits_host, args[1], args[2], args[3], args[4],
+                                   out_host=self.out_host, workspace=self._ws, dev_status=self.dev_status)
 
         self.x_host.zero_()
         self.logits_host.zero_()

@@ -476,4 +476,52 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
   return moe_combine(w.Y, w.inv, w.w, T, k, H, NVFP4_DT_F32, out, stream);
 }
 
+// Device view of page-locked host memory; false for any other pointer.
+static bool host_view(const void* p, void** dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return false;
+  *dev = a.devicePointer;
+  return true;
+}
+
+size_t moe_layer_host_workspace_bytes(int mode, int T, int H, int I, int E, int k) {
+  if (T < 0 || H < 0 || I < 0 || E < 0 || k < 0) return 0;
+  return moe_layer_workspace_bytes(mode, T, H, I, E, k) + align256((size_t)T * H * 2) + align256((size_t)T * E * 4);
+}
+
+int moe_layer_forward_host(int mode, const void* x_host, const float* logits_host, int T, int H, int I, int E, int k,
+                           const uint8_t* w13_codes, const uint8_t* w13_scales_packed, const float* w13_S,
+                           const uint8_t* w2_codes, const uint8_t* w2_scales_packed, const float* w2_S,
+                           const float* S_h, float* out_host, int32_t* dev_status, void* workspace,
+                           size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4) return NVFP4_E_INVAL;
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
+  if (H % 256 != 0 || I % 256 != 0 || k > E || k > 32 || E > 1024) return NVFP4_E_SHAPE;
+  if (T == 0) return NVFP4_OK;
+  if (x_host == nullptr || logits_host == nullptr || out_host == nullptr) return NVFP4_E_INVAL;
+  if (workspace == nullptr || workspace_bytes < moe_layer_host_workspace_bytes(mode, T, H, I, E, k))
+    return NVFP4_E_WORKSPACE;
+  if (!aligned16(workspace) || !aligned16(x_host) || !aligned16(out_host) ||
+      (reinterpret_cast<uintptr_t>(logits_host) & 3u) != 0)
+    return NVFP4_E_ALIGN;
+  CHECK_ARCH();
+  void *xd, *ld, *od;
+  if (!host_view(x_host, &xd) || !host_view(logits_host, &ld) || !host_view(out_host, &od)) return NVFP4_E_INVAL;
+  // the inputs' device copies sit after the layer's own workspace
+  const size_t layer_bytes = moe_layer_workspace_bytes(mode, T, H, I, E, k);
+  uint8_t* x_dev = static_cast<uint8_t*>(workspace) + layer_bytes;
+  float* lg_dev = reinterpret_cast<float*>(x_dev + align256((size_t)T * H * 2));
+  if (launch_stage_in(xd, x_dev, (int64_t)T * H * 2, ld, lg_dev, (int64_t)T * E * 4,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NVFP4_E_CUDA;
+  // the combine kernel writes the output straight into the host buffer
+  return moe_layer_forward(mode, x_dev, lg_dev, T, H, I, E, k, w13_codes, w13_scales_packed, w13_S, w2_codes,
+                           w2_scales_packed, w2_S, S_h, static_cast<float*>(od), dev_status, workspace, layer_bytes,
+                           stream);
+}
+
 }  // extern "C"

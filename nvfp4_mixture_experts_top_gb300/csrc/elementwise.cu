@@ -331,6 +331,41 @@ __global__ void __launch_bounds__(256) swiglu_requant_mx_kernel(const float* __r
 }
 
 // ---------------------------------------------------------------------------
+// host -> device staging of a layer's inputs (page-locked host memory read by
+// SM loads over the host link): range 0 in 16-byte units, range 1 in 4-byte
+// units.  Each thread keeps kStageILP loads in flight before it stores, so
+// the copy costs a few link round trips rather than one per element.
+// ---------------------------------------------------------------------------
+
+constexpr int kStageILP = 4;
+
+__global__ void __launch_bounds__(256) stage_in_kernel(const uint4* s0, uint4* __restrict__ d0, int64_t n0,
+                                                       const uint32_t* s1, uint32_t* __restrict__ d1, int64_t n1) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  for (int64_t i = t; i < n0; i += kStageILP * stride) {
+    uint4 v[kStageILP];
+#pragma unroll
+    for (int u = 0; u < kStageILP; ++u)
+      if (i + u * stride < n0) v[u] = s0[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < kStageILP; ++u)
+      if (i + u * stride < n0) d0[i + u * stride] = v[u];
+  }
+  for (int64_t i = t; i < n1; i += kStageILP * stride) {
+    uint32_t v[kStageILP];
+#pragma unroll
+    for (int u = 0; u < kStageILP; ++u)
+      if (i + u * stride < n1) v[u] = s1[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < kStageILP; ++u)
+      if (i + u * stride < n1) d1[i + u * stride] = v[u];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 
@@ -429,6 +464,19 @@ cudaError_t launch_swiglu_requant_mx(const float* G, int R, int I, uint8_t* h_co
   if (total == 0) return cudaSuccess;
   return launch_pdl(swiglu_requant_mx_kernel, grid_for(total, 256), 256, 0, st, G, (int64_t)R, (int64_t)I, h_codes,
                     h_scales);
+}
+
+cudaError_t launch_stage_in(const void* src16, void* dst16, int64_t bytes16, const void* src4, void* dst4,
+                            int64_t bytes4, cudaStream_t st) {
+  const int64_t n0 = bytes16 / 16, n1 = bytes4 / 4;
+  const int64_t n = n0 > n1 ? n0 : n1;
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 4;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(stage_in_kernel, (int)blocks, 256, 0, st, static_cast<const uint4*>(src16),
+                    static_cast<uint4*>(dst16), n0, static_cast<const uint32_t*>(src4), static_cast<uint32_t*>(dst4),
+                    n1);
 }
 
 }  // namespace nvfp4moe

@@ -50,6 +50,11 @@ cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const 
                                   uint8_t* h_scales, void* h_bf16, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H,
                            int out_dtype, void* out, cudaStream_t st);
+// Copy bytes16 (a multiple of 16) from src16 to dst16 and bytes4 (a multiple
+// of 4) from src4 to dst4 with SM loads: the sources may be page-locked host
+// memory (device views of it), read over the host link.
+cudaError_t launch_stage_in(const void* src16, void* dst16, int64_t bytes16, const void* src4, void* dst4,
+                            int64_t bytes4, cudaStream_t st);
 
 // Routing: top-k + stable counting sort + optional gather.  ws must hold
 // route_workspace_bytes(T, E).

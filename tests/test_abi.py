@@ -83,3 +83,19 @@ def test_mxfp4_host_side_without_gpu():
     assert L.moe_swiglu_requant(ctypes.c_void_p(16), 4, 48, 2, None, ctypes.c_void_p(16), ctypes.c_void_p(16),
                                 None, None) == 2
     assert L.moe_layer_workspace_bytes(2, 16, 4096, 2048, 256, 8) > 16 * 8 * 2 * 2048 * 4
+
+
+def test_host_layer_entry_rejects_device_or_pageable_buffers_without_gpu():
+    """moe_layer_forward_host takes page-locked CPU tensors only; the binding
+    refuses others before doing any work."""
+    import pytest
+    import torch
+    from nvfp4_mixture_experts_top_gb300 import binding
+    x = torch.zeros(2, 256, dtype=torch.bfloat16)  # pageable
+    lg = torch.zeros(2, 8, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        binding.moe_layer_forward_host(binding.MOE_W4A4, x, lg, 2, None, None, None)
+    L = binding.load()
+    assert L.moe_layer_host_workspace_bytes(0, 16, 4096, 2048, 256, 8) == (
+        L.moe_layer_workspace_bytes(0, 16, 4096, 2048, 256, 8) + 16 * 4096 * 2 + 16 * 256 * 4)
+    assert L.moe_layer_host_workspace_bytes(0, -1, 4096, 2048, 256, 8) == 0

@@ -171,9 +171,9 @@ def test_layer_wide_full_size(orc, mode):
 
 @pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
 def test_layer_graph_matches_one_call(orc, mode):
-    """MoELayerGraph (host copies + layer + copy back, replayed as one CUDA
-    graph) gives exactly moe_layer_forward's output, on two different
-    inputs in a row."""
+    """MoELayerGraph (moe_layer_forward_host from pinned host buffers,
+    replayed as one CUDA graph) gives exactly moe_layer_forward's output, on
+    two different inputs in a row."""
     dev = cuda_or_skip()
     cfg = wl.CONFIGS["decode_c16"]
     m = MODES[mode]
@@ -188,3 +188,34 @@ def test_layer_graph_matches_one_call(orc, mode):
         got = graph.run(x.cpu(), logits.cpu())
         assert torch.equal(got, ref.cpu()), seed
         assert int(graph.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16", "mxw4a4"])
+@pytest.mark.parametrize("shape", [(16, 4096, 2048, 256, 8), (3, 256, 512, 7, 2), (40, 1024, 256, 64, 4)])
+def test_layer_host_entry_matches_device_entry(orc, mode, shape):
+    """moe_layer_forward_host (inputs staged from pinned host memory by a
+    kernel, output written to pinned host memory by the combine kernel) is
+    bitwise moe_layer_forward on device copies of the same inputs -- also
+    for a logits row of 7 experts (28 bytes: not a multiple of 16) and for
+    more than one routing chunk (40 tokens)."""
+    dev = cuda_or_skip()
+    T, H, I, E, k = shape
+    cfg = wl.MoEConfig("host_entry", T=T, H=H, I=I, E=E, k=k, routing="uniform")
+    m = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4}[mode]
+    if mode == "mxw4a4":
+        from test_gpu_mx import gpu_mx_weights
+        (g13, _), (g2, _) = gpu_mx_weights(cfg, dev)
+    else:
+        (g13, _), (g2, _) = gpu_weights(cfg, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    x = wl.activations_bf16(T, H, seed=3, device=dev)
+    logits = wl.router_logits(cfg, seed=3, device=dev)
+    ref = B.moe_layer_forward(m, x, logits, k, g13, g2, S_h)
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = B.moe_layer_forward_host(m, xh, lh, k, g13, g2, S_h, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(got, ref.cpu())
+
