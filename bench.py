@@ -266,7 +266,8 @@ def run_gemm_sweep(args, wl):
     del w
     L = B.load()
     rows = []
-    for M in wl.GEMM_SWEEP["Ms"]:
+    Ms = [int(m) for m in args.sweep_ms.split(",")] if args.sweep_ms else list(wl.GEMM_SWEEP["Ms"])
+    for M in Ms:
         a, _ = wl.gemm_operands_fp32(M, 1, K, device=dev)
         ac, as_, aS = B.nvfp4_quantize(a)
         del a
@@ -315,12 +316,13 @@ def run_gemm_sweep(args, wl):
                      "frac_of_roofline": roof_us / us, "bound": "hbm" if per_copy / (hbm * 1e9) > flops / (
                          fp4_peak * 1e12) else "tensor", "copies": copies})
         del Ws, As, outs, g
-    m512 = [r for r in rows if r["M"] == 512][0]
-    result = {"metric": "FP4 TFLOPS at M=512 (single-expert NVFP4 GEMM, N=2048, K=6144)", "value": m512["tflops"],
+    m512 = ([r for r in rows if r["M"] == 512] or rows)[0]
+    result = {"metric": "FP4 TFLOPS at M=%d (single-expert NVFP4 GEMM, N=2048, K=6144)" % m512["M"],
+              "value": m512["tflops"],
               "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
               "ms_per_step": m512["us"] / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
               "dtype": "fp4(e2m1)xfp4, fp32 accumulate", "data": "synthetic",
-              "config": {"workload": "gemm_sweep", "N": N, "K": K, "Ms": list(wl.GEMM_SWEEP["Ms"]),
+              "config": {"workload": "gemm_sweep", "N": N, "K": K, "Ms": Ms,
                          "l2": "rotating %d+ operand copies > 2x L2" % min(r["copies"] for r in rows)},
               "roofline": {"bound": m512["bound"], "achieved": m512["tflops"], "peak": fp4_peak, "unit": "TFLOP/s",
                            "frac": m512["tflops"] / fp4_peak,
@@ -413,6 +415,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--router", action="store_true",
                     help="time the router-logits GEMM for the workload's T, H, E instead of the layer")
+    ap.add_argument("--sweep-ms", default="",
+                    help="gemm_sweep: comma-separated subset of the M values (e.g. for a profiler capture)")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (smaller device footprint for profiler captures)")
     args = ap.parse_args()
@@ -604,11 +608,21 @@ def main():
     torch.cuda.profiler.stop()
     graph_ev.replay()  # the gate_up GEMM durations (second timed pass)
     torch.cuda.synchronize()
+    # spread: five more replays of the layer graph after the timed one
+    spread = [ms_total_timed := t0.elapsed_time(t1)]
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        spread.append(a.elapsed_time(b))
+    spread = sorted(v / K for v in spread)
     if world > 1:
         dist.barrier()
     if not args.no_clocks:
         clocks.stop()
-    ms_total = t0.elapsed_time(t1)
+    ms_total = ms_total_timed
     gemm_ms = [a.elapsed_time(b) for a, b in evs]
     if int(status.item()) != 0:
         raise RuntimeError("device status %d" % int(status.item()))
@@ -661,6 +675,9 @@ def main():
         "e2e": {"value": job_throughput(T, world, e2e_s), "unit": unit, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 4},
         "gpu_launches": launches_per_step * K,
+        "spread": {"replays": len(spread), "ms_per_step_min": spread[0],
+                   "ms_per_step_median": statistics.median(spread), "ms_per_step_max": spread[-1],
+                   "note": "the timed replay and five more of the same graph"},
     }
     if not args.no_clocks:
         result["clocks"] = clocks.summary()
