@@ -206,15 +206,22 @@ def oracle_sample(cfg, mode, ntok, seed=0):
     return run
 
 
-def cpu_baseline(cfg, mode, ntok, seed=0):
+def cpu_baseline(cfg, mode, ntok, seconds=10.0, seed=0):
     """Time the oracle (as it stands) on the first `ntok` tokens of the
-    workload on the host cores.  Returns (tokens/s, cores, seconds)."""
+    workload on the host cores, repeating the sample until at least `seconds`
+    of oracle work have run.  Returns (tokens/s, cores, seconds, passes)."""
     from oracle import oracle as orc
+    ntok = min(ntok, cfg.T)
     run = oracle_sample(cfg, mode, ntok, seed)
+    passes = 0
     t0 = time.perf_counter()
-    run()
-    dt = time.perf_counter() - t0
-    return ntok / dt, orc.num_threads(), dt
+    while True:
+        run()
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return ntok * passes / dt, orc.num_threads(), dt, passes
 
 
 def run_reference(args, cfg, metric, unit):
@@ -410,7 +417,9 @@ def main():
                     choices=["decode_c16", "decode_b512", "wide", "tiny", "gemm_sweep"])
     ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16", "mxw4a4"])
     ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
-    ap.add_argument("--baseline-tokens", type=int, default=4, help="tokens of the in-run CPU baseline")
+    ap.add_argument("--baseline-tokens", type=int, default=16, help="tokens of the in-run CPU baseline sample")
+    ap.add_argument("--baseline-seconds", type=float, default=10.0,
+                    help="the in-run CPU baseline repeats its sample for at least this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--router", action="store_true",
@@ -682,10 +691,11 @@ def main():
     if not args.no_clocks:
         result["clocks"] = clocks.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, dt = cpu_baseline(cfg, args.mode, args.baseline_tokens)
+        v, cores, dt, passes = cpu_baseline(cfg, args.mode, args.baseline_tokens, args.baseline_seconds)
         result["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
-                                  "sample": "first %d tokens of the batch (%.1f s of oracle work)" % (
-                                      args.baseline_tokens, dt)}
+                                  "sample": "first %d tokens of the batch, oracle layer forward %d times "
+                                            "(%.1f s of oracle work)" % (min(args.baseline_tokens, cfg.T),
+                                                                         passes, dt)}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

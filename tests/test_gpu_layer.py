@@ -219,3 +219,42 @@ def test_layer_host_entry_matches_device_entry(orc, mode, shape):
     assert int(status.item()) == 0
     assert torch.equal(got, ref.cpu())
 
+
+
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+@pytest.mark.parametrize("shape", [(5, 256, 256, 4, 4), (33, 256, 256, 1024, 32)])
+def test_layer_degenerate_routing_against_oracle(orc, mode, shape):
+    """Routing extremes through the whole layer: every token to every expert
+    (k = E: the softmax covers all experts), and the largest expert count and
+    top-k the entry points accept (E = 1024, k = 32) over two routing chunks
+    (33 tokens), with most experts receiving one or two rows."""
+    dev = cuda_or_skip()
+    T, H, I, E, k = shape
+    cfg = wl.MoEConfig("degenerate", T=T, H=H, I=I, E=E, k=k, routing="uniform")
+    m = MODES[mode]
+    xt = wl.activations_bf16(T, H, seed=7)
+    logits = wl.router_logits(cfg, seed=7)
+    w13, w2 = _oracle_weights(orc, cfg, range(E), seed=7)
+    g13 = upload_weights(w13, E, 2 * I, H, dev)
+    g2 = upload_weights(w2, E, H, I, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = B.moe_layer_forward(m, xt.to(dev), logits.to(dev), k, g13, g2, S_h, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = orc.moe_layer(mode, xt.float().numpy(), logits.numpy(), k, w13, w2, cfg.S_h)
+    assert_close(got.cpu().numpy(), ref, "%s %s" % (mode, shape))
+
+
+def test_layer_zero_tokens():
+    """T = 0: nothing to do, no error, an empty output."""
+    dev = cuda_or_skip()
+    cfg = wl.CONFIGS["tiny"]
+    (g13, _), (g2, _) = gpu_weights(cfg, dev)
+    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    x = torch.empty(0, cfg.H, dtype=torch.bfloat16, device=dev)
+    lg = torch.empty(0, cfg.E, dtype=torch.float32, device=dev)
+    for m in (B.MOE_W4A4, B.MOE_W4A16):
+        out = B.moe_layer_forward(m, x, lg, cfg.k, g13, g2, S_h)
+        torch.cuda.synchronize()
+        assert tuple(out.shape) == (0, cfg.H)
