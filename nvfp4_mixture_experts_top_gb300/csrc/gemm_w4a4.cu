@@ -73,12 +73,17 @@ struct Geo {
   static constexpr uint32_t OFF_AS = OFF_WS + WS_BYTES;
   static constexpr uint32_t STAGE_BYTES = OFF_AS + 4 * AS_BYTES;
   static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  // split-K epilogue staging (G = 4 only): per epilogue warp a [32 tokens][32
+  // rows] fp32 box in which a K half of a full token group is staged for the
+  // TMA reduce-add; G = 1 adds its K halves with atomics
+  static constexpr int RED_FLOATS = G == 4 ? 4 * 32 * 32 : 4;
   // TMEM columns: two accumulators of 32*G fp32 columns, then per stage 16
   // columns of weight scales and 16 of token scales (4 per K step each)
   static constexpr uint32_t ACC_COLS = TOK_PER_PASS;
   static constexpr uint32_t SF_BASE = 2 * ACC_COLS;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(SF_BASE + STAGES * 32 <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES + RED_FLOATS * 4 + 17 * 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_STAGE = 32;
@@ -164,8 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ volatile int abort_flag;
   __shared__ ItemTable tab;
   __shared__ int4 s_units[kUnitTable];
-  // split-K epilogue staging: per epilogue warp a [32 tokens][32 rows] fp32 box
-  __shared__ __align__(128) float s_red[4][TG * 32];
+  __shared__ __align__(128) float s_red[GE::RED_FLOATS];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -454,32 +458,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS + g * TG, r);
           tmem_ld_wait();
           const int tb = r0 + g * TG;
-          if (p.splits == 2 && tb + TG <= m1) {
-            // a full group of a K half: stage it as [token][row] and let TMA add
-            // it into the output in L2 (two halves onto zero: 0 + a + b == 0 +
-            // b + a, so the sum does not depend on their order)
-            float* box = s_red[q];
-            if (lane == 0) bulk_wait_read_all();  // the previous box has been read
-            __syncwarp();
+          if (p.splits == 1) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) box[i * 32 + lane] = __fmul_rn(__uint_as_float(r[i]), alpha);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_2d(&tm_out, box, it.nt * BM + q * 32, tb);
-              bulk_commit_group();
-            }
-          } else {
+            for (int i = 0; i < 32; ++i)
+              if (tb + i < m1) p.out[(size_t)(tb + i) * p.N + n] = __fmul_rn(__uint_as_float(r[i]), alpha);
+            continue;
+          }
+          // a K half: the two halves add into a zeroed output (0 + a + b ==
+          // 0 + b + a, so the sum does not depend on their order)
+          if constexpr (G == 4) {
+            if (tb + TG <= m1) {
+              // a full group: stage it as [token][row] and let TMA add it into
+              // the output in L2
+              float* box = s_red + q * (TG * 32);
+              if (lane == 0) bulk_wait_read_all();  // the previous box has been read
+              __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (tb + i < m1) {
-                float* dst = p.out + (size_t)(tb + i) * p.N + n;
-                const float v = __fmul_rn(__uint_as_float(r[i]), alpha);
-                if (p.splits == 1) *dst = v;
-                else atomicAdd(dst, v);  // ragged group of a K half: same order argument
+              for (int i = 0; i < 32; ++i) box[i * 32 + lane] = __fmul_rn(__uint_as_float(r[i]), alpha);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_reduce_add_2d(&tm_out, box, it.nt * BM + q * 32, tb);
+                bulk_commit_group();
               }
+              continue;
             }
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (tb + i < m1) atomicAdd(p.out + (size_t)(tb + i) * p.N + n, __fmul_rn(__uint_as_float(r[i]), alpha));
         }
         tc_fence_before();
         __syncwarp();
@@ -492,7 +499,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_all();  // reduce-adds complete before the CTA (and its boxes) go away
+    if constexpr (G == 4) {
+      if (lane == 0) bulk_wait_all();  // reduce-adds complete before the CTA (and its boxes) go away
+    }
     __syncwarp();
   }
 
