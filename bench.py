@@ -20,6 +20,7 @@ replica and value = all ranks' tokens / max time.
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -123,12 +124,16 @@ class ClockSampler:
 
 
 def _kernel_hash(mode="w4a4"):
-    """Hash of the sources of the dominant kernel of a mode (staleness check
-    of the committed DRAM-traffic figure)."""
+    """Hash of the code of the dominant kernel of a mode (staleness check of
+    the committed DRAM-traffic figure): its sources with comments and
+    whitespace removed, so that only a change of code counts."""
     h = hashlib.sha256()
     for fn in ("gemm_%s.cu" % ("w4a4" if mode == "mxw4a4" else mode), "common.cuh", "workitems.cuh"):
-        with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -16,8 +16,9 @@
 //      warp 1    tcgen05.cp of block scales into TMEM + tcgen05.mma
 //      warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32 stores
 //      warp 6    token-scale preparation (shared-memory transpose, below)
-//  * a 5-stage shared-memory ring (36 KB per stage) and two TMEM accumulator
-//    buffers, so loads, MMAs and the epilogue of the previous unit overlap.
+//  * a shared-memory ring (8 x 24 KB for passes of 32 tokens, 5 x 36 KB for
+//    passes of 128; see Geo) and two TMEM accumulator buffers, so loads, MMAs
+//    and the epilogue of the previous unit overlap.
 //  * every mbarrier wait is bounded; a timeout sets NVFP4_E_DEVICE_TIMEOUT,
 //    drains in-flight copies and MMAs, frees TMEM and returns.
 //
