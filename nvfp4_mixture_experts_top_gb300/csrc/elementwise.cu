@@ -207,14 +207,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / q_per_row, c = (i % q_per_row) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const float wj = __ldg(w + t * k + j);
-      const int64_t r = __ldg(inv + t * k + j);
-      const float4 y = __ldg(reinterpret_cast<const float4*>(Y + r * H + c));
-      acc.x = __fadd_rn(acc.x, __fmul_rn(wj, y.x));
-      acc.y = __fadd_rn(acc.y, __fmul_rn(wj, y.y));
-      acc.z = __fadd_rn(acc.z, __fmul_rn(wj, y.z));
-      acc.w = __fadd_rn(acc.w, __fmul_rn(wj, y.w));
+    // the k rows in chunks of 8: the row indices, then the 8 row loads, are
+    // issued together (one or two dependent round trips instead of k); the
+    // sum still runs in j order
+    constexpr int kU = 8;
+    for (int j0 = 0; j0 < k; j0 += kU) {
+      int64_t r[kU];
+      float wj[kU];
+      float4 y[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        r[j] = (j0 + j < k) ? __ldg(inv + t * k + j0 + j) : 0;
+        wj[j] = (j0 + j < k) ? __ldg(w + t * k + j0 + j) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j)
+        if (j0 + j < k) y[j] = __ldg(reinterpret_cast<const float4*>(Y + r[j] * H + c));
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        if (j0 + j < k) {
+          acc.x = __fadd_rn(acc.x, __fmul_rn(wj[j], y[j].x));
+          acc.y = __fadd_rn(acc.y, __fmul_rn(wj[j], y[j].y));
+          acc.z = __fadd_rn(acc.z, __fmul_rn(wj[j], y[j].z));
+          acc.w = __fadd_rn(acc.w, __fmul_rn(wj[j], y[j].w));
+        }
+      }
     }
     if (out_dtype == NVFP4_DT_F32) {
       *reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c) = acc;

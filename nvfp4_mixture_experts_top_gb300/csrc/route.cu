@@ -114,12 +114,20 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   if (t < T && x != nullptr) {
     const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
     float m = 0.0f;
-    for (int64_t i = lane; i < H / 8; i += 32) {
-      const uint4 u = __ldg(row + i);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    // 8 independent 16-byte loads in flight per lane: one warp reads a whole
+    // row (12 KB at H = 6144), which one load at a time took ~24 round trips
+    constexpr int kU = 8;
+    for (int64_t i0 = lane; i0 < H / 8; i0 += 32 * kU) {
+      uint4 u[kU];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
+      for (int j = 0; j < kU; ++j) u[j] = (i0 + 32 * j < H / 8) ? __ldg(row + i0 + 32 * j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const uint32_t wv[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
