@@ -21,6 +21,10 @@
  *    kernel attributes).
  *  - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and returns without synchronising.
+ *  - Kernels are launched as programmatic dependents of the preceding kernel
+ *    on the stream: a kernel's prologue (barrier setup, TMEM allocation) may
+ *    overlap that kernel's end, but it reads and writes memory only after
+ *    that kernel has completed, so stream order holds as with plain launches.
  *  - Arguments are validated on the host before anything is launched, so a
  *    failing call launches nothing.  The return value is an nvfp4_status.
  *  - Kernels that consume routing data check it and report problems through

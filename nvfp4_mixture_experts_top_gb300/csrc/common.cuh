@@ -48,15 +48,6 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -102,25 +93,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
-
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x,
-                                            int32_t y, uint64_t cache_policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(cache_policy)
-      : "memory");
-}
-
-// Untiled bulk copy: both addresses 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
-                                          uint64_t cache_policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(cache_policy)
-      : "memory");
-}
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -172,13 +144,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread
-// has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
 
 // Shared-memory matrix descriptor (tcgen05 format).
 //   start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29,
@@ -225,47 +190,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T with block scales in TMEM, one elected thread.
-__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A * B^T, BF16 inputs; A read from TMEM, B from shared memory.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A * B^T, BF16 inputs, both from shared memory.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Copy 32 rows x 128 bits from shared memory into TMEM, replicated into all
-// four 32-lane quarters ("warpx4"); row i lands in lane i of every quarter,
-// its four 32-bit words in four consecutive columns.
-__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Warp-collective TMEM load: 32 lanes x 32 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -278,16 +202,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-}
-
-// Warp-collective TMEM store: 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
 }
 
 // Warp-collective TMEM store: 32 lanes x 32 consecutive 32-bit columns.
@@ -317,6 +231,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // several times more issue cycles than this form.
 // ---------------------------------------------------------------------------
 
+// D[tmem] (+)= A[smem] * B[smem]^T, FP4 inputs with block scales in TMEM.
 __device__ __forceinline__ void ew_mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
@@ -343,6 +258,7 @@ __device__ __forceinline__ void ew_mma_mxf4_2x(uint32_t d_tmem, uint64_t adesc, 
       : "memory");
 }
 
+// D[tmem] (+)= A * B^T, BF16 inputs, both from shared memory.
 __device__ __forceinline__ void ew_mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
   asm volatile(
@@ -367,6 +283,9 @@ __device__ __forceinline__ void ew_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// Copy 32 rows x 128 bits from shared memory into TMEM, replicated into all
+// four 32-lane quarters ("warpx4"); row i lands in lane i of every quarter,
+// its four 32-bit words in four consecutive columns.
 __device__ __forceinline__ void ew_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -375,6 +294,8 @@ __device__ __forceinline__ void ew_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
       : "memory");
 }
 
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
 __device__ __forceinline__ void ew_commit(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -421,6 +342,7 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // this thread's bulk groups have completed (their global writes are done)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Untiled bulk copy: both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void ew_bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
                                              uint64_t cache_policy) {
   asm volatile(
