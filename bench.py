@@ -1,17 +1,23 @@
 """Benchmark of the NVFP4 MoE layer (decode) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_c16|decode_b512|wide] [--mode w4a4|w4a16|mxw4a4]
+                    [--workload decode_c16|decode_b512|wide|tiny|gemm_sweep]
+                    [--mode w4a4|w4a16|mxw4a4] [--router] [--sweep-ms M,...]
 
 Prints ONE JSON line (rank 0).  A step is one full MoE layer forward over the
-workload's batch: quantise -> route/permute/gather -> gate_up grouped GEMM ->
-SwiGLU+requant -> down grouped GEMM -> combine, all through the C ABI.  The
-timed steps are replays of one CUDA graph holding K captured steps, with
-CUDA events around the gate_up grouped GEMM of every step (the dominant
-kernel) for the roofline figure.  Weights are random N(0, 0.02) quantised on
-the GPU; activations N(0, 1) bf16; routing logits per the workload recipe.
-Touched weights per step exceed the 129 MB L2 by an order of magnitude, so no
-L2 flush is needed between steps.
+workload's batch -- route/permute + activation quantisation -> gate_up
+grouped GEMM -> SwiGLU+requant -> down grouped GEMM -> combine -- as one
+moe_layer_forward call through the C ABI.  The timed region is one replay of
+a CUDA graph holding K such calls.  The dominant kernel's duration (the
+gate_up grouped GEMM, for the roofline figure) comes from a second graph of
+the same K steps through the staged entry points with CUDA events around
+every gate_up launch.  `e2e` replays moe_layer_forward_host (inputs read from
+and output written to pinned host memory) once per step with a host
+synchronisation.  Weights are random N(0, 0.02) quantised on the GPU;
+activations N(0, 1) bf16; routing logits per the workload recipe.  Touched
+weights per step exceed the 129 MB L2 by an order of magnitude, so no L2
+flush is needed between steps.  --router times the router-logits GEMM and
+--workload gemm_sweep the single-expert GEMM sweep instead.
 
 --impl reference times the CPU oracle (the slow C restatement) on a bounded
 sample of the same workload; it is the baseline arm, not a GPU code path.
