@@ -99,3 +99,34 @@ def test_host_layer_entry_rejects_device_or_pageable_buffers_without_gpu():
     assert L.moe_layer_host_workspace_bytes(0, 16, 4096, 2048, 256, 8) == (
         L.moe_layer_workspace_bytes(0, 16, 4096, 2048, 256, 8) + 16 * 4096 * 2 + 16 * 256 * 4)
     assert L.moe_layer_host_workspace_bytes(0, -1, 4096, 2048, 256, 8) == 0
+
+
+def test_layer_entries_validate_on_the_host_without_gpu():
+    """moe_layer_forward and moe_layer_forward_host reject bad arguments on the
+    host, before any device call: status codes, not launches."""
+    from nvfp4_mixture_experts_top_gb300 import binding
+    L = binding.load()
+    P = ctypes.c_void_p
+    ok = P(4096)  # an aligned non-null stand-in; never dereferenced on these paths
+    ws = L.moe_layer_host_workspace_bytes(0, 16, 4096, 2048, 256, 8)
+
+    def host(mode=0, x=ok, lg=ok, T=16, H=4096, I=2048, E=256, k=8, out=ok, work=ok, nbytes=ws):
+        return L.moe_layer_forward_host(mode, x, lg, T, H, I, E, k, ok, ok, ok, ok, ok, ok, ok, out, None, work,
+                                        nbytes, None)
+
+    assert host(mode=7) == 1                    # bad mode
+    assert host(H=100) == 2                     # H % 256 != 0
+    assert host(k=33) == 2                      # k > 32
+    assert host(E=2048) == 2                    # E > 1024
+    assert host(T=0, x=None, lg=None, out=None) == 0  # nothing to do
+    assert host(x=None) == 1                    # null input
+    assert host(out=None) == 1                  # null output
+    assert host(nbytes=ws - 1) == 4             # workspace too small
+    assert host(work=None) == 4
+    assert host(x=P(4096 + 8)) == 3             # misaligned x
+    assert host(lg=P(4096 + 2)) == 3            # logits need 4-byte alignment
+    # the device-memory layer entry: the same shape checks
+    assert L.moe_layer_forward(0, ok, ok, 16, 4000, 2048, 256, 8, ok, ok, ok, ok, ok, ok, ok, ok, None, ok,
+                               L.moe_layer_workspace_bytes(0, 16, 4000, 2048, 256, 8), None) == 2
+    assert L.moe_layer_forward(0, ok, ok, 16, 4096, 2048, 256, 8, ok, ok, ok, ok, ok, ok, ok, ok, None, ok,
+                               L.moe_layer_workspace_bytes(0, 16, 4096, 2048, 256, 8) - 1, None) == 4
