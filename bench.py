@@ -545,7 +545,7 @@ def main():
             chk(L.moe_swiglu_requant(P(G), R, I, 1, None, None, None, P(h_b), st))
             chk(L.moe_grouped_gemm_nvfp4(1, P(h_b), None, None, P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
                                          cfg.E, H, I, R, P(Y), P(status), st))
-        chk(L.moe_combine(P(Y), P(inv), P(tw), T, k, H, 1, P(out), st))
+        chk(L.moe_combine(P(Y), P(inv), P(tw), T, k, H, 1, P(out), P(status), st))
 
     # kernels of this library per step: W4A4 route, quantise-scatter, 2 GEMMs,
     # SwiGLU-requant, combine; W4A16 route, gather, 2 GEMMs, SwiGLU, combine

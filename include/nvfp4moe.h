@@ -259,6 +259,13 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
 
 /* ------------------------------------------------------------------------
  * moe_swiglu_requant -- SwiGLU on the gate_up output and requantisation.
+ * Defined by the layer this library implements -- gate_up, then SwiGLU,
+ * then requantisation to NVFP4, then down -- which is the routed-expert FFN
+ * of the models on the pages ("Native FP4 Is Slower Than Emulated FP4",
+ * section 1: an NVFP4 MoE with 512 routed experts; the pages print no
+ * activation formula, so SwiGLU is the layer definition's own step).  The
+ * requantisation is nvfp4_quantize's rule ("The Benchmark That Confirmed the
+ * Ceiling", section "The NVFP4 Pivot").
  * h[r, i] = silu(G[r, i]) * G[r, I + i], silu(x) = x / (1 + exp(-x)), fp32.
  *   W4A4 : h is quantised to NVFP4 with the static decode scale *S_h
  *          (same rule as nvfp4_quantize): h_codes [R, I/2], h_scales
@@ -275,14 +282,21 @@ int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h,
                        uint8_t* h_scales, void* h_bf16, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * moe_combine -- weighted combine of the expert outputs, done as a gather
+ * moe_combine -- weighted combine of the expert outputs: the scatter half
+ * of the expert-scatter-gather pattern ("The 2x Gap", section "Discovering
+ * the sgl_kernel Alternative"), in which the layer definition combines the
+ * expert outputs with a weighted scatter.  Done here as a gather
  * (deterministic, no atomics):
  *   out[t, n] = sum_{j < k} topk_w[t, j] * Y[inv[t*k + j], n]   (fp32, j order)
  *   Y fp32 [T*k, H]; out [T, H] of out_dtype (NVFP4_DT_F32 or NVFP4_DT_BF16).
+ *   inv: the caller's permutation (from moe_align_permute).  Each entry is
+ *   checked on the device: an entry outside [0, T*k) contributes nothing,
+ *   and sets NVFP4_E_BAD_ROUTING in dev_status (optional, may be NULL);
+ *   no out-of-range row is ever read.
  * Constraints: H % 4 == 0.
  * ------------------------------------------------------------------------ */
 int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, int k, int H, int out_dtype,
-                void* out, nvfp4_stream_t stream);
+                void* out, int32_t* dev_status, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_layer_forward -- the whole layer in one call: every step above,
@@ -352,8 +366,10 @@ int moe_layer_forward_host(int mode, const void* x_host, const float* logits_hos
  *     T > 32736 at E = 128) is refused with NVFP4_E_WORKSPACE before anything
  *     is launched.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     per device, with that device current), and so does the first call
+ *     after a device reset (cudaDeviceReset destroys the context, and the
+ *     next one may hold the array at another address); make those calls
+ *     before any stream capture.
  *   - The array is shared by every call on a device and stays allocated while
  *     the library is loaded.  Calls that overlap on the GPU (different streams
  *     with no ordering between them) race on it; order them on one stream.

@@ -77,7 +77,7 @@ def load(build_if_missing: bool = True):
     L.moe_swiglu_requant.restype = _I
     L.moe_swiglu_requant.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P]
     L.moe_combine.restype = _I
-    L.moe_combine.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P]
+    L.moe_combine.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]
     L.moe_layer_workspace_bytes.restype = _SZ
     L.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
     L.moe_layer_forward.restype = _I
@@ -335,13 +335,14 @@ def moe_swiglu_requant(G, mode, S_h=None):
     return hb[:R]
 
 
-def moe_combine(Y, inv, topk_w, out_dtype=torch.float32):
+def moe_combine(Y, inv, topk_w, out_dtype=torch.float32, dev_status=None):
     L = load()
     T, k = topk_w.shape
     H = Y.shape[1]
     out = _empty((T, H), out_dtype, Y.device)
     dt = NVFP4_DT_F32 if out_dtype == torch.float32 else NVFP4_DT_BF16
-    _check("moe_combine", L.moe_combine(_ptr(Y), _ptr(inv), _ptr(topk_w), T, k, H, dt, _ptr(out), _stream()))
+    _check("moe_combine", L.moe_combine(_ptr(Y), _ptr(inv), _ptr(topk_w), T, k, H, dt, _ptr(out), _ptr(dev_status),
+                                        _stream()))
     return out
 
 

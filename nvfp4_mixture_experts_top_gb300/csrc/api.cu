@@ -6,6 +6,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "../../include/nvfp4moe.h"
 #include "kernels.h"
 
@@ -23,10 +25,18 @@ int current_device() {
 }
 }  // namespace
 
+// The environment is read once per process (a libc scan of the environment
+// on every launch would sit on the enqueue path of latency-bound decode
+// steps); the injection then applies to the first qualifying launch only, so
+// that a test can check in the same process and context that the next launch
+// is correct again.
 int fault_injection_drop_stage() {
-  const char* v = getenv("NVFP4MOE_TEST_DROP_STAGE");
-  if (v == nullptr || *v == 0) return -1;
-  return atoi(v);
+  static std::atomic<int> pending{[] {
+    const char* v = getenv("NVFP4MOE_TEST_DROP_STAGE");
+    return (v == nullptr || *v == 0) ? -1 : atoi(v);
+  }()};
+  if (pending.load(std::memory_order_relaxed) < 0) return -1;
+  return pending.exchange(-1, std::memory_order_relaxed);
 }
 
 int num_sms() {
@@ -350,7 +360,7 @@ int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h,
 }
 
 int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, int k, int H, int out_dtype,
-                void* out, nvfp4_stream_t stream) {
+                void* out, int32_t* dev_status, nvfp4_stream_t stream) {
   if (T < 0 || k <= 0 || H < 0) return NVFP4_E_INVAL;
   if (out_dtype != NVFP4_DT_F32 && out_dtype != NVFP4_DT_BF16) return NVFP4_E_INVAL;
   if (H % 4 != 0) return NVFP4_E_SHAPE;
@@ -358,7 +368,8 @@ int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, 
   if (Y == nullptr || inv == nullptr || topk_w == nullptr || out == nullptr) return NVFP4_E_INVAL;
   if (!aligned16(Y) || !aligned16(out)) return NVFP4_E_ALIGN;
   CHECK_ARCH();
-  return cuda_status(launch_combine(Y, inv, topk_w, T, k, H, out_dtype, out, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_combine(Y, inv, topk_w, T, k, H, out_dtype, out, dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // Carve the layer workspace into its regions (each 256-byte aligned).
@@ -473,7 +484,7 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
                                E, H, I, R, w.Y, dev_status, stream);
     if (s != NVFP4_OK) return s;
   }
-  return moe_combine(w.Y, w.inv, w.w, T, k, H, NVFP4_DT_F32, out, stream);
+  return moe_combine(w.Y, w.inv, w.w, T, k, H, NVFP4_DT_F32, out, dev_status, stream);
 }
 
 // Device view of page-locked host memory; false for any other pointer.

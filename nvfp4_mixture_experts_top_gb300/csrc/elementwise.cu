@@ -197,9 +197,11 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
 // combine: out[t, n] = sum_j w[t, j] * Y[inv[t*k + j], n]  (gather, fp32)
 // ---------------------------------------------------------------------------
 
+// inv comes from the caller: a row outside [0, T*k) contributes nothing and
+// is reported as NVFP4_E_BAD_ROUTING (never read).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ Y, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int T, int k, int64_t H,
-                                                      int out_dtype, void* __restrict__ out) {
+                                                      int out_dtype, void* __restrict__ out, int32_t* dev_status) {
   pdl_wait();
   pdl_trigger();
   const int64_t q_per_row = H / 4;
@@ -211,21 +213,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     // issued together (one or two dependent round trips instead of k); the
     // sum still runs in j order
     constexpr int kU = 8;
+    const uint32_t R = (uint32_t)T * (uint32_t)k;
     for (int j0 = 0; j0 < k; j0 += kU) {
       int64_t r[kU];
       float wj[kU];
       float4 y[kU];
+      bool ok[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
-        r[j] = (j0 + j < k) ? __ldg(inv + t * k + j0 + j) : 0;
+        const int32_t rr = (j0 + j < k) ? __ldg(inv + t * k + j0 + j) : 0;
+        ok[j] = (j0 + j < k) && (uint32_t)rr < R;
+        if (j0 + j < k && !ok[j]) report_status(dev_status, NVFP4_E_BAD_ROUTING);
+        r[j] = ok[j] ? rr : 0;
         wj[j] = (j0 + j < k) ? __ldg(w + t * k + j0 + j) : 0.0f;
       }
 #pragma unroll
       for (int j = 0; j < kU; ++j)
-        if (j0 + j < k) y[j] = __ldg(reinterpret_cast<const float4*>(Y + r[j] * H + c));
+        if (ok[j]) y[j] = __ldg(reinterpret_cast<const float4*>(Y + r[j] * H + c));
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
-        if (j0 + j < k) {
+        if (ok[j]) {
           acc.x = __fadd_rn(acc.x, __fmul_rn(wj[j], y[j].x));
           acc.y = __fadd_rn(acc.y, __fmul_rn(wj[j], y[j].y));
           acc.z = __fadd_rn(acc.z, __fmul_rn(wj[j], y[j].z));
@@ -442,10 +449,11 @@ cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const 
 }
 
 cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H, int out_dtype,
-                           void* out, cudaStream_t st) {
+                           void* out, int32_t* dev_status, cudaStream_t st) {
   const int64_t total = (int64_t)T * (H / 4);
   if (total == 0) return cudaSuccess;
-  return launch_pdl(combine_kernel, grid_for(total, 256), 256, 0, st, Y, inv, w, T, k, (int64_t)H, out_dtype, out);
+  return launch_pdl(combine_kernel, grid_for(total, 256), 256, 0, st, Y, inv, w, T, k, (int64_t)H, out_dtype, out,
+                    dev_status);
 }
 
 cudaError_t launch_mx_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, uint8_t* codes,

@@ -35,12 +35,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // (once per kernel and device).
 cudaError_t ensure_dynamic_smem(const void* func, int bytes);
 
-// Fault injection for the failure-detection tests: the value of the
-// environment variable NVFP4MOE_TEST_DROP_STAGE (read at every launch), or -1
-// when it is unset.  A grouped GEMM (W4A4, MXFP4, W4A16) or router GEMM
-// launched with it set never arms that pipeline stage, so its bounded waits
-// run out: it reports NVFP4_E_DEVICE_TIMEOUT in dev_status, drains, frees
-// TMEM and returns.
+// Fault injection for the failure-detection tests: the environment variable
+// NVFP4MOE_TEST_DROP_STAGE=n, read once per process, makes the FIRST grouped
+// GEMM (W4A4, MXFP4, W4A16) or router GEMM launch of the process never arm
+// its pipeline stage n; that launch's bounded waits run out, it reports
+// NVFP4_E_DEVICE_TIMEOUT in dev_status, drains, frees TMEM and returns.  Every
+// later launch gets -1 (no injection).
 int fault_injection_drop_stage();
 
 cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,
@@ -49,7 +49,7 @@ cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* 
 cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
                                   uint8_t* h_scales, void* h_bf16, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H,
-                           int out_dtype, void* out, cudaStream_t st);
+                           int out_dtype, void* out, int32_t* dev_status, cudaStream_t st);
 // Copy bytes16 (a multiple of 16) from src16 to dst16 and bytes4 (a multiple
 // of 4) from src4 to dst4 with SM loads: the sources may be page-locked host
 // memory (device views of it), read over the host link.

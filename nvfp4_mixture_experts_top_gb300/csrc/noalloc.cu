@@ -17,7 +17,10 @@
 // per-chunk expert masks are rebuilt from the logits each time), so the
 // caller never has to clear anything between calls.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "../../include/nvfp4moe.h"
 #include "kernels.h"
@@ -29,21 +32,63 @@ namespace {
 // chunk and expert, one 32-bit token mask.
 __device__ __align__(256) static uint8_t g_route_scratch[NVFP4MOE_NOALLOC_SCRATCH_BYTES];
 
+// Device address of g_route_scratch, per device, for the CUDA context it was
+// looked up in.  In host code the array's name is only a host-side stand-in;
+// a kernel must be given the address the runtime reports.  A device reset
+// destroys the context and the module with it, and the next context may load
+// the array elsewhere, so the cached address is tagged with the context's
+// unique id and looked up again when the current context differs.  A mutex
+// guards the cache: two host threads may make their first call together.
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];
+struct ScratchSlot {
+  unsigned long long ctx_id;  // 0: nothing cached
+  void* ptr;
+};
+ScratchSlot g_slot[kMaxDevices];
+std::mutex g_slot_mu;
 
-// Device address of g_route_scratch on the current device, looked up once per
-// device.  In host code the array's name is only a host-side stand-in; a
-// kernel must be given the address the runtime reports for the device.
+// Unique id of the calling thread's current context (0 if there is none or
+// the driver entry points are unavailable).  Driver entry points are fetched
+// through the runtime, so the library does not link libcuda.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  }
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_E_CUDA;
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess || ptr == nullptr) return NVFP4_E_CUDA;
-    g_scratch_ptr[dev] = ptr;
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  ScratchSlot& slot = g_slot[dev];
+  const unsigned long long id = current_context_id();
+  if (id != 0 && slot.ctx_id == id) {
+    *out = slot.ptr;
+    return NVFP4_OK;
   }
-  *out = g_scratch_ptr[dev];
+  // first call in this context (this also makes the device's primary
+  // context current if the runtime had not yet done so)
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess || ptr == nullptr) return NVFP4_E_CUDA;
+  slot.ptr = ptr;
+  slot.ctx_id = current_context_id();  // 0 if unknown: then looked up on every call
+  *out = ptr;
   return NVFP4_OK;
 }
 

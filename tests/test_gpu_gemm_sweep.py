@@ -3,8 +3,9 @@ the shape of the pages' FP4 GEMM measurements ("The 2x Gap", sections "The
 Investigation So Far" and "The Pivot": M=512, N=2048, K=6144; M=16-64 per
 expert).  Activations N(0,1) and weights N(0,0.02) are quantised on the GPU
 and by the oracle (bit-exact), then the GEMM runs through the grouped entry
-point with one expert.  Rows are compared with the oracle in full up to M=64
-and on sampled rows (first, last, spread) at M=512 and 4096."""
+point with one expert.  Rows are compared with the oracle in full up to
+M=512, and at M=4096 on every row next to a 128-row tile boundary plus a
+seeded spread (625 rows)."""
 import numpy as np
 import pytest
 import torch
@@ -31,6 +32,19 @@ def weights(orc):
     return (wc.view(1, N, K // 2), packed, wS), (oc[None], os_[None], np.array([oS], np.float32))
 
 
+def _rows(M):
+    """Every row up to M = 512; at larger M the two rows on each side of
+    every 128-row boundary (tile edges of every geometry the kernels use)
+    plus a seeded spread of 512 (625 rows at M = 4096)."""
+    if M <= 512:
+        return np.arange(M)
+    edges = np.arange(0, M, 128)
+    near = np.concatenate([edges - 2, edges - 1, edges, edges + 1])
+    spread = np.random.default_rng(M).choice(M, 512, replace=False)
+    r = np.unique(np.concatenate([near, spread, [M - 1]]))
+    return r[(r >= 0) & (r < M)]
+
+
 @pytest.mark.parametrize("M", wl.GEMM_SWEEP["Ms"])
 def test_gemm_sweep(orc, weights, M):
     dev = cuda_or_skip()
@@ -42,8 +56,7 @@ def test_gemm_sweep(orc, weights, M):
     out = B.moe_grouped_gemm_nvfp4(B.MOE_W4A4, ac, as_, aS, *gw, offs, N, K, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    rows = np.arange(M) if M <= 64 else np.unique(np.r_[0, 1, 127, 128, 129, M // 2, M - 2, M - 1,
-                                                      np.linspace(0, M - 1, 8).astype(int)])
+    rows = _rows(M)
     oac, oas, oaS = orc.quantize(a.cpu().numpy())
     assert np.array_equal(ac.cpu().numpy(), oac) and np.array_equal(as_.cpu().numpy(), oas)
     assert float(aS.item()) == float(oaS)

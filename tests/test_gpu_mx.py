@@ -2,7 +2,8 @@
 oracle: the quantiser bit for bit, the grouped GEMM (kind::mxf4nvf4
 .scale_vec::2X) on ragged expert groups, SwiGLU + requantisation, the fused
 route + quantise front half, and the whole layer (tiny with every
-intermediate; decode shapes at full size on sampled tokens).
+intermediate; decode shapes at full size: every token of decode_c16 and wide, every
+fourth token of decode_b512).
 
 Where a requantised code of h differs, the oracle's own fp32 h must lie
 within 1e-4 (relative) of that code's rounding midpoint or its block's
@@ -13,7 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_close, cuda_or_skip, errors, to_dev, unpack_codes
+from gpu_helpers import assert_close, cuda_or_skip, to_dev, unpack_codes
+from layer_parity import check_layer
 from nvfp4_mixture_experts_top_gb300 import binding as B
 from nvfp4_mixture_experts_top_gb300 import workloads as wl
 
@@ -244,8 +246,9 @@ def test_mx_layer_tiny_all_intermediates(orc):
     assert_close(d["out"].cpu().numpy(), ref, "tiny mxw4a4")
 
 
-@pytest.mark.parametrize("name,tokens", [("decode_c16", [0, 9]), ("wide", [5]), ("decode_b512", [0, 511])])
-def test_mx_layer_full_size(orc, name, tokens):
+@pytest.mark.parametrize("name", ["decode_c16", "wide"])
+def test_mx_layer_full_size(orc, name):
+    """Every token of the batch against the oracle (see layer_parity)."""
     dev = cuda_or_skip()
     cfg = wl.CONFIGS[name]
     x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
@@ -255,30 +258,20 @@ def test_mx_layer_full_size(orc, name, tokens):
     fused = B.moe_layer_forward(B.MOE_MXW4A4, x, logits, cfg.k, g13, g2, None)
     torch.cuda.synchronize()
     assert torch.equal(fused, d["out"]), "moe_layer_forward differs from the staged calls"
-    x_np = x.float().cpu().numpy()
-    lg_np = logits.cpu().numpy()
-    ids, _ = orc.route(lg_np[tokens], cfg.k)
-    used = np.unique(ids)
-    w13, w2 = _oracle_weights(orc, cfg, used, device=dev)
-    for i, e in enumerate(used):
-        assert np.array_equal(g13[0][e].cpu().numpy(), w13[0][i]) and np.array_equal(l13[e].cpu().numpy(), w13[1][i])
-        assert np.array_equal(g2[0][e].cpu().numpy(), w2[0][i]) and np.array_equal(l2[e].cpu().numpy(), w2[1][i])
-    ref, mids = orc.moe_layer("mxw4a4", x_np[tokens], lg_np[tokens][:, used], cfg.k, w13, w2, 0.0,
-                              intermediates=True)
-    got = d["out"].cpu().numpy()[tokens]
-    inv_g = d["rt"]["inv"].cpu().numpy().reshape(cfg.T, cfg.k)
-    hc_g = unpack_codes(d["hc"].cpu().numpy())
-    hc_o = unpack_codes(mids["hq_codes"])
-    amb = mx_ambiguous(mids["h32"], rel=1e-4)
-    inv_o = mids["inv"].reshape(len(tokens), cfg.k)
-    flipped = np.zeros(len(tokens), bool)
-    for i, t in enumerate(tokens):
-        for j in range(cfg.k):
-            diff = hc_g[inv_g[t, j]] != hc_o[inv_o[i, j]]
-            assert not (diff & ~amb[inv_o[i, j]]).any(), "h code differs away from a rounding boundary"
-            flipped[i] |= diff.any()
-    rel, _ = errors(got, ref)
-    assert rel <= 1e-3, rel
-    for i in range(len(tokens)):
-        if not flipped[i]:
-            assert_close(got[i], ref[i], "%s mxw4a4 token %d" % (name, tokens[i]))
+    check_layer(orc, cfg, "mxw4a4", d, x, logits, ((g13[0], l13), (g2[0], l2)), device=dev)
+
+
+def test_mx_layer_decode_b512_full_size(orc):
+    """decode_b512 in MXFP4: 128 tokens spread over the batch (every fourth),
+    against the oracle (see layer_parity)."""
+    dev = cuda_or_skip()
+    cfg = wl.CONFIGS["decode_b512"]
+    x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
+    logits = wl.router_logits(cfg, device=dev)
+    (g13, l13), (g2, l2) = gpu_mx_weights(cfg, dev)
+    d = staged_mx(x, logits, cfg, g13, g2)
+    fused = B.moe_layer_forward(B.MOE_MXW4A4, x, logits, cfg.k, g13, g2, None)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, d["out"]), "moe_layer_forward differs from the staged calls"
+    check_layer(orc, cfg, "mxw4a4", d, x, logits, ((g13[0], l13), (g2[0], l2)), tokens=np.arange(0, cfg.T, 4),
+                device=dev)

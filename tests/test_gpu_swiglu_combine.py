@@ -57,8 +57,37 @@ def test_combine(orc, T, k, H):
     Y = rng.normal(0, 1, (T * k, H)).astype(np.float32)
     inv = rng.permutation(T * k).astype(np.int32)
     w = rng.dirichlet(np.ones(k), T).astype(np.float32)
-    out = B.moe_combine(to_dev(Y, dev), to_dev(inv, dev), to_dev(w, dev))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = B.moe_combine(to_dev(Y, dev), to_dev(inv, dev), to_dev(w, dev), dev_status=status)
     ref = orc.combine(Y, inv.reshape(T, k).ravel(), w.astype(np.float64))
     assert_close(out.cpu().numpy(), ref, "combine")
+    assert int(status.item()) == 0
     outb = B.moe_combine(to_dev(Y, dev), to_dev(inv, dev), to_dev(w, dev), out_dtype=torch.bfloat16)
     assert np.allclose(outb.float().cpu().numpy(), ref, rtol=2 ** -8, atol=1e-6)
+
+
+def test_combine_out_of_range_rows_report_status(orc):
+    """moe_combine takes the permutation from the caller: an entry outside
+    [0, T*k) (one past the end, negative, far out) is never read.  Its term is
+    skipped, NVFP4_E_BAD_ROUTING is reported in the status word, and the
+    in-range terms are still summed."""
+    dev = cuda_or_skip()
+    T, k, H = 4, 3, 256
+    rng = np.random.default_rng(11)
+    Y = rng.normal(0, 1, (T * k, H)).astype(np.float32)
+    inv = rng.permutation(T * k).astype(np.int32)
+    w = rng.dirichlet(np.ones(k), T).astype(np.float32)
+    bad = inv.copy()
+    bad_slots = (1, 5, 7)
+    bad[1], bad[5], bad[7] = T * k, -1, 1 << 30
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = B.moe_combine(to_dev(Y, dev), to_dev(bad, dev), to_dev(w, dev), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 8  # NVFP4_E_BAD_ROUTING
+    w_ref = w.astype(np.float64).ravel().copy()
+    inv_ref = bad.copy()
+    for i in bad_slots:  # a skipped term: weight 0 on an in-range row
+        w_ref[i] = 0.0
+        inv_ref[i] = 0
+    ref = orc.combine(Y, inv_ref, w_ref.reshape(T, k))
+    assert_close(out.cpu().numpy(), ref, "combine with skipped rows")

@@ -4,9 +4,12 @@ no workspace, or a latency-critical path that must not call cudaMalloc).
 
 It is checked through the C ABI against the ordinary moe_align_permute (which
 takes a caller workspace) on the same inputs: identical ids, offsets,
-permutation and gathered rows, routing weights within 1e-6.  Two calls in a
-row with different problem sizes exercise the shared fixed scratch, which is
-reused without clearing.  The file is named so that pytest collects it last.
+permutation and gathered rows, routing weights within 1e-6.  Several calls in
+a row, each over the previous call's leftovers in the shared fixed scratch
+(which is never cleared between calls): decode_b512 twice (16 routing chunks
+of 32 tokens), then wide (2 chunks, 512 experts: its masks land on top of the
+previous call's), then decode_c16 (one chunk).  decode_b512 is also compared
+with the oracle directly.  The file is named so that pytest collects it last.
 """
 import ctypes as C
 
@@ -59,9 +62,11 @@ def _case(name, dev):
     return cfg, logits, xc, xs
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def test_noalloc_matches_workspace_entry_point_twice(orc):
     dev = cuda_or_skip()
-    for name in ("decode_b512", "decode_c16"):  # larger problem first, then a smaller one over its leftovers
+    # multi-chunk problems first (they use the fixed scratch), each over the
+    # previous call's leftovers, then a single-chunk one
+    for name in ("decode_b512", "decode_b512", "wide", "decode_c16"):
         cfg, logits, xc, xs = _case(name, dev)
         ref = _outputs(cfg.T, cfg.E, cfg.k, cfg.H, dev)
         got = _outputs(cfg.T, cfg.E, cfg.k, cfg.H, dev)
@@ -71,6 +76,15 @@ def test_noalloc_matches_workspace_entry_point_twice():
         for key in ("ids", "offsets", "perm", "inv", "codes", "scales", "status"):
             assert torch.equal(got[key], ref[key]), (name, key)
         assert torch.allclose(got["w"], ref["w"], rtol=1e-6, atol=0), name
+        if name == "decode_b512":
+            # and directly against the oracle: routing and permutation bit for bit
+            ids, w = orc.route(logits.cpu().numpy(), cfg.k)
+            offsets, perm, inv = orc.permute(ids, cfg.E)
+            assert np.array_equal(got["ids"].cpu().numpy(), ids)
+            assert np.array_equal(got["offsets"].cpu().numpy(), offsets)
+            assert np.array_equal(got["perm"].cpu().numpy(), perm)
+            assert np.array_equal(got["inv"].cpu().numpy(), inv)
+            assert np.allclose(got["w"].cpu().numpy(), w, rtol=0, atol=1e-6)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
