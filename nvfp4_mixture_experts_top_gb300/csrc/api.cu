@@ -326,6 +326,11 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
   if (mode != MOE_W4A16 && !aligned16(a_scales)) return NVFP4_E_ALIGN;
   CHECK_ARCH();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // many tokens per expert (prefill, large-M GEMMs): CTA pairs on one MMA
+  if (mode != MOE_W4A16 && gemm_w4a4_pair_eligible(E, N, R))
+    return cuda_status(launch_gemm_w4a4_pair(mode == MOE_MXW4A4, static_cast<const uint8_t*>(a), a_scales, a_S,
+                                             w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out,
+                                             dev_status, st));
   if (mode == MOE_MXW4A4)
     return cuda_status(launch_gemm_mxw4a4(static_cast<const uint8_t*>(a), a_scales, w_codes, w_scales_packed,
                                           expert_offsets, E, N, K, R, out, dev_status, st));

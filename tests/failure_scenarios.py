@@ -69,6 +69,26 @@ def gemm(dev, mode):
     return first, int(status.item()), elapsed, out.cpu().numpy(), ref()
 
 
+def gemm_pair(dev, mode):
+    """The CTA-pair GEMM (many tokens per expert): both CTAs of a pair skip
+    the same stage, so both sides' bounded waits run out."""
+    E, N, K = 1, 256, 1024
+    offs = np.array([0, 512], np.int32)
+    w = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", 0, N, K, 6).numpy()]))
+    a = wl.random_fp32((512, K), seed=6, tag="failpair").to(torch.bfloat16).float().numpy()
+    ac, as_, aS = orc.quantize(a)
+    args = (to_dev(ac, dev), to_dev(as_, dev), to_dev(np.array([aS]), dev), *upload_weights(w, E, N, K, dev),
+            to_dev(offs, dev), N, K)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    elapsed = _timed(lambda: B.moe_grouped_gemm_nvfp4(B.MOE_W4A4, *args, dev_status=status))
+    first = int(status.item())
+    status.zero_()
+    out = B.moe_grouped_gemm_nvfp4(B.MOE_W4A4, *args, dev_status=status)
+    torch.cuda.synchronize()
+    return first, int(status.item()), elapsed, out.cpu().numpy(), orc.grouped_gemm_w4a4(ac, as_, aS, w[0], w[1],
+                                                                                          w[2], offs)
+
+
 def router(dev, mode):
     T, H, E = 16, 1024, 256
     x = wl.activations_bf16(T, H, seed=4)
@@ -111,7 +131,7 @@ def layer(dev, mode):
     return first, int(status.item()), elapsed, out.cpu().numpy(), ref
 
 
-SCENARIOS = {"gemm": gemm, "router": router, "layer": layer}
+SCENARIOS = {"gemm": gemm, "gemm_pair": gemm_pair, "router": router, "layer": layer}
 
 
 def main():

@@ -13,7 +13,7 @@ Checks
   inv: bit for bit (routing of the GPU logits equals the oracle's routing);
 * every requantised h code (W4A4 NVFP4 with the static S_h; MXFP4 with its
   per-block shared exponent): equal to the oracle's, except where the
-  oracle's own fp32 h lies within `window` (relative) of that decision's
+  oracle's own fp32 h lies within FLIP_WINDOW (relative) of that decision's
   rounding boundary -- G is accumulated in fp32 on the tensor cores and in
   fp64 by the oracle, so h can differ in its last bits;
 * the output as a whole: relative Frobenius error <= 1e-3;
@@ -38,9 +38,13 @@ import torch
 from gpu_helpers import MAX_ERR_RMS_TOL, REL_FROB_TOL, errors, unpack_codes
 from nvfp4_mixture_experts_top_gb300 import workloads as wl
 
-# Where a requantised h code may differ (relative distance of the oracle's
-# fp32 h to the rounding boundary).
-FLIP_WINDOW = 1e-4
+# Where a requantised h code may differ: the oracle's fp32 h lies within
+# this relative distance of the decision's rounding boundary.  Measured on
+# GB300 over every token of decode_c16, wide and decode_b512 (NVFP4 and
+# MXFP4): |h_gpu - h_oracle| / |h| from the GPU's fp32 G is at most 5.4e-7,
+# and the largest boundary distance any differing code needed was 2.7e-7, so
+# 1e-5 leaves an 18x margin.
+FLIP_WINDOW = 1e-5
 
 # E4M3 decode table from torch's own float8 type (independent of both sides)
 _E4M3 = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()

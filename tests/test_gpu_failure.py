@@ -45,6 +45,13 @@ def test_gemm_bounded_wait_times_out_and_context_survives(mode):
     _run("gemm", mode, 0)
 
 
+@pytest.mark.parametrize("drop", [0, 1])
+def test_pair_gemm_bounded_wait_times_out_and_context_survives(drop):
+    """The CTA-pair GEMM: both CTAs of every pair give up, meet at their final
+    cluster barrier, free their tensor memory and return."""
+    _run("gemm_pair", "w4a4", drop)
+
+
 def test_router_gemm_bounded_wait_times_out_and_context_survives():
     _run("router", "w4a4", 0)
 

@@ -6,16 +6,16 @@ intermediate; decode shapes at full size: every token of decode_c16 and wide, ev
 fourth token of decode_b512).
 
 Where a requantised code of h differs, the oracle's own fp32 h must lie
-within 1e-4 (relative) of that code's rounding midpoint or its block's
-amax within 1e-4 of a power of two (the shared-exponent boundary), for the
-reason given in test_gpu_layer: G is accumulated in fp32 on the GPU and in
-fp64 in the oracle."""
+within FLIP_WINDOW (relative, see layer_parity) of that code's rounding
+midpoint or its block's amax that close to a power of two (the
+shared-exponent boundary): G is accumulated in fp32 on the GPU and in fp64
+in the oracle."""
 import numpy as np
 import pytest
 import torch
 
 from gpu_helpers import assert_close, cuda_or_skip, to_dev, unpack_codes
-from layer_parity import check_layer
+from layer_parity import FLIP_WINDOW, check_layer
 from nvfp4_mixture_experts_top_gb300 import binding as B
 from nvfp4_mixture_experts_top_gb300 import workloads as wl
 
@@ -240,7 +240,7 @@ def test_mx_layer_tiny_all_intermediates(orc):
     assert np.array_equal(d["rt"]["ids"].cpu().numpy(), mids["ids"])
     assert np.array_equal(d["rt"]["offsets"].cpu().numpy(), mids["offsets"])
     assert np.array_equal(d["rt"]["inv"].cpu().numpy(), mids["inv"])
-    amb = mx_ambiguous(mids["h32"], rel=1e-4)
+    amb = mx_ambiguous(mids["h32"], rel=FLIP_WINDOW)
     flips = unpack_codes(d["hc"].cpu().numpy()) != unpack_codes(mids["hq_codes"])
     assert not (flips & ~amb).any()
     assert_close(d["out"].cpu().numpy(), ref, "tiny mxw4a4")
