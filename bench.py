@@ -19,6 +19,13 @@ weights per step exceed the 129 MB L2 by an order of magnitude, so no L2
 flush is needed between steps.  --router times the router-logits GEMM and
 --workload gemm_sweep the single-expert GEMM sweep instead.
 
+At N=1 the line also carries a `secondary` block: the same measurement
+(ms_per_step, tokens/s, gate_up fraction of the measured HBM bandwidth, layer
+fraction, clocks) for every other headline configuration -- decode_c16,
+decode_b512 and wide in W4A4, W4A16 and MXFP4 (decode_b512: W4A4 and MXFP4)
+-- and the single-expert GEMM sweep (FP4 TFLOPS at M=512 and the other M).
+--no-secondary skips it.
+
 --impl reference times the CPU oracle (the slow C restatement) on a bounded
 sample of the same workload; it is the baseline arm, not a GPU code path.
 Multi-GPU: the path does not shard (replicas only); every rank runs its own
@@ -262,11 +269,11 @@ def run_reference(args, cfg, metric, unit):
     print(json.dumps(line), flush=True)
 
 
-def run_gemm_sweep(args, wl):
-    """Single-expert NVFP4 GEMM, N=2048, K=6144, M in {1,16,64,512,4096}.
-    Each M is timed as a CUDA graph of back-to-back GEMMs rotating over enough
-    copies of A, W and out that their total exceeds twice the L2, so every
-    launch reads its operands from HBM.  value = FP4 TFLOPS at M=512."""
+def gemm_sweep_rows(args, wl, Ms):
+    """Single-expert NVFP4 GEMM, N=2048, K=6144, for each M in Ms: a CUDA
+    graph of back-to-back GEMMs rotating over enough copies of A, W and out
+    that their total exceeds twice the L2, so every launch reads its operands
+    from HBM.  Returns (rows, fp4 peak TFLOP/s, peak kind)."""
     import torch
 
     from nvfp4_mixture_experts_top_gb300 import binding as B
@@ -284,7 +291,6 @@ def run_gemm_sweep(args, wl):
     del w
     L = B.load()
     rows = []
-    Ms = [int(m) for m in args.sweep_ms.split(",")] if args.sweep_ms else list(wl.GEMM_SWEEP["Ms"])
     for M in Ms:
         a, _ = wl.gemm_operands_fp32(M, 1, K, device=dev)
         ac, as_, aS = B.nvfp4_quantize(a)
@@ -334,6 +340,14 @@ def run_gemm_sweep(args, wl):
                      "frac_of_roofline": roof_us / us, "bound": "hbm" if per_copy / (hbm * 1e9) > flops / (
                          fp4_peak * 1e12) else "tensor", "copies": copies})
         del Ws, As, outs, g
+    return rows, fp4_peak, peak_kind
+
+
+def run_gemm_sweep(args, wl):
+    """The GEMM sweep as the benchmark's line: value = FP4 TFLOPS at M=512."""
+    Ms = [int(m) for m in args.sweep_ms.split(",")] if args.sweep_ms else list(wl.GEMM_SWEEP["Ms"])
+    N, K = wl.GEMM_SWEEP["N"], wl.GEMM_SWEEP["K"]
+    rows, fp4_peak, peak_kind = gemm_sweep_rows(args, wl, Ms)
     m512 = ([r for r in rows if r["M"] == 512] or rows)[0]
     result = {"metric": "FP4 TFLOPS at M=%d (single-expert NVFP4 GEMM, N=2048, K=6144)" % m512["M"],
               "value": m512["tflops"],
@@ -418,56 +432,18 @@ def run_router(args, cfg, wl):
     print(json.dumps(result), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_c16",
-                    choices=["decode_c16", "decode_b512", "wide", "tiny", "gemm_sweep"])
-    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16", "mxw4a4"])
-    ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
-    ap.add_argument("--baseline-tokens", type=int, default=16, help="tokens of the in-run CPU baseline sample")
-    ap.add_argument("--baseline-seconds", type=float, default=10.0,
-                    help="the in-run CPU baseline repeats its sample for at least this long")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--router", action="store_true",
-                    help="time the router-logits GEMM for the workload's T, H, E instead of the layer")
-    ap.add_argument("--sweep-ms", default="",
-                    help="gemm_sweep: comma-separated subset of the M values (e.g. for a profiler capture)")
-    ap.add_argument("--experts", type=int, default=0,
-                    help="override the expert count (smaller device footprint for profiler captures)")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
-
-    from nvfp4_mixture_experts_top_gb300 import workloads as wl
-    if args.workload == "gemm_sweep":
-        return run_gemm_sweep(args, wl)
-    cfg = wl.CONFIGS[args.workload]
-    if args.experts:
-        cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)
-    if args.router:
-        return run_router(args, cfg, wl)
-    metric = ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if args.mode == "mxw4a4"
-              else "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name))
-    unit = "tokens/s"
-    if args.impl == "reference":
-        return run_reference(args, cfg, metric, unit)
-
+def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, no_clocks=False):
+    """Time the layer of one workload and mode (see the module docstring);
+    full=True adds the end-to-end host-buffer measurement.  Returns the
+    result dict of the JSON line (without cpu_baseline)."""
     import torch
     import torch.distributed as dist
 
     from nvfp4_mixture_experts_top_gb300 import binding as B
-    world, rank, local = _dist()
-    if world > 1:
-        dist.init_process_group("nccl")
+    from nvfp4_mixture_experts_top_gb300 import workloads as wl
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    B.load()
-    B.nvfp4_device_check()
-    mode = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4}[args.mode]
+    mode = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4}[mode_name]
     mx = mode == B.MOE_MXW4A4
     bpe = MX_WEIGHT_BYTES_PER_ELEM if mx else WEIGHT_BYTES_PER_ELEM
 
@@ -607,7 +583,7 @@ def main():
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
-    if not args.no_clocks:
+    if not no_clocks:
         clocks.start()
         t_end = time.time() + 1.0  # clock window under load before the timed region
         while time.time() < t_end:
@@ -640,7 +616,7 @@ def main():
     spread = sorted(v / K for v in spread)
     if world > 1:
         dist.barrier()
-    if not args.no_clocks:
+    if not no_clocks:
         clocks.stop()
     ms_total = ms_total_timed
     gemm_ms = [a.elapsed_time(b) for a, b in evs]
@@ -651,62 +627,166 @@ def main():
     ms_step = max_over_ranks(ms_total / K, world, dev)
     value = job_throughput(T, world, ms_step / 1e3)
 
-    # end to end through the public API with host buffers: MoELayerGraph
-    # replays the host->device copies of x and logits, moe_layer_forward and
-    # the device->host copy of the output as one graph; each step also waits
-    # for the result on the host
-    lg_graph = B.MoELayerGraph(mode, T, H, cfg.E, k, w13, w2, S_h, device=dev)
-    lg_graph.x_host.copy_(x.cpu())
-    lg_graph.logits_host.copy_(logits.cpu())
-    for _ in range(args.warmup):
-        lg_graph.run()
-    te0 = time.perf_counter()
-    for _ in range(K):
-        res = lg_graph.run()
-    e2e_s = max_over_ranks((time.perf_counter() - te0) / K, world, dev)
-    if not torch.equal(res, out.cpu()):
-        raise RuntimeError("e2e result differs from the device-timed step")
-    if int(lg_graph.dev_status.item()) != 0:
-        raise RuntimeError("device status %d in the e2e run" % int(lg_graph.dev_status.item()))
+    e2e = None
+    if full:
+        # end to end through the public API with host buffers: MoELayerGraph
+        # replays moe_layer_forward_host (inputs read from and output written
+        # to pinned host memory by the layer's own kernels) as one graph; each
+        # step also waits for the result on the host
+        lg_graph = B.MoELayerGraph(mode, T, H, cfg.E, k, w13, w2, S_h, device=dev)
+        lg_graph.x_host.copy_(x.cpu())
+        lg_graph.logits_host.copy_(logits.cpu())
+        for _ in range(args.warmup):
+            lg_graph.run()
+        te0 = time.perf_counter()
+        for _ in range(K):
+            res = lg_graph.run()
+        e2e_s = max_over_ranks((time.perf_counter() - te0) / K, world, dev)
+        if not torch.equal(res, out.cpu()):
+            raise RuntimeError("e2e result differs from the device-timed step")
+        if int(lg_graph.dev_status.item()) != 0:
+            raise RuntimeError("device status %d in the e2e run" % int(lg_graph.dev_status.item()))
+        e2e = {"value": job_throughput(T, world, e2e_s), "unit": "tokens/s",
+               "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4, "d2h_bytes_per_step": out.numel() * 4}
+        del lg_graph
 
     hbm, _, peak_kind = _load_peaks()
     gemm_avg_ms = statistics.mean(gemm_ms)
     achieved = gemm1_bytes / (gemm_avg_ms / 1e3) / 1e9
     result = {
-        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {B.MOE_W4A4: "fp4(e2m1)xfp4, fp32 accumulate", B.MOE_W4A16: "fp4(e2m1)xbf16, fp32 accumulate",
                   B.MOE_MXW4A4: "fp4(e2m1)xfp4 (UE8M0 scales), fp32 accumulate"}[mode],
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised on the GPU)",
-        "config": {"workload": cfg.name, "mode": args.mode, "T": T, "hidden": H, "intermediate": I,
+        "config": {"workload": cfg.name, "mode": mode_name, "T": T, "hidden": H, "intermediate": I,
                    "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "no flush: %.2f GB of touched weights per step >> 129 MB L2" % (layer_weight_bytes / 1e9),
                    "timing": "CUDA graph of %d moe_layer_forward calls, CUDA events; gate_up duration from a "
                              "second graph of the %d steps through the staged entry points with events around "
                              "each gate_up launch" % (K, K)},
-        "roofline": {"kernel": "moe_grouped_gemm_nvfp4 gate_up (%s)" % args.mode, "bound": "hbm",
+        "roofline": {"kernel": "moe_grouped_gemm_nvfp4 gate_up (%s)" % mode_name, "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gemm1_bytes,
-                     "avg_launch_ms": gemm_avg_ms, "traffic": _traffic(cfg.name, args.mode)},
+                     "avg_launch_ms": gemm_avg_ms, "traffic": _traffic(cfg.name, mode_name)},
         "layer_hbm": {"weight_bytes_per_step": layer_weight_bytes,
                       "achieved_gbs": layer_weight_bytes / (ms_step / 1e3) / 1e9,
                       "frac_of_peak": layer_weight_bytes / (ms_step / 1e3) / 1e9 / hbm},
-        "e2e": {"value": job_throughput(T, world, e2e_s), "unit": unit, "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
-                "d2h_bytes_per_step": out.numel() * 4},
+        "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "spread": {"replays": len(spread), "ms_per_step_min": spread[0],
                    "ms_per_step_median": statistics.median(spread), "ms_per_step_max": spread[-1],
                    "note": "the timed replay and five more of the same graph"},
     }
-    if not args.no_clocks:
+    if not no_clocks:
         result["clocks"] = clocks.summary()
+    return result
+
+
+def layer_metric(cfg, mode_name):
+    return ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if mode_name == "mxw4a4"
+            else "MoE-layer tokens/s (NVFP4 %s, %s)" % (mode_name.upper(), cfg.name))
+
+
+# The headline configurations other than the one the line is quoted on; the
+# default run measures each of them too (secondary block of the line).
+SECONDARY = (("decode_c16", "w4a16"), ("decode_c16", "mxw4a4"), ("decode_b512", "w4a4"), ("decode_b512", "mxw4a4"),
+             ("wide", "w4a4"), ("wide", "w4a16"), ("wide", "mxw4a4"))
+
+
+def secondary_entry(r):
+    """The compact form of a measure_layer() result for the secondary block."""
+    return {"metric": r["metric"], "value": r["value"], "unit": r["unit"], "ms_per_step": r["ms_per_step"],
+            "config": r["config"], "frac": r["roofline"]["frac"], "gate_up_ms": r["roofline"]["avg_launch_ms"],
+            "layer_frac": r["layer_hbm"]["frac_of_peak"], "clocks": r.get("clocks"),
+            "spread": r["spread"]}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_c16",
+                    choices=["decode_c16", "decode_b512", "wide", "tiny", "gemm_sweep"])
+    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16", "mxw4a4"])
+    ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
+    ap.add_argument("--baseline-tokens", type=int, default=16, help="tokens of the in-run CPU baseline sample")
+    ap.add_argument("--baseline-seconds", type=float, default=10.0,
+                    help="the in-run CPU baseline repeats its sample for at least this long")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="measure only the selected workload (no secondary block of the other headline configs)")
+    ap.add_argument("--router", action="store_true",
+                    help="time the router-logits GEMM for the workload's T, H, E instead of the layer")
+    ap.add_argument("--sweep-ms", default="",
+                    help="gemm_sweep: comma-separated subset of the M values (e.g. for a profiler capture)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (smaller device footprint for profiler captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from nvfp4_mixture_experts_top_gb300 import workloads as wl
+    if args.workload == "gemm_sweep":
+        return run_gemm_sweep(args, wl)
+    cfg = wl.CONFIGS[args.workload]
+    if args.experts:
+        cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)
+    if args.router:
+        return run_router(args, cfg, wl)
+    metric = ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if args.mode == "mxw4a4"
+              else "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name))
+    unit = "tokens/s"
+    if args.impl == "reference":
+        return run_reference(args, cfg, metric, unit)
+
+    import torch
+    import torch.distributed as dist
+
+    from nvfp4_mixture_experts_top_gb300 import binding as B
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.load()
+    B.nvfp4_device_check()
+    result = measure_layer(args, cfg, args.mode, metric, world, rank, local, full=True, no_clocks=args.no_clocks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, dt, passes = cpu_baseline(cfg, args.mode, args.baseline_tokens, args.baseline_seconds)
         result["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
                                   "sample": "first %d tokens of the batch, oracle layer forward %d times "
                                             "(%.1f s of oracle work)" % (min(args.baseline_tokens, cfg.T),
                                                                          passes, dt)}
+    if world == 1 and not args.no_secondary and not args.experts:
+        # every other headline configuration, each measured the same way
+        sec = []
+        for wname, mname in SECONDARY:
+            if (wname, mname) == (cfg.name, args.mode):
+                continue
+            c2 = wl.CONFIGS[wname]
+            r2 = measure_layer(args, c2, mname, layer_metric(c2, mname), world, rank, local, full=False,
+                               no_clocks=args.no_clocks)
+            sec.append(secondary_entry(r2))
+            torch.cuda.empty_cache()
+        if (cfg.name, args.mode) != ("decode_c16", "w4a4"):
+            r2 = measure_layer(args, wl.CONFIGS["decode_c16"], "w4a4", layer_metric(wl.CONFIGS["decode_c16"], "w4a4"),
+                               world, rank, local, full=False, no_clocks=args.no_clocks)
+            sec.insert(0, secondary_entry(r2))
+        # the single-expert GEMM sweep: FP4 TFLOPS at M=512 (and the other M)
+        rows, fp4_peak, peak_kind = gemm_sweep_rows(args, wl, list(wl.GEMM_SWEEP["Ms"]))
+        m512 = [r for r in rows if r["M"] == 512][0]
+        sec.append({"metric": "FP4 TFLOPS at M=512 (single-expert NVFP4 GEMM, N=2048, K=6144)",
+                    "value": m512["tflops"], "unit": "TFLOP/s", "ms_per_step": m512["us"] / 1e3,
+                    "config": {"workload": "gemm_sweep", "N": wl.GEMM_SWEEP["N"], "K": wl.GEMM_SWEEP["K"],
+                               "Ms": list(wl.GEMM_SWEEP["Ms"])},
+                    "frac": m512["tflops"] / fp4_peak,
+                    "peak": fp4_peak, "peak_kind": "measured bf16 x nominal fp4/bf16 ratio 6 (%s)" % peak_kind,
+                    "frac_of_roofline": m512["frac_of_roofline"], "sweep": rows})
+        result["secondary"] = sec
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

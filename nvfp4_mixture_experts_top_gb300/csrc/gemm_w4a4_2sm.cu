@@ -8,18 +8,22 @@
 // tokens per CTA; at large M its shared-memory ring is latency-bound (each
 // 36 KB stage carries 4 M MACs).  This kernel doubles both tile sides by
 // running CTA PAIRS (clusters of two) on one tcgen05 MMA with .cta_group::2:
-//  * a pair tile is 256 weight rows (MMA M = 256: 128 in each CTA) x BN
-//    tokens (MMA N = BN = 128 or 256, half of the token rows in each CTA's
-//    shared memory); each CTA loads only its own 128 weight rows and BN/2
-//    token rows per K stage, yet its tensor core computes 128 x BN -- twice
-//    the MACs per loaded byte of a one-CTA tile;
+//  * a pair tile is 256 weight rows (MMA M = 256: 128 in each CTA) x BN = 256
+//    tokens (MMA N = 256, half of the token rows in each CTA's shared
+//    memory); each CTA loads only its own 128 weight rows and 128 token rows
+//    per K stage, yet its tensor core computes 128 x 256 -- twice the MACs per
+//    loaded byte of a one-CTA tile (the geometry is written for BN = 128 too,
+//    which measured slower than the one-CTA kernel at M = 512 and is not
+//    dispatched);
 //  * swap-AB as in the decode kernel: weights are the MMA's M side, tokens
 //    its N side; one pair tile = (expert, 256-row weight tile, pass of BN
 //    tokens), numbered expert-major as in the decode kernel; persistent pairs
 //    (76 on 152 SMs) walk the tiles round-robin;
 //  * a K split in two halves when the tiles cannot occupy every pair: both
-//    add into a zeroed output (0 + a + b == 0 + b + a: order-independent),
-//    full 32-token groups by TMA reduce-add, ragged ones by atomics.
+//    add into a zeroed output (0 + a + b == 0 + b + a: order-independent);
+//  * epilogue: full 32-token groups are staged in shared memory and written
+//    by TMA (store, or reduce-add for a K half), asynchronously to the warp;
+//    an expert's ragged last group is written (or added) element-wise.
 // Warp roles in each CTA (all converged; single operations via elect.sync):
 //    warp 0    TMA producer: own weight rows, own token rows, both token
 //              halves' scales (each CTA's tensor memory needs the scales of
@@ -44,6 +48,11 @@
 #include "tmap.h"
 #include "workitems.cuh"
 
+// Timestamp hooks for pipeline studies; empty in the library build.
+#ifndef PAIR_TRACE
+#define PAIR_TRACE(point, index)
+#endif
+
 namespace nvfp4moe {
 namespace w4a4_2sm {
 
@@ -64,16 +73,16 @@ struct Geo {
   static constexpr uint32_t OFF_AS = OFF_WS + WS_BYTES;
   static constexpr uint32_t AS_BYTES = BN * 16;        // token scales of the whole pass
   static constexpr uint32_t STAGE_BYTES = ((OFF_AS + AS_BYTES + 1023) / 1024) * 1024;
-  static constexpr int STAGES = 4;
-  // TMEM: one accumulator of BN columns, then per stage 16 columns of weight
-  // scales (4 per K step) and 4*G of token scales: 256 columns at BN = 128,
-  // 448 (allocated as 512) at BN = 256
-  static constexpr int ACC_BUFS = 1;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  // TMEM: accumulators (two of BN columns at BN = 128, one at 256), then per
+  // stage 16 columns of weight scales (4 per K step) and 4*G of token scales:
+  // 448 columns at either geometry, allocated as 512
+  static constexpr int ACC_BUFS = BN == 256 ? 1 : 2;
   static constexpr uint32_t SF_BASE = ACC_BUFS * BN;
   static constexpr uint32_t SF_STAGE = 16 + 4 * G;
   static constexpr uint32_t TMEM_USED = SF_BASE + STAGES * SF_STAGE;
   static constexpr uint32_t TMEM_ALLOC = TMEM_USED <= 256 ? 256 : 512;
-  // split-K staging: per epilogue warp two [32 tokens][32 rows] fp32 boxes
+  // epilogue staging: per epilogue warp two [32 tokens][32 rows] fp32 boxes
   static constexpr uint32_t RED_BYTES = 4 * 2 * TG * 32 * 4;
   static constexpr uint32_t OFF_RED = STAGES * STAGE_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_RED + RED_BYTES + 1024;
@@ -81,6 +90,14 @@ struct Geo {
   static_assert(TMEM_USED <= TMEM_ALLOC && TMEM_ALLOC <= 512, "TMEM budget");
   static_assert(SMEM_BYTES + 17 * 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
 };
+
+// TMA store of an fp32 shared-memory box into global memory, tracked by the
+// issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
 
 struct Params {
   const uint8_t* w_scales;  // packed atoms (per 128-row tile)
@@ -181,7 +198,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // before either touches the other's
   pair::cluster_sync();
   tc_fence_after();
+  if (threadIdx.x == 0) PAIR_TRACE(7, 0);
   pdl_wait();
+  if (threadIdx.x == 0) PAIR_TRACE(7, 1);
   const ExpertRows xr{p.offsets, p.E, p.R};
   if (warp == 2) {
     build_item_table<BN>(xr, NT2, tab, lane);
@@ -195,6 +214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   pdl_trigger();
+  if (threadIdx.x == 0) PAIR_TRACE(7, 2);
   const uint32_t tmem = tmem_base_s;
   const int units = tab.base[p.E] * p.splits;
   auto unit_j = [&](int j, int u) -> Unit {
@@ -223,6 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         uint8_t* sb = smem + stage * STAGE_BYTES;
+        if (lane == 0) PAIR_TRACE(0, it_p);
         if (it_p == p.drop_stage) {
           // fault injection (tests only): never armed; the waits run out
           ++it_p;
@@ -258,6 +279,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    int it_s = 0;
     for (int u = pair_id; ok && u < units; u += npairs) {
       const int split = u % p.splits;
       const int kc0 = split * KCH / p.splits, kc1 = (split + 1) * KCH / p.splits;
@@ -266,6 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
+        if (lane == 0) PAIR_TRACE(1, it_s);
         uint8_t* as_tile = smem + stage * STAGE_BYTES + OFF_AS;
         // token 32g + lane's 16 bytes -> cells [K step kk][group g]
         uint4 v[G];
@@ -311,6 +334,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_proxy_async_smem();  // generic writes -> visible to tcgen05.cp (async proxy)
         __syncwarp();
         pair::ew_arrive_remote(pair::mapa(smem_u32(&sf_ready[stage]), 0));
+        if (lane == 0) PAIR_TRACE(2, it_s);
+        ++it_s;
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
@@ -324,6 +349,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      int it_c = 0;
       const uint32_t smem_base = smem_u32(smem);
       const uint32_t idesc = MX ? idesc_mxf4_ue8m0(2 * BM, BN) : idesc_mxf4nvf4(2 * BM, BN);
       for (int u = pair_id, j = 0; ok && u < units; u += npairs, ++j) {
@@ -341,6 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
+          if (lane == 0) PAIR_TRACE(3, it_c);
           const uint32_t sb = smem_base + stage * STAGE_BYTES;
           const uint32_t sfa = tmem + GE::SF_BASE + stage * GE::SF_STAGE;
           const uint32_t sfb = sfa + 16;
@@ -356,6 +383,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                               (kc != cur.kc0 || kk != 0));
           }
           pair::ew_commit2_both(&empty_bar[stage]);
+          if (lane == 0) PAIR_TRACE(4, it_c);
+          ++it_c;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -391,19 +420,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
+      if (lane == 0 && q == 0) PAIR_TRACE(5, j);
       for (int g = 0; g < it.ng; ++g) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + g * TG, r);
         tmem_ld_wait();
         const int tb = it.r0 + g * TG;
-        if (p.splits == 1) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (tb + i < it.m1) p.out[(size_t)(tb + i) * p.N + n] = __fmul_rn(__uint_as_float(r[i]), alpha);
-          continue;
-        }
         if (tb + TG <= it.m1) {
-          // a full group: stage it as [token][row], TMA adds it in L2
+          // a full group: stage it as [token][row] and let TMA store it (or,
+          // for a K half, add it in L2), asynchronously to this warp
           float* box = red + red_box * (TG * 32);
           if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // box's last use read
           __syncwarp();
@@ -412,10 +437,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d(&tm_out, box, nrow0, tb);
+            if (p.splits == 1) tma_store_2d(&tm_out, box, nrow0, tb);
+            else tma_reduce_add_2d(&tm_out, box, nrow0, tb);
             bulk_commit_group();
           }
           red_box ^= 1;
+          continue;
+        }
+        // the expert's last, ragged group: rows past its end belong to the
+        // next expert and must not be written
+        if (p.splits == 1) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (tb + i < it.m1) p.out[(size_t)(tb + i) * p.N + n] = __fmul_rn(__uint_as_float(r[i]), alpha);
           continue;
         }
 #pragma unroll
@@ -425,21 +459,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       pair::ew_arrive_remote(pair::mapa(smem_u32(&acc_empty[acc]), 0));
+      if (lane == 0 && q == 0) PAIR_TRACE(6, j);
       if (++acc == ACC_BUFS) {
         acc = 0;
         acc_phase ^= 1;
       }
     }
-    if (lane == 0) bulk_wait_all();  // reduce-adds complete before the staging boxes go away
+    if (lane == 0) bulk_wait_all();  // stores and reduce-adds complete before the boxes go away
     __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) PAIR_TRACE(7, 3);
   // the leader's MMAs (which write both CTAs' tensor memory and read both
   // CTAs' shared memory) and every remote arrival have completed
   pair::cluster_sync();
   tc_fence_after();
+  if (threadIdx.x == 0) PAIR_TRACE(7, 4);
   if (warp == 1) pair::tmem_dealloc2(tmem, GE::TMEM_ALLOC);
 }
 
@@ -469,7 +506,8 @@ static cudaError_t launch_pair_geo(const uint8_t* a_codes, const uint8_t* a_scal
   const uint64_t as_pitch = MX ? (uint64_t)mx_scale_pitch(K) : (uint64_t)K / 16;
   err = make_tmap_2d_u8(&tm_bs, a_scales, as_pitch, (uint64_t)R, as_pitch, 16, BN, 0);
   if (err != cudaSuccess) return err;
-  // output [R rows, N fp32]: destination of the split-K reduce-adds, box 32 x 32
+  // output [R rows, N fp32]: destination of the full-group stores and the
+  // split-K reduce-adds, box 32 x 32
   err = make_tmap_2d_f32(&tm_out, out, (uint64_t)N, (uint64_t)R, (uint64_t)N * 4, 32, TG);
   if (err != cudaSuccess) return err;
   Params p;
@@ -511,10 +549,13 @@ static cudaError_t launch_pair_geo(const uint8_t* a_codes, const uint8_t* a_scal
 }
 
 // The pair kernel for problems whose experts see many tokens: on average at
-// least 256 rows per expert (BN = 256 tokens per pass from 1024 rows per
-// expert on, else 128).  Needs N % 256 == 0 and an even SM count.
+// least 1024 rows per expert (passes of 256 tokens).  Measured on GB300 for
+// the single-expert GEMM N = 2048, K = 6144: at M = 4096 34.2 us against 44 us
+// for the one-CTA kernel; at M = 512 (a 128-token geometry of this kernel)
+// 13.6 us against 12.7 us, so below 1024 rows per expert the one-CTA kernel
+// runs.  Needs N % 256 == 0 and an even SM count.
 bool gemm_w4a4_pair_eligible(int E, int N, int R) {
-  return N % 256 == 0 && (long long)R >= 256LL * E && num_sms() >= 2;
+  return N % 256 == 0 && (long long)R >= 1024LL * E && num_sms() >= 2;
 }
 
 cudaError_t launch_gemm_w4a4_pair(bool mx, const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
@@ -523,16 +564,11 @@ cudaError_t launch_gemm_w4a4_pair(bool mx, const uint8_t* a_codes, const uint8_t
                                   cudaStream_t st) {
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  const bool wide = false;  // the 256-token geometry is not enabled yet
   if (mx)
-    return wide ? launch_pair_geo<true, 256>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K,
-                                             R, out, dev_status, st)
-                : launch_pair_geo<true, 128>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K,
-                                             R, out, dev_status, st);
-  return wide ? launch_pair_geo<false, 256>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K,
-                                            R, out, dev_status, st)
-              : launch_pair_geo<false, 128>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K,
-                                            R, out, dev_status, st);
+    return launch_pair_geo<true, 256>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R,
+                                      out, dev_status, st);
+  return launch_pair_geo<false, 256>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                                     dev_status, st);
 }
 
 }  // namespace nvfp4moe

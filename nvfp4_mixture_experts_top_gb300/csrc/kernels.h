@@ -84,7 +84,7 @@ cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, co
                              const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
                              cudaStream_t st);
 // The CTA-pair (.cta_group::2) grouped GEMM for many tokens per expert:
-// eligible when N % 256 == 0 and the experts see >= 256 rows on average.
+// eligible when N % 256 == 0 and the experts see >= 1024 rows on average.
 bool gemm_w4a4_pair_eligible(int E, int N, int R);
 cudaError_t launch_gemm_w4a4_pair(bool mx, const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
                                   const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,

@@ -46,35 +46,46 @@ __device__ __forceinline__ void cluster_sync() {
           : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+// Non-blocking test of a phase, with cluster-scope acquire semantics.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
-// warp_wait (common.cuh) for a barrier that also receives arrivals from the
-// other CTA of the pair: cluster-scope acquire, bounded, converged.
+// warp_wait (common.cuh) for a barrier that is completed from the other SM
+// of the pair (a remote arrival or a multicast tcgen05.commit): polled with a
+// non-blocking test and a short sleep rather than a suspending try_wait,
+// because such a completion did not wake a suspended waiter early (measured
+// on GB300, single-expert GEMM at M = 4096: 108 us with suspending waits,
+// 56 us with polling).  Bounded and converged like warp_wait; the timeout is
+// checked every 64 polls.
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                   int32_t* dev_status) {
-  bool ok = mbar_try_wait_cluster(bar, parity, 0);
+  bool ok = mbar_test_wait_cluster(bar, parity);
   if (!__all_sync(0xFFFFFFFFu, ok)) {
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
-      if (!ok) ok = mbar_try_wait_cluster(bar, parity, kSuspendHintNs);
+    for (uint32_t i = 1;; ++i) {
+      if (!ok) {
+        __nanosleep(32);
+        ok = mbar_test_wait_cluster(bar, parity);
+      }
       if (__all_sync(0xFFFFFFFFu, ok)) break;
-      const bool give_up = *abort_flag || (globaltimer_ns() - t0 > kWaitTimeoutNs);
-      if (__any_sync(0xFFFFFFFFu, give_up)) {
-        if ((threadIdx.x & 31) == 0 && !*abort_flag) {
-          *abort_flag = 1;
-          report_status(dev_status, NVFP4_E_DEVICE_TIMEOUT);
+      if ((i & 63) == 0) {
+        const bool give_up = *abort_flag || (globaltimer_ns() - t0 > kWaitTimeoutNs);
+        if (__any_sync(0xFFFFFFFFu, give_up)) {
+          if ((threadIdx.x & 31) == 0 && !*abort_flag) {
+            *abort_flag = 1;
+            report_status(dev_status, NVFP4_E_DEVICE_TIMEOUT);
+          }
+          return false;
         }
-        return false;
       }
     }
   }
@@ -82,11 +93,15 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
 }
 
 // One arrival (one elected lane) on a barrier given by its shared::cluster
-// address, with release semantics at cluster scope.
+// address (either CTA of the pair), with the default release semantics at CTA
+// scope: the arriving warp's own prior shared-memory writes and tensor-memory
+// reads are complete.  A release at cluster scope would also wait for the
+// thread's outstanding global accesses and measured about 1 us per arrival
+// on GB300 -- longer than a whole pipeline stage.
 __device__ __forceinline__ void ew_arrive_remote(uint32_t cluster_addr) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n\t}" ::"r"(cluster_addr)
+      "@e mbarrier.arrive.shared::cluster.b64 _, [%0];\n\t}" ::"r"(cluster_addr)
       : "memory");
 }
 

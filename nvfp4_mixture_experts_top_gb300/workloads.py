@@ -61,6 +61,13 @@ class MoEConfig:
         s2 = 0.02 * 0.02 * self.H
         return float(np.float32(16.0 * s2 / 2688.0))
 
+    @property
+    def S_h8(self) -> float:
+        """Static decode scale of h requantised to FP8 E4M3 (the W4A8 mode):
+        the same bound 16 * 0.02^2 * H mapped to E4M3's largest value 448."""
+        s2 = 0.02 * 0.02 * self.H
+        return float(np.float32(16.0 * s2 / 448.0))
+
 
 CONFIGS = {
     "tiny": MoEConfig("tiny", T=8, H=256, I=512, E=8, k=2, routing="uniform"),

@@ -25,7 +25,8 @@
  *    Blackwell SM120 GPUs", section "The Core Insight": W4A16 keeps the
  *    activations in BF16, W4A4 quantises them to FP4 as well.
  *  - "Native FP4 Is Slower Than Emulated FP4 ...", section 1: routed experts
- *    (512 experts, 22 active per token).
+ *    (512 experts, 22 active per token); NVFP4 as FP4 weights with FP8
+ *    activations (the W4A8 mode).
  *
  * Readings where the pages are silent (each one is listed with its reason in
  * the design notes of the repository):
@@ -47,6 +48,9 @@
  *    clamped to the UE8M0 range, elements E2M1(RNE, satfinite) of x / 2^E;
  *    an all-zero block takes the smallest scale.  No per-tensor scale.
  *    Scales stored linearly as [rows, cols/32].
+ *  - FP8 activations (W4A8): E4M3 "FN" codes with one fp32 per-tensor decode
+ *    scale, S = amax/448 (dynamic, for x) or a caller-given static S (for
+ *    h); code = E4M3(RNE, satfinite) of x / S, sign kept.
  *  - Router: top-k by logit, ties to the lower expert id, descending order;
  *    weights = softmax over the k selected logits (fp64 here).
  *  - Permutation: stable by (expert, token).
@@ -313,6 +317,47 @@ void orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows
 /* ------------------------------------------------------------------------ */
 /* Router and permutation                                                   */
 /* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) activations with a per-tensor scale (W4A8)                    */
+/* ------------------------------------------------------------------------ */
+
+/* "NVFP4 means FP4 weights with FP8 activations" ("Native FP4 Is Slower Than
+ * Emulated FP4", section 1).  Reading: an activation is one E4M3 "FN" code
+ * times one fp32 per-tensor decode scale S, the same two-level idea as the
+ * NVFP4 tensor scale with E4M3's largest value 448 in place of 6 * 448:
+ *   S = fp32(amax(|x|)) / 448          (one fp32 division; dynamic scale)
+ *   code = sign | E4M3(RNE, satfinite) of |x / S|  (x / S one fp32 division)
+ * The sign bit is copied from x / S even when the magnitude rounds to zero
+ * (-0.1 * 2^-9 * S encodes as 0x80).  S == 0 gives all codes 0.
+ * value = e4m3(code) * S. */
+int orc_fp8_encode(float q) {
+  int neg = signbit(q) ? 1 : 0;
+  return orc_e4m3_encode(fabsf(q)) | (neg << 7);
+}
+
+float orc_fp8_tensor_scale(const float* x, int64_t rows, int64_t cols, int64_t ld) {
+  float amax = 0.0f;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      float a = f32_abs(x[r * ld + c]);
+      if (a > amax) amax = a;
+    }
+  return amax / 448.0f;
+}
+
+/* x [rows, cols] (row stride ld) -> codes [rows, cols] (one byte each).
+ * dynamic != 0: S = amax / 448 is computed and written to *S; otherwise *S
+ * is read. */
+void orc_fp8_quantize(const float* x, int64_t rows, int64_t cols, int64_t ld, int dynamic, float* S,
+                      uint8_t* codes) {
+  if (dynamic) *S = orc_fp8_tensor_scale(x, rows, cols, ld);
+  float s = *S;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c)
+      codes[r * cols + c] = (s == 0.0f) ? 0 : (uint8_t)orc_fp8_encode(x[r * ld + c] / s);
+}
+
+/* ------------------------------------------------------------------------ */
 
 /* Router logits, the step before routing ("The 2x Gap: Diagnosing Suboptimal
  * FP4 GEMM Kernels on Blackwell SM120", section "The Investigation So Far":
@@ -460,6 +505,34 @@ void orc_grouped_gemm_mx(const uint8_t* a_codes, const uint8_t* a_scales, const 
   free(adq);
 }
 
+/* W4A8: out[r, n] = S_a * S_w[e(r)] * sum_k e4m3(a[r,k]) * dec(w[e(r), n, k]),
+ * fp64 accumulation.  a: FP8 codes [R, K]; w as for W4A4; out fp64 [R, N]. */
+void orc_grouped_gemm_w4a8(const uint8_t* a_codes, float S_a, const uint8_t* w_codes, const uint8_t* w_scales,
+                           const float* w_S, const int32_t* offsets, int E, int N, int K, double* out) {
+  int R = offsets[E];
+  double* adq = (double*)malloc(sizeof(double) * (size_t)R * (size_t)K);
+  for (int64_t i = 0; i < (int64_t)R * K; ++i) adq[i] = orc_e4m3_value(a_codes[i]);
+  for (int e = 0; e < E; ++e) {
+    int r0 = offsets[e], r1 = offsets[e + 1];
+    if (r1 <= r0) continue;
+    const uint8_t* wc = w_codes + (int64_t)e * N * (K / 2);
+    const uint8_t* ws = w_scales + (int64_t)e * N * (K / 16);
+    double alpha = (double)S_a * (double)w_S[e];
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+      double* wrow = (double*)malloc(sizeof(double) * (size_t)K);
+      for (int64_t c = 0; c < K; ++c) wrow[c] = dec_elem(wc, ws, K, n, c);
+      for (int r = r0; r < r1; ++r) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < K; ++c) acc += adq[(int64_t)r * K + c] * wrow[c];
+        out[(int64_t)r * N + n] = acc * alpha;
+      }
+      free(wrow);
+    }
+  }
+  free(adq);
+}
+
 /* ------------------------------------------------------------------------ */
 /* SwiGLU, requantisation, combine                                          */
 /* ------------------------------------------------------------------------ */
@@ -497,7 +570,10 @@ void orc_combine(const float* Y, const int32_t* inv, const double* w, int T, int
  * mode 0 = W4A4, 1 = W4A16, 2 = MXFP4 weights and activations (x quantised
  * and h requantised per 32-element block with UE8M0 scales; the per-tensor
  * scales w13_S, w2_S, S_h and S_x do not exist in this format and are not
- * read; hq_scales_o then holds R * I/32 bytes).
+ * read; hq_scales_o then holds R * I/32 bytes), 3 = W4A8 (NVFP4 weights; x
+ * quantised to FP8 E4M3 with the dynamic per-tensor scale, h requantised to
+ * FP8 with the static decode scale S_h; hq_codes_o then holds R * I bytes,
+ * hq_scales_o is not written).
  * x is [T, H] (bf16 values widened to fp32).
  * S_x_in: NULL = the dynamic per-tensor scale of these T rows; otherwise the
  * scale of a larger tensor these rows were taken from (to check a sample of
@@ -525,7 +601,15 @@ void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, 
   orc_route(logits, T, E, k, ids, w);
   orc_permute(ids, T, E, k, offsets, perm, inv);
 
-  if (mode == 2) {
+  if (mode == 3) {
+    uint8_t* xc = (uint8_t*)malloc((size_t)T * H);
+    uint8_t* ac = (uint8_t*)malloc((size_t)R * H);
+    if (S_x_in) S_x = *S_x_in;
+    orc_fp8_quantize(x, T, H, H, S_x_in ? 0 : 1, &S_x, xc);
+    for (int r = 0; r < R; ++r) memcpy(ac + (int64_t)r * H, xc + (int64_t)perm[r] * H, (size_t)H);
+    orc_grouped_gemm_w4a8(ac, S_x, w13_codes, w13_scales, w13_S, offsets, E, 2 * I, H, G64);
+    free(xc); free(ac);
+  } else if (mode == 2) {
     uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
     uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 32);
     uint8_t* ac = (uint8_t*)malloc((size_t)R * H / 2);
@@ -560,7 +644,14 @@ void orc_moe_layer(int mode, const float* x, const float* logits, int T, int H, 
   orc_swiglu(G32, R, I, h64);
   for (int64_t i = 0; i < (int64_t)R * I; ++i) h32[i] = (float)h64[i];
 
-  if (mode == 2) {
+  if (mode == 3) {
+    uint8_t* hc = (uint8_t*)malloc((size_t)R * I);
+    float sh = S_h;
+    orc_fp8_quantize(h32, R, I, I, 0, &sh, hc);
+    orc_grouped_gemm_w4a8(hc, sh, w2_codes, w2_scales, w2_S, offsets, E, H, I, Y64);
+    if (hq_codes_o) memcpy(hq_codes_o, hc, (size_t)R * I);
+    free(hc);
+  } else if (mode == 2) {
     uint8_t* hc = (uint8_t*)malloc((size_t)R * I / 2);
     uint8_t* hs = (uint8_t*)malloc((size_t)R * I / 32);
     orc_mx_quantize(h32, R, I, I, hc, hs);
@@ -609,7 +700,13 @@ void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, i
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
   orc_route(logits, T, E, k, ids, w);
   double* xd = (double*)malloc(sizeof(double) * (size_t)T * H);
-  if (mode == 2) {
+  if (mode == 3) {
+    uint8_t* xc = (uint8_t*)malloc((size_t)T * H);
+    float S_x = S_x_in ? *S_x_in : 0.0f;
+    orc_fp8_quantize(x, T, H, H, S_x_in ? 0 : 1, &S_x, xc);
+    for (int64_t i = 0; i < (int64_t)T * H; ++i) xd[i] = orc_e4m3_value(xc[i]) * (double)S_x;
+    free(xc);
+  } else if (mode == 2) {
     uint8_t* xc = (uint8_t*)malloc((size_t)T * H / 2);
     uint8_t* xs = (uint8_t*)malloc((size_t)T * H / 32);
     orc_mx_quantize(x, T, H, H, xc, xs);
@@ -659,6 +756,9 @@ void orc_moe_layer_naive(int mode, const float* x, const float* logits, int T, i
           orc_mx_quantize_block(h32 + b * 32, &hsc, ec);
           for (int q = 0; q < 32; ++q) hd[b * 32 + q] = orc_e2m1_value(ec[q]) * orc_ue8m0_value(hsc);
         }
+      } else if (mode == 3) {
+        for (int i = 0; i < I; ++i)
+          hd[i] = S_h == 0.0f ? 0.0 : orc_e4m3_value(orc_fp8_encode(h32[i] / S_h)) * (double)S_h;
       } else if (mode == 0) {
         uint8_t hsc;
         uint8_t ec[16];

@@ -75,6 +75,14 @@ def _declare(L):
     L.orc_mx_dequantize.argtypes = [_P, _P, _I64, _I64, _P]
     L.orc_router_logits.restype = None
     L.orc_router_logits.argtypes = [_P, _P, C.c_int, C.c_int, C.c_int, _P]
+    L.orc_fp8_encode.restype = C.c_int
+    L.orc_fp8_encode.argtypes = [C.c_float]
+    L.orc_fp8_tensor_scale.restype = C.c_float
+    L.orc_fp8_tensor_scale.argtypes = [_P, _I64, _I64, _I64]
+    L.orc_fp8_quantize.restype = None
+    L.orc_fp8_quantize.argtypes = [_P, _I64, _I64, _I64, C.c_int, _P, _P]
+    L.orc_grouped_gemm_w4a8.restype = None
+    L.orc_grouped_gemm_w4a8.argtypes = [_P, C.c_float, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, _P]
     L.orc_grouped_gemm_mx.restype = None
     L.orc_grouped_gemm_mx.argtypes = [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, _P]
 
@@ -161,6 +169,30 @@ def dequantize(codes, scales, S, cols):
     out = np.zeros((rows, cols), np.float64)
     lib().orc_dequantize(_p(codes), _p(scales), float(np.float32(S)), rows, cols, _p(out))
     return out
+
+
+def fp8_encode(q: float) -> int:
+    return lib().orc_fp8_encode(float(np.float32(q)))
+
+
+def fp8_tensor_scale(x) -> np.float32:
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    return np.float32(lib().orc_fp8_tensor_scale(_p(x), rows, cols, cols))
+
+
+def fp8_quantize(x, S=None):
+    """FP8 (E4M3) quantisation of x [rows, cols] with one per-tensor decode
+    scale.  S=None: dynamic (S = amax/448).  Returns (codes uint8 [rows,
+    cols], S)."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), np.uint8)
+    s = np.zeros(1, np.float32)
+    if S is not None:
+        s[0] = np.float32(S)
+    lib().orc_fp8_quantize(_p(x), rows, cols, cols, 0 if S is not None else 1, _p(s), _p(codes))
+    return codes, np.float32(s[0])
 
 
 def mx_quantize(x):
@@ -266,6 +298,21 @@ def grouped_gemm_w4a16(a, w_codes, w_scales, w_S, offsets):
     return out
 
 
+def grouped_gemm_w4a8(a_codes, S_a, w_codes, w_scales, w_S, offsets):
+    """FP8 activations [R, K] x NVFP4 weights, fp64 [R, N]."""
+    a_codes = _c(a_codes, np.uint8)
+    w_codes = _c(w_codes, np.uint8)
+    w_scales = _c(w_scales, np.uint8)
+    w_S = _c(w_S, np.float32)
+    offsets = _c(offsets, np.int32)
+    E, N = w_codes.shape[0], w_codes.shape[1]
+    K = a_codes.shape[1]
+    out = np.zeros((int(offsets[-1]), N), np.float64)
+    lib().orc_grouped_gemm_w4a8(_p(a_codes), float(np.float32(S_a)), _p(w_codes), _p(w_scales), _p(w_S),
+                                _p(offsets), E, N, K, _p(out))
+    return out
+
+
 def grouped_gemm_mx(a_codes, a_scales, w_codes, w_scales, offsets):
     a_codes = _c(a_codes, np.uint8)
     a_scales = _c(a_scales, np.uint8)
@@ -299,7 +346,7 @@ def combine(Y, inv, w):
     return out
 
 
-_MODES = {"w4a4": 0, "w4a16": 1, "mxw4a4": 2}
+_MODES = {"w4a4": 0, "w4a16": 1, "mxw4a4": 2, "w4a8": 3}
 
 
 def _weights(w13, w2):
@@ -317,8 +364,10 @@ def _sx(S_x):
 
 
 def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False, S_x=None):
-    """Full layer.  mode: 'w4a4' | 'w4a16' | 'mxw4a4'.  w13 / w2: (codes, scales,
-    S[E]); for 'mxw4a4' the scales are UE8M0 per 32 and S is None.
+    """Full layer.  mode: 'w4a4' | 'w4a16' | 'mxw4a4' | 'w4a8'.  w13 / w2:
+    (codes, scales, S[E]); for 'mxw4a4' the scales are UE8M0 per 32 and S is
+    None.  'w4a8': S_h is the static FP8 decode scale of h, and hq_codes are
+    FP8 codes [R, I].
     S_x: None = dynamic activation scale of x; else the given scale (for a
     sample of rows of a larger batch).  Returns out fp64 [T, H] (and a dict
     of intermediates if asked)."""
@@ -337,7 +386,7 @@ def moe_layer(mode, x, logits, k, w13, w2, S_h, intermediates=False, S_x=None):
     perm = np.zeros(R, np.int32)
     inv = np.zeros(R, np.int32)
     S_x_out = np.zeros(1, np.float32)
-    hq_c = np.zeros((R, I // 2), np.uint8)
+    hq_c = np.zeros((R, I if m == 3 else I // 2), np.uint8)
     hq_s = np.zeros((R, I // (32 if m == 2 else 16)), np.uint8)
     h32 = np.zeros((R, I), np.float32)
     sx = _sx(S_x)

@@ -73,9 +73,9 @@ def gemm_pair(dev, mode):
     """The CTA-pair GEMM (many tokens per expert): both CTAs of a pair skip
     the same stage, so both sides' bounded waits run out."""
     E, N, K = 1, 256, 1024
-    offs = np.array([0, 512], np.int32)
+    offs = np.array([0, 1024], np.int32)
     w = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w13", 0, N, K, 6).numpy()]))
-    a = wl.random_fp32((512, K), seed=6, tag="failpair").to(torch.bfloat16).float().numpy()
+    a = wl.random_fp32((1024, K), seed=6, tag="failpair").to(torch.bfloat16).float().numpy()
     ac, as_, aS = orc.quantize(a)
     args = (to_dev(ac, dev), to_dev(as_, dev), to_dev(np.array([aS]), dev), *upload_weights(w, E, N, K, dev),
             to_dev(offs, dev), N, K)

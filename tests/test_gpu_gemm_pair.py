@@ -1,5 +1,5 @@
 """GPU parity of the CTA-pair grouped GEMM (the .cta_group::2 kernel that
-moe_grouped_gemm_nvfp4 runs when the experts see at least 256 rows on
+moe_grouped_gemm_nvfp4 runs when the experts see at least 1024 rows on
 average and N % 256 == 0) against the oracle's fp64 grouped GEMM, NVFP4 and
 MXFP4: one K stage, ragged last passes, an empty expert, the two-way K split
 and the unsplit many-tiles-per-pair schedule; and routing errors reported
@@ -16,11 +16,11 @@ from test_gpu_mx import pad_scales, upload_mx_weights
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (counts per expert, N, K): all with >= 256 rows per expert on average
-    ([256], 256, 256),               # one pass, one K stage (no split)
-    ([300], 512, 1024),              # ragged last pass (300 = 2 x 128 + 44), K split in two
-    ([300, 0, 500], 256, 768),       # an empty expert; halves of 1 and 2 K stages
-    ([1000, 1100], 4096, 512),       # 304 tiles: several per pair, no split
+    # (counts per expert, N, K): all with >= 1024 rows per expert on average
+    ([1024], 256, 256),              # four full passes, one K stage (no split)
+    ([1100], 512, 1024),             # ragged last pass (1100 = 4 x 256 + 76), K split in two
+    ([1100, 0, 2000], 512, 768),     # an empty expert; K halves of 1 and 2 stages
+    ([2100, 2200], 4096, 512),       # 304 pair tiles, several per pair, no split
 ]
 
 
@@ -74,7 +74,7 @@ def test_pair_gemm_mxfp4(orc, case):
 def test_pair_gemm_bad_offsets_report_status():
     """Inconsistent offsets are reported through dev_status, not trapped."""
     dev = cuda_or_skip()
-    E, N, K, R = 2, 256, 256, 600
+    E, N, K, R = 2, 256, 256, 2100
     wc = torch.zeros(E, N, K // 2, dtype=torch.uint8, device=dev)
     ws = torch.zeros(E * N * K // 16, dtype=torch.uint8, device=dev)
     wS = torch.ones(E, device=dev)
@@ -82,7 +82,7 @@ def test_pair_gemm_bad_offsets_report_status():
     asc = torch.zeros(R, K // 16, dtype=torch.uint8, device=dev)
     aS = torch.ones(1, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    offs = torch.tensor([0, 400, 300], dtype=torch.int32, device=dev)  # last != R, and decreasing
+    offs = torch.tensor([0, 1400, 1300], dtype=torch.int32, device=dev)  # last != R, and decreasing
     B.moe_grouped_gemm_nvfp4(B.MOE_W4A4, a, asc, aS, wc, ws, wS, offs, N, K, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 8  # NVFP4_E_BAD_ROUTING
