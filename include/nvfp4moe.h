@@ -10,9 +10,11 @@
  *   requantise to NVFP4 -> grouped GEMM down -> weighted combine,
  * with tiny and ragged per-expert M ("The 2x Gap: Diagnosing Suboptimal FP4
  * GEMM Kernels on Blackwell SM120", section "The Investigation So Far":
- * 256 experts, 8 active, ~16 tokens per expert).  Two modes: W4A4 (FP4
+ * 256 experts, 8 active, ~16 tokens per expert).  Modes: W4A4 (FP4
  * activations too) and W4A16 (BF16 activations, FP4 weights dequantised in
- * the kernel) ("The 24% Ceiling", section "The Core Insight").
+ * the kernel) ("The 24% Ceiling", section "The Core Insight"); W4A8 (FP8
+ * activations, "Native FP4 Is Slower Than Emulated FP4", section 1); and
+ * MXFP4 weights and activations.
  *
  * Conventions shared by every entry point
  *  - Pointers are DEVICE pointers unless a comment says otherwise.  The
@@ -65,7 +67,7 @@ typedef enum nvfp4_status {
 
 enum { NVFP4_DT_BF16 = 0, NVFP4_DT_F32 = 1 };
 enum { NVFP4_SCALE_STATIC = 0, NVFP4_SCALE_DYNAMIC = 1 };
-enum { MOE_W4A4 = 0, MOE_W4A16 = 1, MOE_MXW4A4 = 2 };
+enum { MOE_W4A4 = 0, MOE_W4A16 = 1, MOE_MXW4A4 = 2, MOE_W4A8 = 3 };
 enum { MOE_ACT_NONE = 0, MOE_ACT_NVFP4 = 1, MOE_ACT_BF16 = 2 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -152,6 +154,28 @@ int mxfp4_pack_weight_scales(const uint8_t* scales_linear, int E, int N, int K, 
                              nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * fp8_quantize -- FP8 activations for the W4A8 mode.  "Native FP4 Is Slower
+ * Than Emulated FP4", section 1: NVFP4 as "FP4 weights with FP8
+ * activations".  The page gives the element type only; the scale is read as
+ * one fp32 per-tensor decode scale, as for NVFP4's tensor level:
+ *   S = amax(|x|) / 448                   (dynamic; or a caller-given S)
+ *   code = sign(x / S) | E4M3(|x / S|)    (x / S one fp32 IEEE division;
+ *                                          RNE, saturating at 448; the sign
+ *                                          bit is kept when the magnitude
+ *                                          rounds to zero)
+ *   value = e4m3(code) * S; S == 0 gives all codes 0.
+ *   x          [rows, cols] of x_dtype (NVFP4_DT_BF16 or NVFP4_DT_F32), row
+ *              stride ld_x elements
+ *   S          device fp32 scalar; NVFP4_SCALE_STATIC: read,
+ *              NVFP4_SCALE_DYNAMIC: written
+ *   codes      out [rows, cols], one E4M3 byte per element
+ *   workspace  >= nvfp4_quantize_workspace_bytes() bytes (dynamic mode only)
+ * Constraints: cols % 16 == 0; ld_x % 8 == 0 (bf16) or % 4 == 0 (f32).
+ * ------------------------------------------------------------------------ */
+int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x, float* S, int scale_mode,
+                 uint8_t* codes, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_router_logits -- the router scores that the routing step ranks ("The
  * 2x Gap", section "The Investigation So Far": each token goes to 8 of 256
  * experts by these scores):
@@ -226,6 +250,16 @@ int moe_route_quantize_mxfp4(const void* x, const float* logits, int T, int H, i
                              uint8_t* a_scales, int32_t* dev_status, void* workspace, size_t workspace_bytes,
                              nvfp4_stream_t stream);
 
+/* moe_route_quantize_fp8 -- the same front half for MOE_W4A8: routing and
+ * permutation as moe_align_permute, and x quantised to FP8 with the dynamic
+ * per-tensor scale exactly as fp8_quantize, written straight into permuted
+ * order: a_codes [T*k, H] (one byte per element), S_x (device fp32 scalar,
+ * amax(|x|) / 448).  Constraints: as moe_route_quantize_nvfp4. */
+int moe_route_quantize_fp8(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                           float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, float* S_x,
+                           uint8_t* a_codes, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                           nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * moe_grouped_gemm_nvfp4 -- ragged grouped GEMM over experts.
  * "The 2x Gap", sections "The Investigation So Far" and "Discovering the
@@ -236,12 +270,16 @@ int moe_route_quantize_mxfp4(const void* x, const float* logits, int T, int H, i
  *   W4A4 : out[r, n] = a_S * w_S[e] * sum_k dec(a[r,k]) * dec(w[e,n,k])
  *   W4A16: out[r, n] =        w_S[e] * sum_k a[r,k]      * dec(w[e,n,k])
  *   MXW4A4: out[r, n] =              sum_k dec(a[r,k]) * dec(w[e,n,k])
+ *   W4A8 : out[r, n] = a_S * w_S[e] * sum_k e4m3(a[r,k]) * dec(w[e,n,k])
  * with dec(.) = e2m1(code) * e4m3(block scale) (MXFP4: * 2^(scale-127) per
  * 32 elements), fp32 accumulation.
  *   W4A4 : a = codes [R, K/2], a_scales = [R, K/16], a_S = device fp32 scalar
  *   W4A16: a = bf16 [R, K], a_scales = NULL, a_S = NULL
  *   MXW4A4: a = codes [R, K/2], a_scales [R, mxfp4_scale_pitch(K)], a_S and
  *          w_S unused (may be NULL)
+ *   W4A8 : a = FP8 E4M3 codes [R, K] (fp8_quantize), a_scales = NULL, a_S =
+ *          device fp32 scalar; runs on F16 operands (e2m1 * e4m3 weights and
+ *          E4M3 activations are both exact in f16), fp32 accumulation
  *   w_codes        [E, N, K/2]
  *   w_scales_packed  from nvfp4_pack_weight_scales (mxfp4_pack_weight_scales)
  *   w_S            fp32 [E]
@@ -275,6 +313,8 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
  *   MXW4A4: h is quantised to MXFP4 (as mxfp4_quantize): h_codes [R, I/2],
  *          h_scales [R, mxfp4_scale_pitch(I)]; S_h and h_bf16 unused.  The
  *          block scales come from h itself, so no calibration is needed.
+ *   W4A8 : h is quantised to FP8 with the static decode scale *S_h (as
+ *          fp8_quantize): h_codes [R, I]; h_scales and h_bf16 unused.
  *   G fp32 [R, 2I] (gate columns 0..I-1, up columns I..2I-1).
  * Constraints: I % 16 == 0.
  * ------------------------------------------------------------------------ */
@@ -302,12 +342,13 @@ int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, 
  * moe_layer_forward -- the whole layer in one call: every step above,
  * enqueued in order on `stream` with no host synchronisation, so the call
  * can be captured in a CUDA graph.
- *   mode        MOE_W4A4, MOE_W4A16 or MOE_MXW4A4
+ *   mode        MOE_W4A4, MOE_W4A16, MOE_MXW4A4 or MOE_W4A8
  *   x           bf16 [T, H]; logits fp32 [T, E]
  *   w13_*       gate_up weights: codes [E, 2I, H/2], packed scales, S [E]
  *   w2_*        down weights:    codes [E, H, I/2],  packed scales, S [E]
  *               (MXW4A4: MXFP4 packed scales; w13_S, w2_S unused, may be NULL)
- *   S_h         device fp32 scalar, static decode scale of h (W4A4 only)
+ *   S_h         device fp32 scalar, static decode scale of h (W4A4: NVFP4's
+ *               per-tensor scale; W4A8: the FP8 scale; unused otherwise)
  *   out         fp32 [T, H]
  *   workspace   >= moe_layer_workspace_bytes(mode, T, H, I, E, k); holds
  *               every intermediate (routing, activations, G, h, Y)

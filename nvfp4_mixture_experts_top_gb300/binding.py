@@ -17,7 +17,7 @@ from . import build as _build
 NVFP4_OK = 0
 NVFP4_DT_BF16, NVFP4_DT_F32 = 0, 1
 NVFP4_SCALE_STATIC, NVFP4_SCALE_DYNAMIC = 0, 1
-MOE_W4A4, MOE_W4A16, MOE_MXW4A4 = 0, 1, 2
+MOE_W4A4, MOE_W4A16, MOE_MXW4A4, MOE_W4A8 = 0, 1, 2, 3
 MOE_ACT_NONE, MOE_ACT_NVFP4, MOE_ACT_BF16 = 0, 1, 2
 STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4_E_ALIGN", 4: "NVFP4_E_WORKSPACE",
                 5: "NVFP4_E_ARCH", 6: "NVFP4_E_CUDA", 7: "NVFP4_E_DEVICE_TIMEOUT", 8: "NVFP4_E_BAD_ROUTING"}
@@ -29,7 +29,7 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspac
            "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4", "mxfp4_scale_pitch",
            "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4",
            "moe_router_logits_workspace_bytes", "moe_router_logits", "moe_layer_host_workspace_bytes",
-           "moe_layer_forward_host")
+           "moe_layer_forward_host", "fp8_quantize", "moe_route_quantize_fp8")
 
 
 class Nvfp4Error(RuntimeError):
@@ -103,6 +103,10 @@ def load(build_if_missing: bool = True):
     L.mxfp4_pack_weight_scales.argtypes = [_P, _I, _I, _I, _P, _P]
     L.moe_route_quantize_mxfp4.restype = _I
     L.moe_route_quantize_mxfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.fp8_quantize.restype = _I
+    L.fp8_quantize.argtypes = [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _SZ, _P]
+    L.moe_route_quantize_fp8.restype = _I
+    L.moe_route_quantize_fp8.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     _lib = L
     return L
 
@@ -306,6 +310,50 @@ def moe_route_quantize_mxfp4(x, logits, k, dev_status=None):
     return out
 
 
+def fp8_quantize(x, S=None, codes=None, workspace=None):
+    """FP8 (E4M3) codes of x [rows, cols] (bf16 or fp32) with one per-tensor
+    decode scale.  S=None: dynamic (written to a new device scalar).
+    Returns (codes uint8 [rows, cols], S)."""
+    L = load()
+    rows, cols = x.shape
+    dev = x.device
+    dt = NVFP4_DT_BF16 if x.dtype == torch.bfloat16 else NVFP4_DT_F32
+    dynamic = S is None
+    if S is None:
+        S = torch.zeros(4, dtype=torch.float32, device=dev)
+    if codes is None:
+        codes = _empty((rows, cols), torch.uint8, dev)
+    if workspace is None and dynamic:
+        workspace = _empty(int(L.nvfp4_quantize_workspace_bytes(rows, cols)), torch.uint8, dev)
+    _check("fp8_quantize", L.fp8_quantize(_ptr(x), dt, rows, cols, x.stride(0), _ptr(S),
+                                          NVFP4_SCALE_DYNAMIC if dynamic else NVFP4_SCALE_STATIC, _ptr(codes),
+                                          _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream()))
+    return codes, S[:1]
+
+
+def moe_route_quantize_fp8(x, logits, k, dev_status=None):
+    """Routing + FP8 quantisation of x [T, H] bf16 written in permuted order.
+    Returns dict(ids, w, offsets, perm, inv, S_x, act_codes)."""
+    L = load()
+    T, H = x.shape
+    E = logits.shape[1]
+    dev = x.device
+    R = T * k
+    out = dict(ids=_empty((T, k), torch.int32, dev), w=_empty((T, k), torch.float32, dev),
+               offsets=_empty((E + 1,), torch.int32, dev), perm=_empty((max(R, 1),), torch.int32, dev),
+               inv=_empty((max(R, 1),), torch.int32, dev), S_x=torch.zeros(4, dtype=torch.float32, device=dev),
+               act_codes=_empty((max(R, 1), H), torch.uint8, dev))
+    ws = _empty(max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256), torch.uint8, dev)
+    _check("moe_route_quantize_fp8",
+           L.moe_route_quantize_fp8(_ptr(x), _ptr(logits), T, H, E, k, _ptr(out["ids"]), _ptr(out["w"]),
+                                    _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv"]), _ptr(out["S_x"]),
+                                    _ptr(out["act_codes"]), _ptr(dev_status), _ptr(ws), ws.numel(), _stream()))
+    for key in ("perm", "inv", "act_codes"):
+        out[key] = out[key][:R]
+    out["S_x"] = out["S_x"][:1]
+    return out
+
+
 def moe_grouped_gemm_nvfp4(mode, a, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, N, K, out=None,
                            dev_status=None):
     L = load()
@@ -324,6 +372,11 @@ def moe_swiglu_requant(G, mode, S_h=None):
     R, I2 = G.shape
     I = I2 // 2
     dev = G.device
+    if mode == MOE_W4A8:
+        hc = _empty((max(R, 1), I), torch.uint8, dev)
+        _check("moe_swiglu_requant",
+               L.moe_swiglu_requant(_ptr(G), R, I, mode, _ptr(S_h), _ptr(hc), None, None, _stream()))
+        return hc[:R]
     if mode in (MOE_W4A4, MOE_MXW4A4):
         hc = _empty((max(R, 1), I // 2), torch.uint8, dev)
         hs = _empty((max(R, 1), I // 16 if mode == MOE_W4A4 else mxfp4_scale_pitch(I)), torch.uint8, dev)

@@ -307,11 +307,68 @@ int moe_route_quantize_mxfp4(const void* x, const float* logits, int T, int H, i
   return cuda_status(launch_mx_quantize_scatter(x, T, H, k, inv, a_codes, a_scales, st));
 }
 
+int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x, float* S, int scale_mode,
+                 uint8_t* codes, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (rows < 0 || cols < 0 || S == nullptr) return NVFP4_E_INVAL;
+  if (x_dtype != NVFP4_DT_BF16 && x_dtype != NVFP4_DT_F32) return NVFP4_E_INVAL;
+  if (scale_mode != NVFP4_SCALE_STATIC && scale_mode != NVFP4_SCALE_DYNAMIC) return NVFP4_E_INVAL;
+  if (cols % 16 != 0 || ld_x < cols) return NVFP4_E_SHAPE;
+  if ((x_dtype == NVFP4_DT_BF16 && ld_x % 8 != 0) || (x_dtype == NVFP4_DT_F32 && ld_x % 4 != 0))
+    return NVFP4_E_SHAPE;
+  if (rows > 0 && cols > 0) {
+    if (x == nullptr || codes == nullptr) return NVFP4_E_INVAL;
+    if (!aligned16(x) || !aligned16(codes)) return NVFP4_E_ALIGN;
+  }
+  if (!aligned16(S)) return NVFP4_E_ALIGN;
+  if (scale_mode == NVFP4_SCALE_DYNAMIC) {
+    if (workspace == nullptr || workspace_bytes < nvfp4_quantize_workspace_bytes(rows, cols))
+      return NVFP4_E_WORKSPACE;
+    if (!aligned16(workspace)) return NVFP4_E_ALIGN;
+  }
+  CHECK_ARCH();
+  return cuda_status(launch_fp8_quantize(x, x_dtype, rows, cols, ld_x, S, scale_mode == NVFP4_SCALE_DYNAMIC,
+                                         static_cast<uint32_t*>(workspace), codes,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_route_quantize_fp8(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                           float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, float* S_x,
+                           uint8_t* a_codes, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                           nvfp4_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
+  if (k > E || k > 32 || E > 1024 || H % 256 != 0) return NVFP4_E_SHAPE;
+  if (expert_offsets == nullptr || S_x == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(expert_offsets) || !aligned16(S_x)) return NVFP4_E_ALIGN;
+  if (T > 0) {
+    if (x == nullptr || logits == nullptr || topk_ids == nullptr || topk_w == nullptr || perm == nullptr ||
+        inv == nullptr || a_codes == nullptr)
+      return NVFP4_E_INVAL;
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(perm) ||
+        !aligned16(inv) || !aligned16(a_codes))
+      return NVFP4_E_ALIGN;
+    if (workspace == nullptr || workspace_bytes < route_workspace_bytes(T, E)) return NVFP4_E_WORKSPACE;
+    if (!aligned16(workspace)) return NVFP4_E_ALIGN;
+  }
+  CHECK_ARCH();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (cudaMemsetAsync(S_x, 0, sizeof(float), st) != cudaSuccess) return NVFP4_E_CUDA;
+    return cuda_status(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st));
+  }
+  // routing (+ the activation amax in the same pass), then each token's FP8
+  // row goes straight to its k permuted rows
+  if (launch_route_only(logits, T, E, k, topk_ids, topk_w, expert_offsets, perm, inv, dev_status, workspace, st, x,
+                        H) != cudaSuccess)
+    return NVFP4_E_CUDA;
+  return cuda_status(launch_fp8_quantize_scatter(x, T, H, k, inv, static_cast<const uint32_t*>(workspace) + 1, S_x,
+                                                 a_codes, st));
+}
+
 int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, const float* a_S,
                            const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                            const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
                            int32_t* dev_status, nvfp4_stream_t stream) {
-  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4) return NVFP4_E_INVAL;
+  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8) return NVFP4_E_INVAL;
   if (E <= 0 || N < 0 || K < 0 || R < 0) return NVFP4_E_INVAL;
   if (N % 128 != 0 || K % 256 != 0) return NVFP4_E_SHAPE;
   if (R == 0 || N == 0 || K == 0) return NVFP4_OK;
@@ -320,14 +377,18 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
     return NVFP4_E_INVAL;
   if (mode != MOE_MXW4A4 && w_S == nullptr) return NVFP4_E_INVAL;
   if (mode == MOE_W4A4 && (a_scales == nullptr || a_S == nullptr)) return NVFP4_E_INVAL;
+  if (mode == MOE_W4A8 && a_S == nullptr) return NVFP4_E_INVAL;
   if (mode == MOE_MXW4A4 && a_scales == nullptr) return NVFP4_E_INVAL;
   if (!aligned16(a) || !aligned16(w_codes) || !aligned16(w_scales_packed) || !aligned16(out))
     return NVFP4_E_ALIGN;
-  if (mode != MOE_W4A16 && !aligned16(a_scales)) return NVFP4_E_ALIGN;
+  if ((mode == MOE_W4A4 || mode == MOE_MXW4A4) && !aligned16(a_scales)) return NVFP4_E_ALIGN;
   CHECK_ARCH();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == MOE_W4A8)
+    return cuda_status(launch_gemm_w4a8(static_cast<const uint8_t*>(a), a_S, w_codes, w_scales_packed, w_S,
+                                        expert_offsets, E, N, K, R, out, dev_status, st));
   // many tokens per expert (prefill, large-M GEMMs): CTA pairs on one MMA
-  if (mode != MOE_W4A16 && gemm_w4a4_pair_eligible(E, N, R))
+  if ((mode == MOE_W4A4 || mode == MOE_MXW4A4) && gemm_w4a4_pair_eligible(E, N, R))
     return cuda_status(launch_gemm_w4a4_pair(mode == MOE_MXW4A4, static_cast<const uint8_t*>(a), a_scales, a_S,
                                              w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out,
                                              dev_status, st));
@@ -343,7 +404,7 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
 
 int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
                        uint8_t* h_scales, void* h_bf16, nvfp4_stream_t stream) {
-  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4) return NVFP4_E_INVAL;
+  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8) return NVFP4_E_INVAL;
   if (R < 0 || I < 0) return NVFP4_E_INVAL;
   if (I % (mode == MOE_MXW4A4 ? 32 : 16) != 0) return NVFP4_E_SHAPE;
   if ((int64_t)R * I == 0) return NVFP4_OK;
@@ -355,9 +416,10 @@ int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h,
     return cuda_status(launch_swiglu_requant_mx(G, R, I, h_codes, h_scales, reinterpret_cast<cudaStream_t>(stream)));
   }
   if (mode == MOE_W4A4 && (S_h == nullptr || h_codes == nullptr || h_scales == nullptr)) return NVFP4_E_INVAL;
+  if (mode == MOE_W4A8 && (S_h == nullptr || h_codes == nullptr)) return NVFP4_E_INVAL;
   if (mode == MOE_W4A16 && h_bf16 == nullptr) return NVFP4_E_INVAL;
   if (!aligned16(G)) return NVFP4_E_ALIGN;
-  if (mode == MOE_W4A4 && !aligned16(h_codes)) return NVFP4_E_ALIGN;
+  if ((mode == MOE_W4A4 || mode == MOE_W4A8) && !aligned16(h_codes)) return NVFP4_E_ALIGN;
   if (mode == MOE_W4A16 && !aligned16(h_bf16)) return NVFP4_E_ALIGN;
   CHECK_ARCH();
   return cuda_status(
@@ -412,6 +474,10 @@ static LayerWs carve(void* base, int mode, int T, int H, int I, int E, int k) {
     w.a_scales = take(R * (size_t)mx_scale_pitch(H));
     w.h_codes = take(R * I / 2);
     w.h_scales = take(R * (size_t)mx_scale_pitch(I));
+  } else if (mode == MOE_W4A8) {
+    w.S_x = reinterpret_cast<float*>(take(16));
+    w.a_codes = take(R * H);
+    w.h_codes = take(R * I);
   } else if (mode == MOE_W4A4) {
     w.S_x = reinterpret_cast<float*>(take(16));
     w.a_codes = take(R * H / 2);
@@ -436,7 +502,7 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
                       const uint8_t* w2_codes, const uint8_t* w2_scales_packed, const float* w2_S, const float* S_h,
                       float* out, int32_t* dev_status, void* workspace, size_t workspace_bytes,
                       nvfp4_stream_t stream) {
-  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4) return NVFP4_E_INVAL;
+  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8) return NVFP4_E_INVAL;
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
   if (H % 256 != 0 || I % 256 != 0 || k > E || k > 32 || E > 1024) return NVFP4_E_SHAPE;
   if (T == 0) return NVFP4_OK;
@@ -444,7 +510,7 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
       w2_codes == nullptr || w2_scales_packed == nullptr || out == nullptr)
     return NVFP4_E_INVAL;
   if (mode != MOE_MXW4A4 && (w13_S == nullptr || w2_S == nullptr)) return NVFP4_E_INVAL;
-  if (mode == MOE_W4A4 && S_h == nullptr) return NVFP4_E_INVAL;
+  if ((mode == MOE_W4A4 || mode == MOE_W4A8) && S_h == nullptr) return NVFP4_E_INVAL;
   if (workspace == nullptr || workspace_bytes < moe_layer_workspace_bytes(mode, T, H, I, E, k))
     return NVFP4_E_WORKSPACE;
   if (!aligned16(workspace) || !aligned16(x) || !aligned16(out)) return NVFP4_E_ALIGN;
@@ -463,6 +529,18 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
     if (s != NVFP4_OK) return s;
     s = moe_grouped_gemm_nvfp4(MOE_MXW4A4, w.h_codes, w.h_scales, nullptr, w2_codes, w2_scales_packed, nullptr,
                                w.offsets, E, H, I, R, w.Y, dev_status, stream);
+    if (s != NVFP4_OK) return s;
+  } else if (mode == MOE_W4A8) {
+    s = moe_route_quantize_fp8(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_codes,
+                               dev_status, w.route, route_workspace_bytes(T, E), stream);
+    if (s != NVFP4_OK) return s;
+    s = moe_grouped_gemm_nvfp4(MOE_W4A8, w.a_codes, nullptr, w.S_x, w13_codes, w13_scales_packed, w13_S, w.offsets,
+                               E, 2 * I, H, R, w.G, dev_status, stream);
+    if (s != NVFP4_OK) return s;
+    s = moe_swiglu_requant(w.G, R, I, MOE_W4A8, S_h, w.h_codes, nullptr, nullptr, stream);
+    if (s != NVFP4_OK) return s;
+    s = moe_grouped_gemm_nvfp4(MOE_W4A8, w.h_codes, nullptr, S_h, w2_codes, w2_scales_packed, w2_S, w.offsets, E,
+                               H, I, R, w.Y, dev_status, stream);
     if (s != NVFP4_OK) return s;
   } else if (mode == MOE_W4A4) {
     s = moe_route_quantize_nvfp4(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_codes,
@@ -514,7 +592,7 @@ int moe_layer_forward_host(int mode, const void* x_host, const float* logits_hos
                            const uint8_t* w2_codes, const uint8_t* w2_scales_packed, const float* w2_S,
                            const float* S_h, float* out_host, int32_t* dev_status, void* workspace,
                            size_t workspace_bytes, nvfp4_stream_t stream) {
-  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4) return NVFP4_E_INVAL;
+  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8) return NVFP4_E_INVAL;
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
   if (H % 256 != 0 || I % 256 != 0 || k > E || k > 32 || E > 1024) return NVFP4_E_SHAPE;
   if (T == 0) return NVFP4_OK;

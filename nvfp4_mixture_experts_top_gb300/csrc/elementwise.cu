@@ -1,6 +1,7 @@
 // elementwise.cu -- HBM-bound kernels of the NVFP4 MoE path: quantiser
 // (with the warp-shuffle tensor amax), weight-scale packing, SwiGLU +
-// requantisation, and the weighted combine; and their MXFP4 counterparts.
+// requantisation, and the weighted combine; their MXFP4 counterparts; and the
+// FP8 (E4M3, per-tensor scale) activation quantisers of the W4A8 mode.
 //
 // All of them are one-pass streaming kernels: coalesced 16-byte loads and
 // stores, grids sized in multiples of the SM count, no shared-memory staging
@@ -126,6 +127,76 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(const __nv_bfloat
 }
 
 // ---------------------------------------------------------------------------
+// FP8 (E4M3) activations with a per-tensor decode scale (the W4A8 mode)
+// ---------------------------------------------------------------------------
+
+// FP8 activation code of x with decode scale s: the sign bit of x / s, then
+// E4M3(RNE, satfinite) of |x / s|; s == 0 gives code 0.
+__device__ __forceinline__ uint32_t fp8_code(float x, float s) {
+  if (s == 0.0f) return 0;
+  const float q = __fdiv_rn(x, s);
+  return e4m3_from_f32(fabsf(q)) | ((__float_as_uint(q) >> 31) << 7);
+}
+
+// Eight inputs -> eight FP8 codes (two little-endian words), decode scale s.
+__device__ __forceinline__ uint2 fp8_codes8(const float (&v)[8], float s) {
+  uint32_t w[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    w[q] = fp8_code(v[4 * q], s) | (fp8_code(v[4 * q + 1], s) << 8) | (fp8_code(v[4 * q + 2], s) << 16) |
+           (fp8_code(v[4 * q + 3], s) << 24);
+  return make_uint2(w[0], w[1]);
+}
+
+// One thread per 8 elements.  dynamic: S = amax / 448 from the amax word;
+// static: S read from *S.
+template <typename T>
+__global__ void __launch_bounds__(256) fp8_quantize_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+                                                           int64_t ld, float* __restrict__ S, int dynamic,
+                                                           const uint32_t* __restrict__ amax_bits,
+                                                           uint8_t* __restrict__ codes) {
+  pdl_wait();
+  pdl_trigger();
+  float s;
+  if (dynamic) {
+    s = __fdiv_rn(__uint_as_float(*amax_bits), 448.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *S = s;
+  } else {
+    s = *S;
+  }
+  const int64_t nv_row = cols / 8;
+  const int64_t nv = rows * nv_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nv_row, c = (i % nv_row) * 8;
+    float v[8];
+    load8<T>(x + r * ld + c, v);
+    *reinterpret_cast<uint2*>(codes + r * cols + c) = fp8_codes8(v, s);
+  }
+}
+
+// Quantise x [T, H] (bf16) to FP8 with the dynamic scale S = amax / 448 and
+// write every token's row straight to its k permuted rows inv[t*k + j].
+__global__ void __launch_bounds__(256) fp8_quantize_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T,
+                                                                   int64_t H, int k, const int32_t* __restrict__ inv,
+                                                                   const uint32_t* __restrict__ amax_bits,
+                                                                   float* __restrict__ S,
+                                                                   uint8_t* __restrict__ codes) {
+  pdl_wait();
+  pdl_trigger();
+  const float s = __fdiv_rn(__uint_as_float(*amax_bits), 448.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *S = s;
+  const int64_t nv_row = H / 8;
+  const int64_t nv = (int64_t)T * nv_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / nv_row, c = (i % nv_row) * 8;
+    float v[8];
+    load8<__nv_bfloat16>(x + t * H + c, v);
+    const uint2 w = fp8_codes8(v, s);
+    for (int j = 0; j < k; ++j) *reinterpret_cast<uint2*>(codes + (int64_t)__ldg(inv + t * k + j) * H + c) = w;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // weight-scale packing: linear [E, N, K/16] -> 512-byte atoms
 // ---------------------------------------------------------------------------
 
@@ -160,7 +231,7 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
   pdl_trigger();
   const int64_t nb_row = I / 16;
   const int64_t nblk = R * nb_row;
-  const float s = (mode == MOE_W4A4) ? *S_h : 0.0f;
+  const float s = (mode == MOE_W4A4 || mode == MOE_W4A8) ? *S_h : 0.0f;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / nb_row, b = i % nb_row;
     const float4* gp = reinterpret_cast<const float4*>(G + r * 2 * I + b * 16);
@@ -179,6 +250,13 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
       const uint32_t sc = quantize_block16(h, s, w0, w1);
       *reinterpret_cast<uint2*>(h_codes + r * (I / 2) + b * 8) = make_uint2(w0, w1);
       h_scales[r * nb_row + b] = (uint8_t)sc;
+    } else if (mode == MOE_W4A8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = fp8_code(h[4 * q], s) | (fp8_code(h[4 * q + 1], s) << 8) | (fp8_code(h[4 * q + 2], s) << 16) |
+               (fp8_code(h[4 * q + 3], s) << 24);
+      *reinterpret_cast<uint4*>(h_codes + r * I + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
       uint32_t w[8];
 #pragma unroll
@@ -431,6 +509,39 @@ cudaError_t launch_quantize_scatter(const void* x_bf16, int T, int H, int k, con
   if (nblk == 0) return cudaSuccess;
   return launch_pdl(quantize_scatter_kernel, grid_for(nblk, 256), 256, 0, st, static_cast<const __nv_bfloat16*>(x_bf16),
                     T, (int64_t)H, k, inv, amax_bits, S, codes, scales);
+}
+
+cudaError_t launch_fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,
+                                int dynamic, uint32_t* amax_ws, uint8_t* codes, cudaStream_t st) {
+  if (rows == 0) {
+    if (dynamic) return cudaMemsetAsync(S, 0, sizeof(float), st);
+    return cudaSuccess;
+  }
+  if (dynamic) {
+    cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    const int g = grid_for(rows * cols / 8, 256);
+    if (x_dtype == NVFP4_DT_BF16)
+      e = launch_pdl(amax_kernel<__nv_bfloat16>, g, 256, 0, st, static_cast<const __nv_bfloat16*>(x), rows, cols, ld,
+                     amax_ws);
+    else
+      e = launch_pdl(amax_kernel<float>, g, 256, 0, st, static_cast<const float*>(x), rows, cols, ld, amax_ws);
+    if (e != cudaSuccess) return e;
+  }
+  const int g = grid_for(rows * cols / 8, 256);
+  if (x_dtype == NVFP4_DT_BF16)
+    return launch_pdl(fp8_quantize_kernel<__nv_bfloat16>, g, 256, 0, st, static_cast<const __nv_bfloat16*>(x), rows,
+                      cols, ld, S, dynamic, static_cast<const uint32_t*>(amax_ws), codes);
+  return launch_pdl(fp8_quantize_kernel<float>, g, 256, 0, st, static_cast<const float*>(x), rows, cols, ld, S,
+                    dynamic, static_cast<const uint32_t*>(amax_ws), codes);
+}
+
+cudaError_t launch_fp8_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
+                                        const uint32_t* amax_bits, float* S, uint8_t* codes, cudaStream_t st) {
+  const int64_t nv = (int64_t)T * (H / 8);
+  if (nv == 0) return cudaSuccess;
+  return launch_pdl(fp8_quantize_scatter_kernel, grid_for(nv, 256), 256, 0, st,
+                    static_cast<const __nv_bfloat16*>(x_bf16), T, (int64_t)H, k, inv, amax_bits, S, codes);
 }
 
 cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st) {

@@ -1,6 +1,8 @@
 // gemm_w4a16.cu -- ragged grouped GEMM with BF16 activations and NVFP4
 // weights (W4A16): the FP4 weights are dequantised to BF16 inside the kernel
-// and multiplied on the tensor cores with tcgen05.mma kind::f16.
+// and multiplied on the tensor cores with tcgen05.mma kind::f16.  The same
+// kernel, instantiated with FP8 = true, runs the W4A8 mode (FP8 E4M3
+// activations with a per-tensor scale; F16 operands, see the template).
 //
 // e2m1 * e4m3 products need at most 6 significant bits and lie in
 // [2^-10, 2688], so the dequantised weight is exact in BF16 and the only
@@ -68,6 +70,8 @@ constexpr int NUM_THREADS = (6 + NUM_DEQ_WARPS) * 32;  // 448
 struct Params {
   const uint8_t* w_scales;
   const float* w_S;
+  const uint8_t* a_fp8;  // W4A8: FP8 token codes [R, K] (read by the dequantisation warps)
+  const float* a_S;      // W4A8: their per-tensor decode scale
   const int32_t* offsets;
   float* out;
   int32_t* dev_status;
@@ -97,6 +101,46 @@ __device__ __forceinline__ void dequant8(uint32_t codes, __half2 scale2, uint32_
   }
 }
 
+// 8 packed E2M1 codes times one E4M3 scale -> 8 F16 in 4 words, for the
+// W4A8 mode's F16 MMA (no widening: e2m1 * e4m3 is exact in f16).
+__device__ __forceinline__ void dequant8_f16(uint32_t codes, __half2 scale2, uint32_t* out) {
+  uint32_t h2s[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h2s[0]), "=r"(h2s[1]), "=r"(h2s[2]), "=r"(h2s[3])
+      : "r"(codes));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h2s[i]), scale2);
+    out[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+// Two E4M3 codes (low byte = the lower-K element) -> one f16x2 word (exact).
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)two));
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with F16 inputs and fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
+  return (1u << 4)              // D format: F32 (A and B formats 0: F16)
+         | ((N >> 3) << 17)
+         | ((M >> 4) << 24);
+}
+
+// FP8 = false: W4A16 (BF16 tokens by TMA, weights dequantised to BF16).
+// FP8 = true: W4A8 -- FP8 E4M3 token codes with a per-tensor scale; weights
+// dequantised to F16 and the tokens converted to F16 (both exact) by the
+// dequantisation warps, which write them into the stage's B area in the
+// 128-byte-swizzled layout the TMA would have produced; MMA kind::f16 with
+// F16 operands; alpha = a_S * w_S[e].
+template <bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                       const Params p) {
@@ -136,7 +180,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
-    prefetch_tmap(&tm_b);
+    if (!FP8) prefetch_tmap(&tm_b);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, TMEM_COLS);
@@ -179,7 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       const WorkItem it = item_j(j, w);
       const uint8_t* wsc = p.w_scales + ((size_t)(it.e * NT + it.nt) * (p.K / 64)) * 512;
-      const uint32_t bytes = W_BYTES + WS_BYTES + it.ng * NATOM * B_GROUP;
+      const uint32_t bytes = W_BYTES + WS_BYTES + (FP8 ? 0 : it.ng * NATOM * B_GROUP);
       for (int kc = 0; kc < KCH; ++kc) {
         if (!warp_wait(&raw_empty[stage], phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
@@ -200,6 +244,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ew_arrive_expect_tx(&raw_full[stage], bytes);
         ew_tma_load_2d(sb + OFF_W, &tm_w, &raw_full[stage], kc * (KC / 2), it.e * p.N + it.nt * BM, pol_w);
         ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * NATOM * 512, WS_BYTES, &raw_full[stage], pol_w);
+        if (!FP8)
         for (int g = 0; g < it.ng; ++g)
 #pragma unroll
           for (int a = 0; a < NATOM; ++a)
@@ -229,7 +274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t smem_base = smem_u32(smem);
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       const int ng = item_j(j, w).ng;
-      const uint32_t idesc = idesc_bf16(BM, TG * ng);
+      const uint32_t idesc = FP8 ? idesc_f16(BM, TG * ng) : idesc_bf16(BM, TG * ng);
       if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
         ok = false;
         break;
@@ -283,7 +328,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       const WorkItem it = item_j(j, w);
-      const float alpha = __ldg(p.w_S + it.e);
+      const float alpha = FP8 ? __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e)) : __ldg(p.w_S + it.e);
       const int n = it.nt * BM + q * 32 + lane;
       if (!warp_wait(&acc_full[acc], acc_phase, &abort_flag, p.dev_status)) {
         ok = false;
@@ -317,7 +362,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0, slot_phase = 0;
     bool ok = true;
     int it_d = 0;
-    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+    // W4A8 token conversion: thread t of the 256 dequantisation threads owns
+    // token row (t & 31) of group t >> 7, K atom (t >> 5) & 3 (64 codes)
+    const int tt = (warp - 6) * 32 + lane;
+    const int tg = tt >> 7, tatom = (tt >> 5) & 3, trow = tt & 31;
+    for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
+      int t_src = -1;  // global token row this thread converts, or -1
+      if (FP8) {
+        const WorkItem it = item_j(j, w);
+        const int row = it.r0 + tg * TG + trow;
+        if (tg < it.ng && row < p.R) t_src = row;
+      }
       for (int kc = 0; kc < KCH; ++kc) {
         if (!warp_wait(&raw_full[stage], phase, &abort_flag, p.dev_status) ||
             !warp_wait(&a_empty[slot], slot_phase ^ 1, &abort_flag, p.dev_status)) {
@@ -326,6 +381,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         if (lane == 0 && warp == 6) W4A16_TRACE(1, it_d);
+        uint4 tok[4];  // W4A8: this thread's 64 token codes of the stage, in flight during the dequantisation
+        if (FP8) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.a_fp8 + (size_t)(t_src < 0 ? 0 : t_src) * p.K +
+                                                            kc * KC + tatom * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tok[i] = t_src < 0 ? make_uint4(0, 0, 0, 0) : __ldg(src + i);
+        }
         const uint8_t* sw = smem + stage * RSTAGE_BYTES + OFF_W + r * 128;
         const uint8_t* ss = smem + stage * RSTAGE_BYTES + OFF_WS;
         // row r's 64 bytes for K half h: 16-byte chunks 4h..4h+3, placed by the
@@ -345,10 +407,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 4; ++j) {  // 16-element block j
             const __half sh = __float2half_rn(f32_from_e4m3((s4 >> (8 * j)) & 0xFFu));
             const __half2 s2 = __halves2half2(sh, sh);
-            dequant8(words[2 * j], s2, outw + 8 * j);
-            dequant8(words[2 * j + 1], s2, outw + 8 * j + 4);
+            if (FP8) {
+              dequant8_f16(words[2 * j], s2, outw + 8 * j);
+              dequant8_f16(words[2 * j + 1], s2, outw + 8 * j + 4);
+            } else {
+              dequant8(words[2 * j], s2, outw + 8 * j);
+              dequant8(words[2 * j + 1], s2, outw + 8 * j + 4);
+            }
           }
           tmem_st_32x32b_x32(a_col + 32 * part, outw);
+        }
+        if (FP8) {
+          // the tokens: 64 codes -> 64 f16 = 8 chunks of 16 bytes at chunk
+          // c ^ (row & 7) of the row's 128-byte line (128-byte swizzle)
+          if (t_src >= 0) {  // other rows of the B area are not read (N = 32 * ng) or not stored
+            uint8_t* dst = smem + stage * RSTAGE_BYTES + OFF_B + tatom * B_ATOM + tg * B_GROUP + trow * 128;
+            const uint32_t wv[16] = {tok[0].x, tok[0].y, tok[0].z, tok[0].w, tok[1].x, tok[1].y, tok[1].z, tok[1].w,
+                                     tok[2].x, tok[2].y, tok[2].z, tok[2].w, tok[3].x, tok[3].y, tok[3].z, tok[3].w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(dst + ((c ^ (trow & 7)) << 4)) =
+                  make_uint4(f16x2_from_e4m3x2(wv[2 * c] & 0xFFFFu), f16x2_from_e4m3x2(wv[2 * c] >> 16),
+                             f16x2_from_e4m3x2(wv[2 * c + 1] & 0xFFFFu), f16x2_from_e4m3x2(wv[2 * c + 1] >> 16));
+          }
+          fence_proxy_async_smem();  // generic writes -> visible to the MMA (async proxy)
         }
         tmem_st_wait();
         if (lane == 0 && warp == 6) W4A16_TRACE(2, it_d);
@@ -379,14 +461,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace w4a16
 
-cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const uint8_t* w_scales_packed,
-                              const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
-                              int32_t* dev_status, cudaStream_t st) {
+template <bool FP8>
+static cudaError_t launch_dequant_gemm(const void* a, const float* a_S, const uint8_t* w_codes,
+                                       const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E,
+                                       int N, int K, int R, float* out, int32_t* dev_status, cudaStream_t st) {
   using namespace w4a16;
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   {
-    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a16_kernel), SMEM_BYTES);
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a16_kernel<FP8>), SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tm_w, tm_b;
@@ -394,12 +477,18 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
   cudaError_t err =
       make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, 128);
   if (err != cudaSuccess) return err;
-  // bf16 tokens viewed as bytes: [R rows, 2K bytes], box 128 B x 32 rows, 128-byte swizzle
-  err = make_tmap_2d_u8(&tm_b, a_bf16, (uint64_t)K * 2, (uint64_t)R, (uint64_t)K * 2, 128, TG, 128);
-  if (err != cudaSuccess) return err;
+  if (FP8) {
+    tm_b = tm_w;  // not used: the dequantisation warps read the FP8 tokens
+  } else {
+    // bf16 tokens viewed as bytes: [R rows, 2K bytes], box 128 B x 32 rows, 128-byte swizzle
+    err = make_tmap_2d_u8(&tm_b, a, (uint64_t)K * 2, (uint64_t)R, (uint64_t)K * 2, 128, TG, 128);
+    if (err != cudaSuccess) return err;
+  }
   Params p;
   p.w_scales = w_scales_packed;
   p.w_S = w_S;
+  p.a_fp8 = FP8 ? static_cast<const uint8_t*>(a) : nullptr;
+  p.a_S = a_S;
   p.offsets = offsets;
   p.out = out;
   p.dev_status = dev_status;
@@ -408,7 +497,21 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
   p.K = K;
   p.R = R;
   p.drop_stage = fault_injection_drop_stage();
-  return launch_pdl(gemm_w4a16_kernel, num_sms(), NUM_THREADS, SMEM_BYTES, st, tm_w, tm_b, p);
+  return launch_pdl(gemm_w4a16_kernel<FP8>, num_sms(), NUM_THREADS, SMEM_BYTES, st, tm_w, tm_b, p);
+}
+
+cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const uint8_t* w_scales_packed,
+                              const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
+                              int32_t* dev_status, cudaStream_t st) {
+  return launch_dequant_gemm<false>(a_bf16, nullptr, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                                    dev_status, st);
+}
+
+cudaError_t launch_gemm_w4a8(const uint8_t* a_fp8, const float* a_S, const uint8_t* w_codes,
+                             const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E, int N,
+                             int K, int R, float* out, int32_t* dev_status, cudaStream_t st) {
+  return launch_dequant_gemm<true>(a_fp8, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out, dev_status,
+                                   st);
 }
 
 }  // namespace nvfp4moe

@@ -93,6 +93,18 @@ cudaError_t launch_gemm_w4a4_pair(bool mx, const uint8_t* a_codes, const uint8_t
 cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const uint8_t* w_scales_packed,
                               const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
                               int32_t* dev_status, cudaStream_t st);
+// W4A8: FP8 E4M3 token codes [R, K] with the per-tensor decode scale *a_S.
+cudaError_t launch_gemm_w4a8(const uint8_t* a_fp8, const float* a_S, const uint8_t* w_codes,
+                             const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E, int N,
+                             int K, int R, float* out, int32_t* dev_status, cudaStream_t st);
+// FP8 (E4M3) activations with one per-tensor decode scale (the W4A8 mode):
+// dynamic S = amax / 448 written to *S, or static *S read.
+cudaError_t launch_fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld, float* S,
+                                int dynamic, uint32_t* amax_ws, uint8_t* codes, cudaStream_t st);
+// x [T, H] bf16 -> FP8 codes of each token in its k permuted rows (amax bits
+// from the routing pass; S written to *S).
+cudaError_t launch_fp8_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
+                                        const uint32_t* amax_bits, float* S, uint8_t* codes, cudaStream_t st);
 
 // Router logits [T, E] = x [T, H] . W [E, H]^T (bf16 in, fp32 out) on the
 // tensor cores, K split over the SMs; workspace holds the fp32 partials

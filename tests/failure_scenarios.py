@@ -54,6 +54,14 @@ def gemm(dev, mode):
                 to_dev(offs, dev), N, K)
         m = B.MOE_W4A4
         ref = lambda: orc.grouped_gemm_w4a4(ac, as_, aS, w[0], w[1], w[2], offs)  # noqa: E731
+    elif mode == "w4a8":
+        w = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, N, K).numpy() for e in range(E)]))
+        a = wl.random_fp32((8, K), seed=3, tag="fail8").to(torch.bfloat16).float().numpy()
+        ac, aS = orc.fp8_quantize(a)
+        args = (to_dev(ac, dev), None, to_dev(np.array([aS]), dev), *upload_weights(w, E, N, K, dev),
+                to_dev(offs, dev), N, K)
+        m = B.MOE_W4A8
+        ref = lambda: orc.grouped_gemm_w4a8(ac, aS, w[0], w[1], w[2], offs)  # noqa: E731
     else:
         w = orc.quantize_experts(np.stack([wl.expert_weight_fp32("w2", e, N, K).numpy() for e in range(E)]))
         a = wl.random_fp32((8, K), seed=2, tag="fail16").to(torch.bfloat16).float().numpy()

@@ -12,10 +12,11 @@ Checks
 * routing ids, offsets restricted to the sample, and the permutation through
   inv: bit for bit (routing of the GPU logits equals the oracle's routing);
 * every requantised h code (W4A4 NVFP4 with the static S_h; MXFP4 with its
-  per-block shared exponent): equal to the oracle's, except where the
-  oracle's own fp32 h lies within FLIP_WINDOW (relative) of that decision's
-  rounding boundary -- G is accumulated in fp32 on the tensor cores and in
-  fp64 by the oracle, so h can differ in its last bits;
+  per-block shared exponent; W4A8 FP8 with its static scale): equal to the
+  oracle's, except where the oracle's own fp32 h lies within FLIP_WINDOW
+  (relative) of that decision's rounding boundary -- G is accumulated in
+  fp32 on the tensor cores and in fp64 by the oracle, so h can differ in its
+  last bits;
 * the output as a whole: relative Frobenius error <= 1e-3;
 * every token without an h-code difference: relative Frobenius error <= 1e-3
   and max error <= 1e-2 x that token's output RMS;
@@ -117,8 +118,22 @@ def mx_boundary_distance(v):
     return np.minimum(d_el, np.repeat(d_scale, 32, axis=1))
 
 
+def fp8_boundary_distance(v, S):
+    """Relative distance of every element of v (fp32 values about to be
+    FP8-quantised with decode scale S) to the nearest E4M3 rounding midpoint."""
+    q = np.abs(np.asarray(v, np.float64)) / np.float64(S)
+    grid = _E4M3[:0x7F]
+    mids = (grid[1:] + grid[:-1]) / 2
+    idx = np.clip(np.searchsorted(mids, q), 1, len(mids) - 1)
+    d = np.minimum(np.abs(q - mids[idx - 1]), np.abs(q - mids[idx]))
+    return d / np.maximum(q, 1e-30)
+
+
 def _decode_h(codes, scales, fmt, S_h):
-    """Decoded h [rows, I] (fp64) from packed codes and linear block scales."""
+    """Decoded h [rows, I] (fp64) from packed codes and linear block scales
+    (FP8: one E4M3 code per element, no block scales)."""
+    if fmt == "fp8":
+        return _E4M3[codes] * np.float64(S_h)
     c = unpack_codes(codes)
     v = _E2M1[c]
     if fmt == "nvfp4":
@@ -149,7 +164,8 @@ def check_layer(orc, cfg, mode, d, x, logits, gpu_w, tokens=None, seed=0, device
     with the oracle on `tokens` (default: all).  gpu_w: ((codes13, lin13),
     (codes2, lin2)) on the GPU, to check the weights are the oracle's.
     Returns a dict of the figures it printed."""
-    fmt = "mx" if mode == "mxw4a4" else "nvfp4"
+    fmt = "mx" if mode == "mxw4a4" else "nvfp4"           # the weights' format
+    hfmt = {"w4a4": "nvfp4", "mxw4a4": "mx", "w4a8": "fp8"}.get(mode)  # requantised h
     T, k, I, H = cfg.T, cfg.k, cfg.I, cfg.H
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     x_np = x.float().cpu().numpy()
@@ -164,10 +180,10 @@ def check_layer(orc, cfg, mode, d, x, logits, gpu_w, tokens=None, seed=0, device
     assert np.array_equal(l13.index_select(0, idx).cpu().numpy()[..., : w13[1].shape[-1]], w13[1])
     assert np.array_equal(c2.index_select(0, idx).cpu().numpy(), w2[0])
     assert np.array_equal(l2.index_select(0, idx).cpu().numpy()[..., : w2[1].shape[-1]], w2[1])
-    S_x = orc.tensor_scale(x_np) if mode == "w4a4" else None
-    if mode == "w4a4":
+    S_x = {"w4a4": orc.tensor_scale, "w4a8": orc.fp8_tensor_scale}[mode](x_np) if mode in ("w4a4", "w4a8") else None
+    if S_x is not None:
         assert float(d["S_x"].item()) == float(S_x)
-    S_h = cfg.S_h if mode == "w4a4" else 0.0
+    S_h = {"w4a4": cfg.S_h, "w4a8": cfg.S_h8}.get(mode, 0.0)
     ref, mids = orc.moe_layer(mode, x_np[tokens], lg_np[tokens][:, used], k, w13, w2, S_h,
                               intermediates=True, S_x=S_x)
     # routing: the GPU's ids (global expert numbers) are the oracle's
@@ -179,18 +195,23 @@ def check_layer(orc, cfg, mode, d, x, logits, gpu_w, tokens=None, seed=0, device
     w_tok = mids["w"].reshape(len(tokens), k)
     figs = {"config": cfg.name, "mode": mode, "tokens": int(len(tokens))}
     flipped = {}
-    if mode in ("w4a4", "mxw4a4"):
+    if hfmt is not None:
         hc_g = d["hc"].cpu().numpy()
-        hs_g = d["hs"].cpu().numpy()
-        hs_g = hs_g[:, : (I // 16 if fmt == "nvfp4" else I // 32)]
         rows_g = inv_g[tokens].ravel()
         rows_o = inv_o.ravel()
         h32 = mids["h32"][rows_o]
-        d_o = np.concatenate([nvfp4_boundary_distance(h32[r:r + 256], S_h) if fmt == "nvfp4"
-                              else mx_boundary_distance(h32[r:r + 256]) for r in range(0, len(rows_o), 256)])
-        cg = unpack_codes(hc_g[rows_g])
-        co = unpack_codes(mids["hq_codes"][rows_o])
-        diff = (cg != co) | np.repeat(hs_g[rows_g] != mids["hq_scales"][rows_o], 16 if fmt == "nvfp4" else 32, 1)
+        dist_fn = {"nvfp4": lambda v: nvfp4_boundary_distance(v, S_h), "mx": mx_boundary_distance,
+                   "fp8": lambda v: fp8_boundary_distance(v, S_h)}[hfmt]
+        d_o = np.concatenate([dist_fn(h32[r:r + 256]) for r in range(0, len(rows_o), 256)])
+        if hfmt == "fp8":
+            hs_g = hs_o = None
+            diff = hc_g[rows_g] != mids["hq_codes"][rows_o]
+        else:
+            hs_g = d["hs"].cpu().numpy()[:, : (I // 16 if hfmt == "nvfp4" else I // 32)]
+            hs_o = mids["hq_scales"]
+            cg = unpack_codes(hc_g[rows_g])
+            co = unpack_codes(mids["hq_codes"][rows_o])
+            diff = (cg != co) | np.repeat(hs_g[rows_g] != hs_o[rows_o], 16 if hfmt == "nvfp4" else 32, 1)
         figs["h_elements"] = int(diff.size)
         figs["h_code_flips"] = int(diff.sum())
         figs["flip_max_boundary_distance"] = float(d_o[diff].max()) if diff.any() else 0.0
@@ -204,8 +225,8 @@ def check_layer(orc, cfg, mode, d, x, logits, gpu_w, tokens=None, seed=0, device
         q = np.quantile(relh[big], [0.5, 0.99, 0.9999, 1.0])
         figs["h_rel_diff_quantiles"] = {"p50": q[0], "p99": q[1], "p99.99": q[2], "max": q[3]}
         if diff.any():
-            dec_g = _decode_h(hc_g[rows_g], hs_g[rows_g], fmt, S_h)
-            dec_o = _decode_h(mids["hq_codes"][rows_o], mids["hq_scales"][rows_o], fmt, S_h)
+            dec_g = _decode_h(hc_g[rows_g], None if hs_g is None else hs_g[rows_g], hfmt, S_h)
+            dec_o = _decode_h(mids["hq_codes"][rows_o], None if hs_o is None else hs_o[rows_o], hfmt, S_h)
             dh = np.abs(dec_g - dec_o) * diff
             dh = dh.reshape(len(tokens), k, I)
             for i in np.nonzero(dh.reshape(len(tokens), -1).any(1))[0]:

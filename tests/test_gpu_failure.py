@@ -40,7 +40,7 @@ def _run(scenario, mode, drop):
     return res
 
 
-@pytest.mark.parametrize("mode", ["w4a4", "w4a16"])
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16", "w4a8"])
 def test_gemm_bounded_wait_times_out_and_context_survives(mode):
     _run("gemm", mode, 0)
 

@@ -155,7 +155,7 @@ def test_layer_graph_matches_one_call(orc, mode):
         assert int(graph.dev_status.item()) == 0
 
 
-@pytest.mark.parametrize("mode", ["w4a4", "w4a16", "mxw4a4"])
+@pytest.mark.parametrize("mode", ["w4a4", "w4a16", "mxw4a4", "w4a8"])
 @pytest.mark.parametrize("shape", [(16, 4096, 2048, 256, 8), (3, 256, 512, 7, 2), (40, 1024, 256, 64, 4)])
 def test_layer_host_entry_matches_device_entry(orc, mode, shape):
     """moe_layer_forward_host (inputs staged from pinned host memory by a
@@ -166,7 +166,7 @@ def test_layer_host_entry_matches_device_entry(orc, mode, shape):
     dev = cuda_or_skip()
     T, H, I, E, k = shape
     cfg = wl.MoEConfig("host_entry", T=T, H=H, I=I, E=E, k=k, routing="uniform")
-    m = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4}[mode]
+    m = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4, "w4a8": B.MOE_W4A8}[mode]
     if mode == "mxw4a4":
         from test_gpu_mx import gpu_mx_weights
         (g13, _), (g2, _) = gpu_mx_weights(cfg, dev)
