@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload decode_c16|decode_b512|wide|tiny|gemm_sweep]
-                    [--mode w4a4|w4a16|mxw4a4] [--router] [--sweep-ms M,...]
+                    [--mode w4a4|w4a16|mxw4a4|w4a8] [--router] [--sweep-ms M,...]
 
 Prints ONE JSON line (rank 0).  A step is one full MoE layer forward over the
 workload's batch -- route/permute + activation quantisation -> gate_up
@@ -21,9 +21,9 @@ flush is needed between steps.  --router times the router-logits GEMM and
 
 At N=1 the line also carries a `secondary` block: the same measurement
 (ms_per_step, tokens/s, gate_up fraction of the measured HBM bandwidth, layer
-fraction, clocks) for every other headline configuration -- decode_c16,
-decode_b512 and wide in W4A4, W4A16 and MXFP4 (decode_b512: W4A4 and MXFP4)
--- and the single-expert GEMM sweep (FP4 TFLOPS at M=512 and the other M).
+fraction, clocks) for every other headline configuration -- decode_c16 and
+wide in W4A4, W4A16, MXFP4 and W4A8, decode_b512 in W4A4 and MXFP4 -- and the
+single-expert GEMM sweep (FP4 TFLOPS at M=512 and the other M).
 --no-secondary skips it.
 
 --impl reference times the CPU oracle (the slow C restatement) on a bounded
@@ -141,7 +141,8 @@ def _kernel_hash(mode="w4a4"):
     the committed DRAM-traffic figure): its sources with comments and
     whitespace removed, so that only a change of code counts."""
     h = hashlib.sha256()
-    for fn in ("gemm_%s.cu" % ("w4a4" if mode == "mxw4a4" else mode), "common.cuh", "workitems.cuh"):
+    src = {"w4a4": "gemm_w4a4.cu", "mxw4a4": "gemm_w4a4.cu", "w4a16": "gemm_w4a16.cu", "w4a8": "gemm_w4a16.cu"}[mode]
+    for fn in (src, "common.cuh", "workitems.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", fn)) as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
@@ -216,11 +217,12 @@ def oracle_sample(cfg, mode, ntok, seed=0):
     q = orc.mx_quantize_experts if mode == "mxw4a4" else orc.quantize_experts
     w13 = q(np.stack([wl.expert_weight_fp32("w13", e, 2 * cfg.I, cfg.H, seed).numpy() for e in used]))
     w2 = q(np.stack([wl.expert_weight_fp32("w2", e, cfg.H, cfg.I, seed).numpy() for e in used]))
-    S_x = orc.tensor_scale(x) if mode == "w4a4" else None
+    S_x = {"w4a4": orc.tensor_scale, "w4a8": orc.fp8_tensor_scale}[mode](x) if mode in ("w4a4", "w4a8") else None
+    S_h = cfg.S_h8 if mode == "w4a8" else cfg.S_h
     xs, ls = x[toks], logits[toks][:, used]
 
     def run():
-        orc.moe_layer(mode, xs, ls, cfg.k, w13, w2, cfg.S_h, S_x=S_x)
+        orc.moe_layer(mode, xs, ls, cfg.k, w13, w2, S_h, S_x=S_x)
     return run
 
 
@@ -443,14 +445,14 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
     from nvfp4_mixture_experts_top_gb300 import workloads as wl
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    mode = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4}[mode_name]
+    mode = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16, "mxw4a4": B.MOE_MXW4A4, "w4a8": B.MOE_W4A8}[mode_name]
     mx = mode == B.MOE_MXW4A4
     bpe = MX_WEIGHT_BYTES_PER_ELEM if mx else WEIGHT_BYTES_PER_ELEM
 
     (w13, w2) = gpu_weights(cfg, dev, B, wl, mx=mx)
     x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
     logits = wl.router_logits(cfg, device=dev)
-    S_h = torch.tensor([cfg.S_h], dtype=torch.float32, device=dev)
+    S_h = torch.tensor([cfg.S_h8 if mode == B.MOE_W4A8 else cfg.S_h], dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     I, H, k, T, R = cfg.I, cfg.H, cfg.k, cfg.T, cfg.R
 
@@ -463,11 +465,11 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
     offs = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
     perm = torch.empty(R, dtype=torch.int32, device=dev)
     inv = torch.empty(R, dtype=torch.int32, device=dev)
-    a_c = torch.empty(R, H // 2, dtype=torch.uint8, device=dev)
+    a_c = torch.empty(R, H if mode == B.MOE_W4A8 else H // 2, dtype=torch.uint8, device=dev)
     a_s = torch.empty(R, B.mxfp4_scale_pitch(H) if mx else H // 16, dtype=torch.uint8, device=dev)
     a_b = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
     G = torch.empty(R, 2 * I, dtype=torch.float32, device=dev)
-    h_c = torch.empty(R, I // 2, dtype=torch.uint8, device=dev)
+    h_c = torch.empty(R, I if mode == B.MOE_W4A8 else I // 2, dtype=torch.uint8, device=dev)
     h_s = torch.empty(R, B.mxfp4_scale_pitch(I) if mx else I // 16, dtype=torch.uint8, device=dev)
     h_b = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
     Y = torch.empty(R, H, dtype=torch.float32, device=dev)
@@ -493,6 +495,19 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
                 ev_pair[1].record()
             chk(L.moe_swiglu_requant(P(G), R, I, 2, None, P(h_c), P(h_s), None, st))
             chk(L.moe_grouped_gemm_nvfp4(2, P(h_c), P(h_s), None, P(w2[0]), P(w2[1]), None, P(offs),
+                                         cfg.E, H, I, R, P(Y), P(status), st))
+        elif mode == B.MOE_W4A8:
+            # routing + FP8 quantisation straight into permuted rows
+            chk(L.moe_route_quantize_fp8(P(x), P(logits), T, H, cfg.E, k, P(ids), P(tw), P(offs), P(perm),
+                                         P(inv), P(S_x), P(a_c), P(status), P(ws_route), ws_route.numel(), st))
+            if ev_pair:
+                ev_pair[0].record()
+            chk(L.moe_grouped_gemm_nvfp4(3, P(a_c), None, P(S_x), P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
+                                         cfg.E, 2 * I, H, R, P(G), P(status), st))
+            if ev_pair:
+                ev_pair[1].record()
+            chk(L.moe_swiglu_requant(P(G), R, I, 3, P(S_h), P(h_c), None, None, st))
+            chk(L.moe_grouped_gemm_nvfp4(3, P(h_c), None, P(S_h), P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
                                          cfg.E, H, I, R, P(Y), P(status), st))
         elif mode == B.MOE_W4A4:
             # routing + activation quantisation straight into permuted rows
@@ -551,7 +566,7 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
     touched = int((counts > 0).sum())
     w13_bytes = touched * 2 * I * H * bpe
     w2_bytes = touched * H * I * bpe
-    act_in = R * H * (2.0 if mode == B.MOE_W4A16 else bpe)
+    act_in = R * H * {B.MOE_W4A16: 2.0, B.MOE_W4A8: 1.0}.get(mode, bpe)
     gemm1_bytes = w13_bytes + act_in + R * 2 * I * 4
     layer_weight_bytes = w13_bytes + w2_bytes
 
@@ -657,7 +672,8 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {B.MOE_W4A4: "fp4(e2m1)xfp4, fp32 accumulate", B.MOE_W4A16: "fp4(e2m1)xbf16, fp32 accumulate",
-                  B.MOE_MXW4A4: "fp4(e2m1)xfp4 (UE8M0 scales), fp32 accumulate"}[mode],
+                  B.MOE_MXW4A4: "fp4(e2m1)xfp4 (UE8M0 scales), fp32 accumulate",
+                  B.MOE_W4A8: "fp4(e2m1)xfp8(e4m3) on f16 operands, fp32 accumulate"}[mode],
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised on the GPU)",
         "config": {"workload": cfg.name, "mode": mode_name, "T": T, "hidden": H, "intermediate": I,
                    "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,
@@ -685,14 +701,17 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
 
 
 def layer_metric(cfg, mode_name):
-    return ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if mode_name == "mxw4a4"
-            else "MoE-layer tokens/s (NVFP4 %s, %s)" % (mode_name.upper(), cfg.name))
+    if mode_name == "mxw4a4":
+        return "MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name
+    if mode_name == "w4a8":
+        return "MoE-layer tokens/s (NVFP4 weights, FP8 activations, %s)" % cfg.name
+    return "MoE-layer tokens/s (NVFP4 %s, %s)" % (mode_name.upper(), cfg.name)
 
 
 # The headline configurations other than the one the line is quoted on; the
 # default run measures each of them too (secondary block of the line).
-SECONDARY = (("decode_c16", "w4a16"), ("decode_c16", "mxw4a4"), ("decode_b512", "w4a4"), ("decode_b512", "mxw4a4"),
-             ("wide", "w4a4"), ("wide", "w4a16"), ("wide", "mxw4a4"))
+SECONDARY = (("decode_c16", "w4a16"), ("decode_c16", "mxw4a4"), ("decode_c16", "w4a8"), ("decode_b512", "w4a4"),
+             ("decode_b512", "mxw4a4"), ("wide", "w4a4"), ("wide", "w4a16"), ("wide", "mxw4a4"), ("wide", "w4a8"))
 
 
 def secondary_entry(r):
@@ -711,7 +730,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_c16",
                     choices=["decode_c16", "decode_b512", "wide", "tiny", "gemm_sweep"])
-    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16", "mxw4a4"])
+    ap.add_argument("--mode", default="w4a4", choices=["w4a4", "w4a16", "mxw4a4", "w4a8"])
     ap.add_argument("--ref-tokens", type=int, default=1, help="tokens per reference-arm step")
     ap.add_argument("--baseline-tokens", type=int, default=16, help="tokens of the in-run CPU baseline sample")
     ap.add_argument("--baseline-seconds", type=float, default=10.0,
@@ -737,8 +756,7 @@ def main():
         cfg = wl.small_variant(cfg, E=args.experts, name=cfg.name + "_E%d" % args.experts)
     if args.router:
         return run_router(args, cfg, wl)
-    metric = ("MoE-layer tokens/s (MXFP4 W4A4, %s)" % cfg.name if args.mode == "mxw4a4"
-              else "MoE-layer tokens/s (NVFP4 %s, %s)" % (args.mode.upper(), cfg.name))
+    metric = layer_metric(cfg, args.mode)
     unit = "tokens/s"
     if args.impl == "reference":
         return run_reference(args, cfg, metric, unit)

@@ -14,9 +14,10 @@ Checks
 * every requantised h code (W4A4 NVFP4 with the static S_h; MXFP4 with its
   per-block shared exponent; W4A8 FP8 with its static scale): equal to the
   oracle's, except where the oracle's own fp32 h lies within FLIP_WINDOW
-  (relative) of that decision's rounding boundary -- G is accumulated in
-  fp32 on the tensor cores and in fp64 by the oracle, so h can differ in its
-  last bits;
+  (relative) of that decision's rounding boundary, or within the measured
+  difference between the GPU's pre-rounding h (from its fp32 G) and the
+  oracle's -- G is accumulated in fp32 on the tensor cores and in fp64 by
+  the oracle, so h can differ in its last bits;
 * the output as a whole: relative Frobenius error <= 1e-3;
 * every token without an h-code difference: relative Frobenius error <= 1e-3
   and max error <= 1e-2 x that token's output RMS;
@@ -42,9 +43,12 @@ from nvfp4_mixture_experts_top_gb300 import workloads as wl
 # Where a requantised h code may differ: the oracle's fp32 h lies within
 # this relative distance of the decision's rounding boundary.  Measured on
 # GB300 over every token of decode_c16, wide and decode_b512 (NVFP4 and
-# MXFP4): |h_gpu - h_oracle| / |h| from the GPU's fp32 G is at most 5.4e-7,
-# and the largest boundary distance any differing code needed was 2.7e-7, so
-# 1e-5 leaves an 18x margin.
+# MXFP4 requantisation): |h_gpu - h_oracle| / |h| from the GPU's fp32 G is at
+# most 5.4e-7, and the largest boundary distance any differing code needed was
+# 2.7e-7, so 1e-5 leaves an 18x margin.  The W4A8 mode's G comes from F16
+# MMAs whose accumulation differs more from fp64 (p99 5e-6 relative in h),
+# so there a code may also differ where the measured pre-rounding difference
+# of that element reaches the boundary.
 FLIP_WINDOW = 1e-5
 
 # E4M3 decode table from torch's own float8 type (independent of both sides)
@@ -212,18 +216,25 @@ def check_layer(orc, cfg, mode, d, x, logits, gpu_w, tokens=None, seed=0, device
             cg = unpack_codes(hc_g[rows_g])
             co = unpack_codes(mids["hq_codes"][rows_o])
             diff = (cg != co) | np.repeat(hs_g[rows_g] != hs_o[rows_o], 16 if hfmt == "nvfp4" else 32, 1)
-        figs["h_elements"] = int(diff.size)
-        figs["h_code_flips"] = int(diff.sum())
-        figs["flip_max_boundary_distance"] = float(d_o[diff].max()) if diff.any() else 0.0
-        assert not (diff & (d_o > FLIP_WINDOW)).any(), \
-            "h code differs where the oracle's h is %.3e (relative) from a boundary" % d_o[diff & (d_o > FLIP_WINDOW)].max()
-        # pre-rounding difference of h, from the GPU's own fp32 G
+        # pre-rounding difference of h, from the GPU's own fp32 G (the host's
+        # fp32 SwiGLU of it; the GPU's own expf may differ by an ulp or two)
         h_g = _silu_mul_f32(d["G"].cpu().numpy()[rows_g], I).astype(np.float64)
         h_o = mids["h32"][rows_o].astype(np.float64)
         relh = np.abs(h_g - h_o) / np.maximum(np.abs(h_o), 1e-30)
         big = np.abs(h_o) > 1e-6 * np.abs(h_o).max()
         q = np.quantile(relh[big], [0.5, 0.99, 0.9999, 1.0])
         figs["h_rel_diff_quantiles"] = {"p50": q[0], "p99": q[1], "p99.99": q[2], "max": q[3]}
+        figs["h_elements"] = int(diff.size)
+        figs["h_code_flips"] = int(diff.sum())
+        figs["flip_max_boundary_distance"] = float(d_o[diff].max()) if diff.any() else 0.0
+        # a code may differ where the oracle's h lies within FLIP_WINDOW of the
+        # boundary, or within the measured pre-rounding difference at that
+        # element (which the boundary then lies between, up to ulp slack)
+        legit = (d_o <= FLIP_WINDOW) | (d_o <= 2.0 * relh + 1e-6)
+        figs["flips_beyond_window"] = int((diff & (d_o > FLIP_WINDOW)).sum())
+        assert not (diff & ~legit).any(), \
+            "h code differs where the oracle's h is %.3e (relative) from a boundary and the GPU's pre-rounding h " \
+            "only %.3e away" % (d_o[diff & ~legit].max(), relh[diff & ~legit].max())
         if diff.any():
             dec_g = _decode_h(hc_g[rows_g], None if hs_g is None else hs_g[rows_g], hfmt, S_h)
             dec_o = _decode_h(mids["hq_codes"][rows_o], None if hs_o is None else hs_o[rows_o], hfmt, S_h)
