@@ -367,10 +367,13 @@ def run_gemm_sweep(args, wl):
 
 
 def run_router(args, cfg, wl):
-    """Router logits (moe_router_logits) for the workload's T, H, E: a CUDA
-    graph of back-to-back calls rotating over copies of x and W_router whose
-    total exceeds twice the L2, so every call reads its operands from HBM.
-    value = tokens/s of the router step alone."""
+    """Router for the workload's T, H, E, k: graphs of back-to-back calls
+    rotating over copies of x and W_router whose total exceeds twice the L2,
+    so every call reads its operands from HBM.  Three forms are timed:
+    moe_router_logits alone; moe_router_logits + moe_align_permute (the
+    staged router and routing); moe_router_route (router and routing in one
+    call: the router GEMM and, for T <= 32, one fused reduce/top-k/permute
+    kernel).  value = tokens/s of moe_router_route."""
     import torch
 
     from nvfp4_mixture_experts_top_gb300 import binding as B
@@ -379,7 +382,8 @@ def run_router(args, cfg, wl):
     L = B.load()
     B.nvfp4_device_check()
     hbm, _, peak_kind = _load_peaks()
-    T, H, E = cfg.T, cfg.H, cfg.E
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    R = T * k
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_copy = E * H * 2 + T * H * 2 + T * E * 4
     copies = int(max(2, np.ceil(2 * l2 / per_copy)))
@@ -389,48 +393,75 @@ def run_router(args, cfg, wl):
     Ws = [w.clone() for _ in range(copies)]
     outs = [torch.empty(T, E, device=dev) for _ in range(copies)]
     ws = torch.empty(int(L.moe_router_logits_workspace_bytes(T, H, E)), dtype=torch.uint8, device=dev)
+    ws_rr = torch.empty(int(L.moe_router_route_workspace_bytes(T, H, E, k)), dtype=torch.uint8, device=dev)
+    ws_rt = torch.empty(max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256), dtype=torch.uint8, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    inv = torch.empty(R, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    P = lambda t: None if t is None else t.data_ptr()  # noqa: E731
 
-    def launch(i):
-        r = L.moe_router_logits(Xs[i].data_ptr(), Ws[i].data_ptr(), T, H, E, outs[i].data_ptr(), status.data_ptr(),
-                                ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    def chk(name, r):
         if r != 0:
-            raise B.Nvfp4Error("moe_router_logits", r)
+            raise B.Nvfp4Error(name, r)
 
-    for i in range(args.warmup):
-        launch(i % copies)
-    reps = max(args.steps, copies)
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g, stream=side):
-            for i in range(reps):
-                launch(i % copies)
-    torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError("device status %d" % int(status.item()))
-    us = e0.elapsed_time(e1) * 1e3 / reps
-    gbs = per_copy / (us * 1e-6) / 1e9
+    def logits_only(i):
+        chk("moe_router_logits", L.moe_router_logits(P(Xs[i]), P(Ws[i]), T, H, E, P(outs[i]), P(status), P(ws),
+                                                      ws.numel(), torch.cuda.current_stream().cuda_stream))
+
+    def staged(i):
+        logits_only(i)
+        chk("moe_align_permute", L.moe_align_permute(P(outs[i]), T, E, k, P(ids), P(tw), P(offs), P(perm), P(inv), 0,
+                                                      None, None, 0, None, None, P(status), P(ws_rt), ws_rt.numel(),
+                                                      torch.cuda.current_stream().cuda_stream))
+
+    def fused(i):
+        chk("moe_router_route", L.moe_router_route(P(Xs[i]), P(Ws[i]), T, H, E, k, P(outs[i]), P(ids), P(tw),
+                                                    P(offs), P(perm), P(inv), P(status), P(ws_rr), ws_rr.numel(),
+                                                    torch.cuda.current_stream().cuda_stream))
+
+    def time_graph(fn):
+        for i in range(args.warmup):
+            fn(i % copies)
+        reps = max(args.steps, copies)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(reps):
+                    fn(i % copies)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError("device status %d" % int(status.item()))
+        return e0.elapsed_time(e1) * 1e3 / reps, reps
+
+    us_logits, _ = time_graph(logits_only)
+    us_staged, _ = time_graph(staged)
+    us, reps = time_graph(fused)
+    gbs = per_copy / (us_logits * 1e-6) / 1e9
     splits = int(L.moe_router_logits_workspace_bytes(T, H, E)) // max(1, T * E * 4)
-    result = {"metric": "router-logits tokens/s (%s: T=%d, H=%d, E=%d)" % (cfg.name, T, H, E),
+    fused_kernels = 2 if T <= 32 else (3 if splits > 1 else 2)
+    result = {"metric": "router + routing tokens/s (%s: T=%d, H=%d, E=%d, top-%d)" % (cfg.name, T, H, E, k),
               "value": T / (us * 1e-6), "unit": "tokens/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
               "ms_per_step": us / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
               "dtype": "bf16xbf16, fp32 accumulate", "data": "synthetic",
-              "config": {"workload": cfg.name + "_router", "T": T, "hidden": H, "experts": E,
-                         "k_splits": max(1, splits),
-                         "l2": "rotating %d operand copies > 2x L2" % copies},
-              "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                           "peak_kind": peak_kind, "algorithmic_bytes_per_launch": per_copy, "avg_launch_us": us,
-                           "traffic": None},
-              "gpu_launches": reps * (2 if splits > 1 else 1)}
+              "config": {"workload": cfg.name + "_router", "T": T, "hidden": H, "experts": E, "top_k": k,
+                         "k_splits": max(1, splits), "l2": "rotating %d operand copies > 2x L2" % copies},
+              "router_logits_us": us_logits, "router_then_align_permute_us": us_staged, "router_route_us": us,
+              "roofline": {"kernel": "router logits GEMM (+ reduce)", "bound": "hbm", "achieved": gbs, "peak": hbm,
+                           "unit": "GB/s", "frac": gbs / hbm, "peak_kind": peak_kind,
+                           "algorithmic_bytes_per_launch": per_copy, "avg_launch_us": us_logits, "traffic": None},
+              "gpu_launches": reps * fused_kernels}
     print(json.dumps(result), flush=True)
 
 

@@ -196,6 +196,30 @@ int moe_router_logits(const void* x, const void* w_router, int T, int H, int E, 
                       int32_t* dev_status, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_router_route -- the router and the routing in one call: router logits
+ * (as moe_router_logits), then top-k, softmax and the expert permutation (as
+ * moe_align_permute) ("The 2x Gap", section "The Investigation So Far": each
+ * token goes to 8 of 256 experts by these scores).  For a decode batch
+ * (T <= 32) it is two kernels: the router GEMM, then one kernel that sums the
+ * GEMM's K-range partials in a fixed order, selects the top k of each token
+ * and builds the permutation; larger T runs the router GEMM, its reduce and
+ * the routing kernel.  Either way the results are bitwise those of
+ * moe_router_logits followed by moe_align_permute.
+ *   x bf16 [T, H]; w_router bf16 [E, H]
+ *   logits  optional out fp32 [T, E] (NULL: not returned)
+ *   topk_ids, topk_w, expert_offsets, perm, inv: as moe_align_permute
+ *   workspace >= moe_router_route_workspace_bytes(T, H, E, k) (for the
+ *   current device)
+ *   dev_status: optional; NVFP4_E_DEVICE_TIMEOUT from the router GEMM's
+ *   bounded waits, NVFP4_E_BAD_ROUTING from the routing.
+ * Constraints: H % 64 == 0, 1 <= k <= min(E, 32), E <= 1024.
+ * ------------------------------------------------------------------------ */
+size_t moe_router_route_workspace_bytes(int T, int H, int E, int k);
+int moe_router_route(const void* x, const void* w_router, int T, int H, int E, int k, float* logits,
+                     int32_t* topk_ids, float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv,
+                     int32_t* dev_status, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_align_permute -- router top-k plus the expert permutation.
  * Routing: "The 2x Gap", section "The Investigation So Far" (top-8 of 256
  * experts); "Native FP4 Is Slower ...", section 1 (22 of 512).  Per token t:

@@ -29,7 +29,8 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspac
            "moe_layer_forward", "moe_align_permute_noalloc", "moe_route_quantize_nvfp4", "mxfp4_scale_pitch",
            "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4",
            "moe_router_logits_workspace_bytes", "moe_router_logits", "moe_layer_host_workspace_bytes",
-           "moe_layer_forward_host", "fp8_quantize", "moe_route_quantize_fp8")
+           "moe_layer_forward_host", "fp8_quantize", "moe_route_quantize_fp8", "moe_router_route_workspace_bytes",
+           "moe_router_route")
 
 
 class Nvfp4Error(RuntimeError):
@@ -103,6 +104,10 @@ def load(build_if_missing: bool = True):
     L.mxfp4_pack_weight_scales.argtypes = [_P, _I, _I, _I, _P, _P]
     L.moe_route_quantize_mxfp4.restype = _I
     L.moe_route_quantize_mxfp4.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_router_route_workspace_bytes.restype = _SZ
+    L.moe_router_route_workspace_bytes.argtypes = [_I, _I, _I, _I]
+    L.moe_router_route.restype = _I
+    L.moe_router_route.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.fp8_quantize.restype = _I
     L.fp8_quantize.argtypes = [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _SZ, _P]
     L.moe_route_quantize_fp8.restype = _I
@@ -223,6 +228,29 @@ def moe_router_logits(x, w_router, out=None, workspace=None, dev_status=None):
         workspace = _empty(int(L.moe_router_logits_workspace_bytes(T, H, E)), torch.uint8, x.device)
     _check("moe_router_logits", L.moe_router_logits(_ptr(x), _ptr(w_router), T, H, E, _ptr(out), _ptr(dev_status),
                                                     _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def moe_router_route(x, w_router, k, want_logits=True, dev_status=None, workspace=None):
+    """Router logits + top-k + permutation of x [T, H] bf16 with w_router
+    [E, H] bf16.  Returns dict(ids, w, offsets, perm, inv[, logits])."""
+    L = load()
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    R = T * k
+    out = dict(ids=_empty((T, k), torch.int32, dev), w=_empty((T, k), torch.float32, dev),
+               offsets=_empty((E + 1,), torch.int32, dev), perm=_empty((max(R, 1),), torch.int32, dev),
+               inv=_empty((max(R, 1),), torch.int32, dev))
+    if want_logits:
+        out["logits"] = _empty((T, E), torch.float32, dev)
+    if workspace is None:
+        workspace = _empty(max(int(L.moe_router_route_workspace_bytes(T, H, E, k)), 256), torch.uint8, dev)
+    _check("moe_router_route",
+           L.moe_router_route(_ptr(x), _ptr(w_router), T, H, E, k, _ptr(out.get("logits")), _ptr(out["ids"]),
+                              _ptr(out["w"]), _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv"]),
+                              _ptr(dev_status), _ptr(workspace), workspace.numel(), _stream()))
+    out["perm"], out["inv"] = out["perm"][:R], out["inv"][:R]
     return out
 
 

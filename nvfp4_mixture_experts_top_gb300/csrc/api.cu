@@ -208,6 +208,35 @@ int moe_router_logits(const void* x, const void* w_router, int T, int H, int E, 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_router_route_workspace_bytes(int T, int H, int E, int k) {
+  (void)k;
+  if (T < 0 || H < 0 || E < 0) return 0;
+  return router_route_workspace_bytes(T, H, E);
+}
+
+int moe_router_route(const void* x, const void* w_router, int T, int H, int E, int k, float* logits,
+                     int32_t* topk_ids, float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv,
+                     int32_t* dev_status, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
+  if (H % 64 != 0 || k > E || k > 32 || E > 1024) return NVFP4_E_SHAPE;
+  if (expert_offsets == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(expert_offsets)) return NVFP4_E_ALIGN;
+  if (T > 0) {
+    if (x == nullptr || w_router == nullptr || topk_ids == nullptr || topk_w == nullptr || perm == nullptr ||
+        inv == nullptr)
+      return NVFP4_E_INVAL;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(perm) ||
+        !aligned16(inv) || (logits != nullptr && !aligned16(logits)))
+      return NVFP4_E_ALIGN;
+    if (workspace == nullptr || workspace_bytes < moe_router_route_workspace_bytes(T, H, E, k))
+      return NVFP4_E_WORKSPACE;
+    if (!aligned16(workspace)) return NVFP4_E_ALIGN;
+  }
+  CHECK_ARCH();
+  return cuda_status(launch_router_route(x, w_router, T, H, E, k, logits, topk_ids, topk_w, expert_offsets, perm,
+                                         inv, dev_status, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_align_permute_workspace_bytes(int T, int E, int k) {
   (void)k;
   if (T < 0 || E < 0) return 0;

@@ -112,6 +112,14 @@ cudaError_t launch_fp8_quantize_scatter(const void* x_bf16, int T, int H, int k,
 size_t router_workspace_bytes(int T, int H, int E);
 cudaError_t launch_router_logits(const void* x_bf16, const void* w_bf16, int T, int H, int E, float* logits,
                                  void* workspace, int32_t* dev_status, cudaStream_t st);
+// Router logits + top-k + permutation: for T <= 32 two launches (the router
+// GEMM, then one fused kernel: fixed-order partial sums, top-k, stable
+// permutation); otherwise the router GEMM, its reduce and the routing kernel.
+// logits may be NULL (not returned).
+size_t router_route_workspace_bytes(int T, int H, int E);
+cudaError_t launch_router_route(const void* x_bf16, const void* w_bf16, int T, int H, int E, int k, float* logits,
+                                int32_t* ids, float* w, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                int32_t* dev_status, void* workspace, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // MXFP4 (32-element blocks, UE8M0 scales)

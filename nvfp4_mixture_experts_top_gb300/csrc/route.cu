@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace nvfp4moe {
 
@@ -32,53 +33,6 @@ constexpr int kChunk = 32;
 size_t route_workspace_bytes(int T, int E) {
   const size_t C = (size_t)(T + kChunk - 1) / kChunk;
   return 256 + ((C * (size_t)E * 4 + 255) & ~(size_t)255);
-}
-
-template <int NPER>
-__device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, int k, int lane, int& my_id,
-                                          float& my_w) {
-  float v[NPER];
-#pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldg(l + e) : 0.0f;
-  }
-  uint32_t taken = 0;
-  my_id = 0;
-  float my_v = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    // local best among untaken entries (ascending id, strict > keeps the lower id on ties)
-    float bv = 0.0f;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < NPER; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (bi == 0x7FFFFFFF || v[i] > bv)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (oi != 0x7FFFFFFF && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_id = bi;
-      my_v = bv;
-    }
-  }
-  const float lmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-  const float ex = (lane < k) ? expf(__fsub_rn(my_v, lmax)) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
-  my_w = __fdiv_rn(ex, sum);
 }
 
 template <int NPER>

@@ -78,3 +78,46 @@ def test_router_logits_rejects_bad_shapes():
     w = torch.zeros(8, 100, dtype=torch.bfloat16, device=dev)
     with pytest.raises(B.Nvfp4Error):
         B.moe_router_logits(x, w)  # H % 64 != 0
+
+
+ROUTE_SHAPES = [  # (T, H, E, k)
+    (16, 4096, 256, 8),   # decode C=16: the fused router kernel
+    (1, 1024, 64, 4),     # one token
+    (32, 2048, 512, 22),  # a full routing chunk, wide-expert top-k
+    (7, 256, 1024, 32),   # the largest E and k the call accepts
+    (33, 1024, 256, 8),   # two chunks: router GEMM + reduce + routing kernel
+    (64, 4096, 512, 22),  # wide
+]
+
+
+@pytest.mark.parametrize("T,H,E,k", ROUTE_SHAPES)
+def test_router_route_fused_matches_staged_and_oracle(orc, T, H, E, k):
+    """moe_router_route (router GEMM + fused fixed-order reduce, top-k and
+    permutation at T <= 32) is bitwise moe_router_logits followed by
+    moe_align_permute, twice in a row (the completion counter resets itself),
+    and its routing of its own logits is the oracle's bit for bit."""
+    dev = cuda_or_skip()
+    x, w = _inputs(T, H, E, seed=3 * T + E)
+    x, w = x.to(dev), w.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    first = B.moe_router_route(x, w, k, dev_status=status)
+    got = B.moe_router_route(x, w, k, dev_status=status)
+    lg = B.moe_router_logits(x, w)
+    rt = B.moe_align_permute(lg, k)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for key in ("ids", "w", "offsets", "perm", "inv"):
+        assert torch.equal(got[key], first[key]), key
+        assert torch.equal(got[key], rt[key]), key
+    assert torch.equal(got["logits"], lg)
+    ids, wts = orc.route(got["logits"].cpu().numpy(), k)
+    offs, perm, inv = orc.permute(ids, E)
+    assert np.array_equal(got["ids"].cpu().numpy(), ids)
+    assert np.array_equal(got["offsets"].cpu().numpy(), offs)
+    assert np.array_equal(got["perm"].cpu().numpy(), perm)
+    assert np.array_equal(got["inv"].cpu().numpy(), inv)
+    assert np.allclose(got["w"].cpu().numpy(), wts, rtol=0, atol=1e-6)
+    # without the logits output the routing is the same
+    nolog = B.moe_router_route(x, w, k, want_logits=False)
+    torch.cuda.synchronize()
+    assert torch.equal(nolog["perm"], got["perm"]) and torch.equal(nolog["w"], got["w"])
