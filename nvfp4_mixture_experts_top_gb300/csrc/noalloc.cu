@@ -13,9 +13,9 @@
 // loads it, and is shared by every call on that GPU: two calls that overlap on
 // the GPU (different streams, no ordering between them) race on it and give
 // undefined results.  Every scratch word is written before it is read within
-// one call (the completion counter is cleared by the call itself, the
-// per-chunk expert masks are rebuilt from the logits each time), so the
-// caller never has to clear anything between calls.
+// one call (the per-chunk expert masks and activation maxima are rebuilt from
+// the inputs each time), so the caller never has to clear anything between
+// calls.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
@@ -28,8 +28,8 @@
 namespace nvfp4moe {
 namespace {
 
-// Fixed scratch: a 256-byte header (completion counter) and, per 32-token
-// chunk and expert, one 32-bit token mask.
+// Fixed scratch: a 256-byte header, then per 32-token chunk and expert one
+// 32-bit token mask, then per chunk one activation maximum.
 __device__ __align__(256) static uint8_t g_route_scratch[NVFP4MOE_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_route_scratch, per device, for the CUDA context it was

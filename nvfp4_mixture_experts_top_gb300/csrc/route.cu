@@ -1,5 +1,5 @@
-// route.cu -- router top-k and the stable expert permutation (counting sort)
-// in one launch, plus the gather of activation rows into permuted order.
+// route.cu -- router top-k and the stable expert permutation (counting sort),
+// plus the gather of activation rows into permuted order.
 //
 // route_kernel: one CTA per chunk of 32 tokens, one warp per token.
 //  1. top-k: the token's logits sit in registers (E/32 per lane, a
@@ -8,15 +8,16 @@
 //     are an fp32 softmax over the k selected logits.
 //  2. the chunk records, per expert, a 32-bit mask of its tokens that chose
 //     that expert (shared-memory atomicOr; the mask is order-independent).
-//  3. the last CTA to finish (device-scope counter) computes the per-expert
-//     counts (popcounts of all chunks' masks), an exclusive block scan ->
-//     expert_offsets, and then places every (token, slot) pair:
+//  3. placement: per-expert counts (popcounts of all chunks' masks), an
+//     exclusive block scan -> expert_offsets, and every (token, slot) pair at
 //       row = offsets[e] + (rows of expert e in earlier chunks)
 //                        + popcount(mask bits of earlier tokens in the chunk)
-//     which is stable by (expert, token) by construction; then it resets the
-//     counter.  With a single chunk (T <= 32, decode) the one CTA does this
-//     straight from shared memory, without the round trips through global
-//     memory and the counter.
+//     which is stable by (expert, token) by construction.
+//     With a single chunk (T <= 32, decode) the one CTA does this straight
+//     from shared memory.  With several chunks each CTA stores its chunk's
+//     masks (and activation amax) and route_place_kernel -- the next launch,
+//     a programmatic dependent -- does the placement: no completion counter,
+//     so nothing in the scratch has to be zeroed (no memset node).
 // gather_kernel: one warp per permuted row, 16-byte vector copies.
 #include <math.h>
 
@@ -28,33 +29,98 @@ namespace nvfp4moe {
 
 constexpr int kMaxE = 1024;
 constexpr int kChunk = 32;
+// dynamic shared memory of the parallel placement: masks and prefixes of up
+// to 24K (chunk, expert) cells (e.g. 3072 tokens at 256 experts)
+constexpr size_t kPlaceSmemMax = 192 * 1024;
 
-// Scratch layout: [0, 256) chunk counter and activation amax; then masks [C][E] u32.
+// Scratch layout: [0, 256) the activation amax in word 1; then masks [C][E]
+// u32; then per-chunk activation amax [C] u32.
 size_t route_workspace_bytes(int T, int E) {
   const size_t C = (size_t)(T + kChunk - 1) / kChunk;
-  return 256 + ((C * (size_t)E * 4 + 255) & ~(size_t)255);
+  return 256 + ((C * (size_t)E * 4 + 255) & ~(size_t)255) + ((C * 4 + 255) & ~(size_t)255);
+}
+
+// Counts, exclusive scan -> offsets, and the stable placement of every
+// (token, slot) pair of C chunks (all threads of a 1024-thread CTA, thread e
+// = expert e).  single: one chunk whose ids and masks are in shared memory;
+// otherwise they are read from global memory (ids [T, k], masks [C][E]).
+__device__ __forceinline__ void route_place(int T, int E, int k, int C, bool single, const int32_t* s_ids,
+                                            const uint32_t* s_mask, const int32_t* ids, const uint32_t* masks,
+                                            int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dev_status,
+                                            int32_t* base, int32_t* warp_tot) {
+  const int e = threadIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int cnt = 0;
+  if (e < E) {
+    if (single) cnt = __popc(s_mask[e]);
+    else
+      for (int cc = 0; cc < C; ++cc) cnt += __popc(__ldcg(masks + (int64_t)cc * E + e));
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int sum = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, sum, o);
+      if (lane >= o) sum += y;
+    }
+    warp_tot[lane] = sum;
+  }
+  __syncthreads();
+  const int excl = incl - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
+  if (e < E) {
+    offsets[e] = excl;
+    base[e] = excl;
+    if (e == E - 1) {
+      offsets[E] = excl + cnt;
+      if (excl + cnt != T * k) report_status(dev_status, NVFP4_E_BAD_ROUTING);
+    }
+  }
+  __syncthreads();
+  // chunks in order: pairs of chunk cc go after the rows of earlier chunks
+  for (int cc = 0; cc < C; ++cc) {
+    for (int pidx = threadIdx.x; pidx < kChunk * k; pidx += blockDim.x) {
+      const int tl = pidx / k, j = pidx % k;
+      const int tt = cc * kChunk + tl;
+      if (tt < T) {
+        const int ee = single ? s_ids[tl * k + j] : __ldcg(ids + (int64_t)tt * k + j);
+        const uint32_t m = single ? s_mask[ee] : __ldcg(masks + (int64_t)cc * E + ee);
+        const int row = base[ee] + __popc(m & ((1u << tl) - 1u));
+        perm[row] = tt;
+        inv[(int64_t)tt * k + j] = row;
+      }
+    }
+    __syncthreads();
+    if (e < E && !single) base[e] += __popc(__ldcg(masks + (int64_t)cc * E + e));
+    __syncthreads();
+  }
 }
 
 template <int NPER>
 __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                      int32_t* __restrict__ ids, float* __restrict__ w,
                                                      int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-                                                     int32_t* __restrict__ inv, uint32_t* __restrict__ counter,
-                                                     uint32_t* __restrict__ masks, int32_t* dev_status,
+                                                     int32_t* __restrict__ inv, uint32_t* __restrict__ masks,
+                                                     uint32_t* __restrict__ amax_part, int32_t* dev_status,
                                                      const __nv_bfloat16* __restrict__ x, int64_t H,
                                                      uint32_t* __restrict__ amax_bits) {
   __shared__ uint32_t mask[kMaxE];
   __shared__ int32_t base[kMaxE];
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t s_ids[kChunk * 32];  // this chunk's expert ids (k <= 32)
-  __shared__ bool last;
   __shared__ uint32_t s_amax;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const int C = gridDim.x;
   // a single chunk (T <= 32, the decode case) keeps everything in shared
-  // memory: no mask round trip through global memory, no counter, and the
-  // activation amax is stored, not accumulated into a zeroed word
+  // memory: no mask round trip through global memory, and the placement
+  // follows in this launch
   const bool single = (C == 1);
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0;
   if (threadIdx.x == 0) s_amax = 0;
@@ -85,7 +151,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) atomicMax(single ? &s_amax : amax_bits, __float_as_uint(m));
+    if (lane == 0) atomicMax(&s_amax, __float_as_uint(m));
   }
   if (t < T) {
     int my_id;
@@ -99,26 +165,68 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     }
   }
   __syncthreads();
-  if (single && x != nullptr && threadIdx.x == 0) *amax_bits = s_amax;
   if (!single) {
+    // several chunks: store this chunk's masks and amax; the placement is
+    // route_place_kernel's (the next launch)
     for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = mask[e];
-
-    // 3: the last chunk to finish does the scan and the scatter
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = (atomicAdd(counter, 1u) == (uint32_t)(C - 1));
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
+    if (x != nullptr && threadIdx.x == 0) amax_part[c] = s_amax;
+    return;
   }
+  if (x != nullptr && threadIdx.x == 0) *amax_bits = s_amax;
+  route_place(T, E, k, 1, true, s_ids, mask, ids, masks, offsets, perm, inv, dev_status, base, warp_tot);
+}
 
-  const int e = threadIdx.x;
+// The placement of a routing over several chunks (one CTA of 1024 threads,
+// launched as a programmatic dependent of route_kernel): the activation amax
+// over the chunks' partials (when x was given), then
+//  A. every chunk's masks into shared memory (many loads in flight), and per
+//     expert e (thread e) its count and, for every chunk, the rows of e in
+//     earlier chunks: pre[c][e];
+//  B. offsets by a block scan of the counts;
+//  C. every (token, slot) pair placed independently:
+//       row = offsets[e] + pre[c][e] + popcount(mask[c][e] bits below t)
+// The chunks' masks and prefixes take 2 * C * E * 4 bytes of shared memory
+// (dynamic; the launcher checks the size).  Walking the chunks in order with
+// the masks in global memory instead took two dependent L2 round trips per
+// chunk (~25 us at 16 chunks).
+__global__ void __launch_bounds__(1024) route_place_kernel(int T, int E, int k, const int32_t* __restrict__ ids,
+                                                           const uint32_t* __restrict__ masks,
+                                                           const uint32_t* __restrict__ amax_part,
+                                                           uint32_t* __restrict__ amax_bits,
+                                                           int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                                           int32_t* __restrict__ inv, int32_t* dev_status) {
+  extern __shared__ uint32_t sm[];  // [C][E] masks, then [C][E] rows of earlier chunks
+  __shared__ int32_t base[kMaxE];
+  __shared__ int32_t warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
+  const int C = (T + kChunk - 1) / kChunk;
+  const int e = threadIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* s_mask = sm;
+  uint32_t* s_pre = sm + C * E;
+  if (amax_bits != nullptr && threadIdx.x < 32) {
+    uint32_t m = 0;
+    for (int c = threadIdx.x; c < C; c += 32) m = max(m, __ldcg(amax_part + c));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (threadIdx.x == 0) *amax_bits = m;
+  }
+  const int n = C * E;
+  for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+    uint32_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (i0 + j * (int)blockDim.x < n) ? __ldcg(masks + i0 + j * blockDim.x) : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (i0 + j * (int)blockDim.x < n) s_mask[i0 + j * blockDim.x] = v[j];
+  }
+  __syncthreads();
   int cnt = 0;
-  if (e < E) {
-    if (single) cnt = __popc(mask[e]);
-    else
-      for (int cc = 0; cc < C; ++cc) cnt += __popc(__ldcg(masks + (int64_t)cc * E + e));
-  }
+  if (e < E)
+    for (int c = 0; c < C; ++c) {
+      s_pre[c * E + e] = (uint32_t)cnt;
+      cnt += __popc(s_mask[c * E + e]);
+    }
   int incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -128,13 +236,13 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int s = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+    int sum = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, s, o);
-      if (lane >= o) s += y;
+      const int y = __shfl_up_sync(0xFFFFFFFFu, sum, o);
+      if (lane >= o) sum += y;
     }
-    warp_tot[lane] = s;
+    warp_tot[lane] = sum;
   }
   __syncthreads();
   const int excl = incl - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
@@ -147,24 +255,48 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     }
   }
   __syncthreads();
-  // chunks in order: pairs of chunk cc go after the rows of earlier chunks
-  for (int cc = 0; cc < C; ++cc) {
-    for (int pidx = threadIdx.x; pidx < kChunk * k; pidx += blockDim.x) {
-      const int tl = pidx / k, j = pidx % k;
-      const int tt = cc * kChunk + tl;
-      if (tt < T) {
-        const int ee = single ? s_ids[tl * k + j] : __ldcg(ids + (int64_t)tt * k + j);
-        const uint32_t m = single ? mask[ee] : __ldcg(masks + (int64_t)cc * E + ee);
-        const int row = base[ee] + __popc(m & ((1u << tl) - 1u));
-        perm[row] = tt;
-        inv[(int64_t)tt * k + j] = row;
+  const int np = T * k;
+  for (int i0 = threadIdx.x; i0 < np; i0 += 8 * blockDim.x) {
+    int ee[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ee[j] = (i0 + j * (int)blockDim.x < np) ? __ldcg(ids + i0 + j * blockDim.x) : 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * blockDim.x;
+      if (i < np) {
+        const int t = i / k, c = t / kChunk, tl = t % kChunk;
+        const int x = c * E + ee[j];
+        const int row = base[ee[j]] + (int)s_pre[x] + __popc(s_mask[x] & ((1u << tl) - 1u));
+        perm[row] = t;
+        inv[i] = row;
       }
     }
-    __syncthreads();
-    if (e < E && !single) base[e] += __popc(__ldcg(masks + (int64_t)cc * E + e));
-    __syncthreads();
   }
-  if (threadIdx.x == 0 && !single) *counter = 0;
+}
+
+// The same placement for routings whose masks do not fit in shared memory:
+// the chunks in order, masks and ids read from global memory.
+__global__ void __launch_bounds__(1024) route_place_serial_kernel(int T, int E, int k,
+                                                                  const int32_t* __restrict__ ids,
+                                                                  const uint32_t* __restrict__ masks,
+                                                                  const uint32_t* __restrict__ amax_part,
+                                                                  uint32_t* __restrict__ amax_bits,
+                                                                  int32_t* __restrict__ offsets,
+                                                                  int32_t* __restrict__ perm,
+                                                                  int32_t* __restrict__ inv, int32_t* dev_status) {
+  __shared__ int32_t base[kMaxE];
+  __shared__ int32_t warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
+  const int C = (T + kChunk - 1) / kChunk;
+  if (amax_bits != nullptr && threadIdx.x < 32) {
+    uint32_t m = 0;
+    for (int c = threadIdx.x; c < C; c += 32) m = max(m, __ldcg(amax_part + c));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (threadIdx.x == 0) *amax_bits = m;
+  }
+  route_place(T, E, k, C, false, nullptr, nullptr, ids, masks, offsets, perm, inv, dev_status, base, warp_tot);
 }
 
 // One warp per permuted row: copy `row_bytes` (and `sc_bytes` of scales).
@@ -194,24 +326,34 @@ cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t*
                               cudaStream_t st, const void* x_bf16, int64_t H) {
   if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st);
   const int C = (T + kChunk - 1) / kChunk;
-  uint32_t* counter = static_cast<uint32_t*>(ws);      // word 0: chunk counter, word 1: activation amax
+  uint32_t* amax = static_cast<uint32_t*>(ws) + 1;  // word 1: activation amax
   uint32_t* masks = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
-  if (C > 1) {
-    // several chunks meet through the counter and accumulate the amax
-    const cudaError_t e = cudaMemsetAsync(counter, 0, 2 * sizeof(uint32_t), st);
-    if (e != cudaSuccess) return e;
-  }
+  uint32_t* amax_part =
+      reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256 + (((size_t)C * E * 4 + 255) & ~(size_t)255));
   const int nper = (E + 31) / 32;
-#define NVFP4MOE_ROUTE(NP)                                                                                        \
-  return launch_pdl(route_kernel<NP>, C, 1024, 0, st, logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, counter, \
-                    masks, dev_status, static_cast<const __nv_bfloat16*>(x_bf16), (int64_t)H, counter + 1)
+  cudaError_t err;
+#define NVFP4MOE_ROUTE(NP)                                                                                       \
+  err = launch_pdl(route_kernel<NP>, C, 1024, 0, st, logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, masks, \
+                   amax_part, dev_status, static_cast<const __nv_bfloat16*>(x_bf16), (int64_t)H, amax)
   if (nper <= 1) NVFP4MOE_ROUTE(1);
-  if (nper <= 2) NVFP4MOE_ROUTE(2);
-  if (nper <= 4) NVFP4MOE_ROUTE(4);
-  if (nper <= 8) NVFP4MOE_ROUTE(8);
-  if (nper <= 16) NVFP4MOE_ROUTE(16);
-  NVFP4MOE_ROUTE(32);
+  else if (nper <= 2) NVFP4MOE_ROUTE(2);
+  else if (nper <= 4) NVFP4MOE_ROUTE(4);
+  else if (nper <= 8) NVFP4MOE_ROUTE(8);
+  else if (nper <= 16) NVFP4MOE_ROUTE(16);
+  else NVFP4MOE_ROUTE(32);
 #undef NVFP4MOE_ROUTE
+  if (err != cudaSuccess || C == 1) return err;
+  const size_t smem = 2 * (size_t)C * E * sizeof(uint32_t);
+  if (smem <= kPlaceSmemMax) {
+    err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_place_kernel), (int)kPlaceSmemMax);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(route_place_kernel, 1, 1024, smem, st, T, E, k, static_cast<const int32_t*>(topk_ids),
+                      static_cast<const uint32_t*>(masks), static_cast<const uint32_t*>(amax_part),
+                      x_bf16 != nullptr ? amax : nullptr, offsets, perm, inv, dev_status);
+  }
+  return launch_pdl(route_place_serial_kernel, 1, 1024, 0, st, T, E, k, static_cast<const int32_t*>(topk_ids),
+                    static_cast<const uint32_t*>(masks), static_cast<const uint32_t*>(amax_part),
+                    x_bf16 != nullptr ? amax : nullptr, offsets, perm, inv, dev_status);
 }
 
 cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* act_in, const uint8_t* act_in_scales,
