@@ -426,11 +426,12 @@ int moe_layer_forward_host(int mode, const void* x_host, const float* logits_hos
  * scratch in a fixed array of NVFP4MOE_NOALLOC_SCRATCH_BYTES bytes inside the
  * library's own device memory: it allocates nothing and calls no allocating
  * routine.
- *   - Limit: a call needs 256 + 4 * ceil(T / 32) * E + 4 * ceil(T / 32)
- *     bytes of scratch (each term after the first rounded up to 256); a
- *     larger problem (e.g. T > 4064 tokens at E = 1024 experts, T > 32480 at
- *     E = 128) is refused with NVFP4_E_WORKSPACE before anything is
- *     launched.
+ *   - Limit: a call needs 256 + 4 * B * E + 4 * B bytes of scratch (each
+ *     term after the first rounded up to 256), B = ceil(T / 32) thread
+ *     blocks of routing, times 4 for 33 <= T <= 256 (eight tokens per block
+ *     there); a larger problem (e.g. T > 4064 tokens at E = 1024 experts,
+ *     T > 32480 at E = 128) is refused with NVFP4_E_WORKSPACE before
+ *     anything is launched.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current), and so does the first call
  *     after a device reset (cudaDeviceReset destroys the context, and the

@@ -1,7 +1,8 @@
 // route.cu -- router top-k and the stable expert permutation (counting sort),
 // plus the gather of activation rows into permuted order.
 //
-// route_kernel: one CTA per chunk of 32 tokens, one warp per token.
+// route_kernel: one warp per token; one CTA per chunk of 32 tokens, or, for
+// up to 8 chunks, four CTAs of 8 tokens per chunk (see route_subs).
 //  1. top-k: the token's logits sit in registers (E/32 per lane, a
 //     compile-time count); k rounds of a warp-shuffle arg-max (ties to the
 //     lower expert id) give the experts in descending logit order; the weights
@@ -14,7 +15,7 @@
 //                        + popcount(mask bits of earlier tokens in the chunk)
 //     which is stable by (expert, token) by construction.
 //     With a single chunk (T <= 32, decode) the one CTA does this straight
-//     from shared memory.  With several chunks each CTA stores its chunk's
+//     from shared memory.  With several chunks each CTA stores its tokens'
 //     masks (and activation amax) and route_place_kernel -- the next launch,
 //     a programmatic dependent -- does the placement: no completion counter,
 //     so nothing in the scratch has to be zeroed (no memset node).
@@ -33,18 +34,32 @@ constexpr int kChunk = 32;
 // to 24K (chunk, expert) cells (e.g. 3072 tokens at 256 experts)
 constexpr size_t kPlaceSmemMax = 192 * 1024;
 
-// Scratch layout: [0, 256) the activation amax in word 1; then masks [C][E]
-// u32; then per-chunk activation amax [C] u32.
+// CTAs per 32-token chunk in the multi-chunk launch: four CTAs of eight
+// tokens while there are at most 8 chunks (T <= 256), so that the top-k --
+// k shuffle rounds per token, up to 22 rounds over 512 experts at the wide
+// workload -- runs on four times as many SMs; one CTA of 32 tokens beyond.
+static int route_subs(int C) { return C > 1 && C <= 8 ? 4 : 1; }
+
+// Scratch layout: [0, 256) the activation amax in word 1; then one mask per
+// (CTA, expert) [C * subs][E] u32; then per-CTA activation amax [C * subs].
 size_t route_workspace_bytes(int T, int E) {
   const size_t C = (size_t)(T + kChunk - 1) / kChunk;
-  return 256 + ((C * (size_t)E * 4 + 255) & ~(size_t)255) + ((C * 4 + 255) & ~(size_t)255);
+  const size_t CS = C * (size_t)route_subs((int)C);
+  return 256 + ((CS * (size_t)E * 4 + 255) & ~(size_t)255) + ((CS * 4 + 255) & ~(size_t)255);
+}
+
+// Chunk cc's mask of expert e: the OR of its `subs` CTAs' masks.
+__device__ __forceinline__ uint32_t chunk_mask(const uint32_t* masks, int subs, int cc, int E, int e) {
+  uint32_t m = 0;
+  for (int j = 0; j < subs; ++j) m |= __ldcg(masks + (int64_t)(cc * subs + j) * E + e);
+  return m;
 }
 
 // Counts, exclusive scan -> offsets, and the stable placement of every
 // (token, slot) pair of C chunks (all threads of a 1024-thread CTA, thread e
 // = expert e).  single: one chunk whose ids and masks are in shared memory;
 // otherwise they are read from global memory (ids [T, k], masks [C][E]).
-__device__ __forceinline__ void route_place(int T, int E, int k, int C, bool single, const int32_t* s_ids,
+__device__ __forceinline__ void route_place(int T, int E, int k, int C, int subs, bool single, const int32_t* s_ids,
                                             const uint32_t* s_mask, const int32_t* ids, const uint32_t* masks,
                                             int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dev_status,
                                             int32_t* base, int32_t* warp_tot) {
@@ -53,7 +68,7 @@ __device__ __forceinline__ void route_place(int T, int E, int k, int C, bool sin
   if (e < E) {
     if (single) cnt = __popc(s_mask[e]);
     else
-      for (int cc = 0; cc < C; ++cc) cnt += __popc(__ldcg(masks + (int64_t)cc * E + e));
+      for (int cc = 0; cc < C; ++cc) cnt += __popc(chunk_mask(masks, subs, cc, E, e));
   }
   int incl = cnt;
 #pragma unroll
@@ -90,14 +105,14 @@ __device__ __forceinline__ void route_place(int T, int E, int k, int C, bool sin
       const int tt = cc * kChunk + tl;
       if (tt < T) {
         const int ee = single ? s_ids[tl * k + j] : __ldcg(ids + (int64_t)tt * k + j);
-        const uint32_t m = single ? s_mask[ee] : __ldcg(masks + (int64_t)cc * E + ee);
+        const uint32_t m = single ? s_mask[ee] : chunk_mask(masks, subs, cc, E, ee);
         const int row = base[ee] + __popc(m & ((1u << tl) - 1u));
         perm[row] = tt;
         inv[(int64_t)tt * k + j] = row;
       }
     }
     __syncthreads();
-    if (e < E && !single) base[e] += __popc(__ldcg(masks + (int64_t)cc * E + e));
+    if (e < E && !single) base[e] += __popc(chunk_mask(masks, subs, cc, E, e));
     __syncthreads();
   }
 }
@@ -116,12 +131,11 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   __shared__ int32_t s_ids[kChunk * 32];  // this chunk's expert ids (k <= 32)
   __shared__ uint32_t s_amax;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
-  const int C = gridDim.x;
+  const int tpc = blockDim.x >> 5;  // tokens of this CTA: 32, or 8 (four CTAs per chunk)
   // a single chunk (T <= 32, the decode case) keeps everything in shared
   // memory: no mask round trip through global memory, and the placement
   // follows in this launch
-  const bool single = (C == 1);
+  const bool single = (gridDim.x == 1);
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0;
   if (threadIdx.x == 0) s_amax = 0;
   pdl_wait();
@@ -130,7 +144,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
 
   // 1-2: top-k of this chunk's tokens, chunk mask (and, when x is given, the
   // amax of the token's activation row for the per-tensor NVFP4 scale)
-  const int t = c * kChunk + warp;
+  const int t = blockIdx.x * tpc + warp;  // token; its bit in the chunk mask is t % 32
   if (t < T && x != nullptr) {
     const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
     float m = 0.0f;
@@ -161,19 +175,19 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
       ids[(int64_t)t * k + lane] = my_id;
       w[(int64_t)t * k + lane] = my_w;
       s_ids[warp * k + lane] = my_id;
-      atomicOr(&mask[my_id], 1u << warp);
+      atomicOr(&mask[my_id], 1u << (t % kChunk));
     }
   }
   __syncthreads();
   if (!single) {
     // several chunks: store this chunk's masks and amax; the placement is
     // route_place_kernel's (the next launch)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)c * E + e] = mask[e];
-    if (x != nullptr && threadIdx.x == 0) amax_part[c] = s_amax;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[(int64_t)blockIdx.x * E + e] = mask[e];
+    if (x != nullptr && threadIdx.x == 0) amax_part[blockIdx.x] = s_amax;
     return;
   }
   if (x != nullptr && threadIdx.x == 0) *amax_bits = s_amax;
-  route_place(T, E, k, 1, true, s_ids, mask, ids, masks, offsets, perm, inv, dev_status, base, warp_tot);
+  route_place(T, E, k, 1, 1, true, s_ids, mask, ids, masks, offsets, perm, inv, dev_status, base, warp_tot);
 }
 
 // The placement of a routing over several chunks (one CTA of 1024 threads,
@@ -189,7 +203,8 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
 // (dynamic; the launcher checks the size).  Walking the chunks in order with
 // the masks in global memory instead took two dependent L2 round trips per
 // chunk (~25 us at 16 chunks).
-__global__ void __launch_bounds__(1024) route_place_kernel(int T, int E, int k, const int32_t* __restrict__ ids,
+__global__ void __launch_bounds__(1024) route_place_kernel(int T, int E, int k, int subs,
+                                                           const int32_t* __restrict__ ids,
                                                            const uint32_t* __restrict__ masks,
                                                            const uint32_t* __restrict__ amax_part,
                                                            uint32_t* __restrict__ amax_bits,
@@ -206,16 +221,22 @@ __global__ void __launch_bounds__(1024) route_place_kernel(int T, int E, int k, 
   uint32_t* s_pre = sm + C * E;
   if (amax_bits != nullptr && threadIdx.x < 32) {
     uint32_t m = 0;
-    for (int c = threadIdx.x; c < C; c += 32) m = max(m, __ldcg(amax_part + c));
+    for (int c = threadIdx.x; c < C * subs; c += 32) m = max(m, __ldcg(amax_part + c));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (threadIdx.x == 0) *amax_bits = m;
   }
+  // chunk masks = the OR of each chunk's `subs` per-CTA masks
   const int n = C * E;
   for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
     uint32_t v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = (i0 + j * (int)blockDim.x < n) ? __ldcg(masks + i0 + j * blockDim.x) : 0u;
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * blockDim.x;
+      v[j] = 0u;
+      if (i < n)
+        for (int q = 0; q < subs; ++q) v[j] |= __ldcg(masks + (int64_t)((i / E) * subs + q) * E + (i % E));
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (i0 + j * (int)blockDim.x < n) s_mask[i0 + j * blockDim.x] = v[j];
@@ -276,7 +297,7 @@ __global__ void __launch_bounds__(1024) route_place_kernel(int T, int E, int k, 
 
 // The same placement for routings whose masks do not fit in shared memory:
 // the chunks in order, masks and ids read from global memory.
-__global__ void __launch_bounds__(1024) route_place_serial_kernel(int T, int E, int k,
+__global__ void __launch_bounds__(1024) route_place_serial_kernel(int T, int E, int k, int subs,
                                                                   const int32_t* __restrict__ ids,
                                                                   const uint32_t* __restrict__ masks,
                                                                   const uint32_t* __restrict__ amax_part,
@@ -291,12 +312,13 @@ __global__ void __launch_bounds__(1024) route_place_serial_kernel(int T, int E, 
   const int C = (T + kChunk - 1) / kChunk;
   if (amax_bits != nullptr && threadIdx.x < 32) {
     uint32_t m = 0;
-    for (int c = threadIdx.x; c < C; c += 32) m = max(m, __ldcg(amax_part + c));
+    for (int c = threadIdx.x; c < C * subs; c += 32) m = max(m, __ldcg(amax_part + c));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (threadIdx.x == 0) *amax_bits = m;
   }
-  route_place(T, E, k, C, false, nullptr, nullptr, ids, masks, offsets, perm, inv, dev_status, base, warp_tot);
+  route_place(T, E, k, C, subs, false, nullptr, nullptr, ids, masks, offsets, perm, inv, dev_status, base,
+              warp_tot);
 }
 
 // One warp per permuted row: copy `row_bytes` (and `sc_bytes` of scales).
@@ -326,15 +348,16 @@ cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t*
                               cudaStream_t st, const void* x_bf16, int64_t H) {
   if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st);
   const int C = (T + kChunk - 1) / kChunk;
+  const int subs = route_subs(C);
   uint32_t* amax = static_cast<uint32_t*>(ws) + 1;  // word 1: activation amax
   uint32_t* masks = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
-  uint32_t* amax_part =
-      reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256 + (((size_t)C * E * 4 + 255) & ~(size_t)255));
+  uint32_t* amax_part = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256 +
+                                                    (((size_t)C * subs * E * 4 + 255) & ~(size_t)255));
   const int nper = (E + 31) / 32;
   cudaError_t err;
-#define NVFP4MOE_ROUTE(NP)                                                                                       \
-  err = launch_pdl(route_kernel<NP>, C, 1024, 0, st, logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, masks, \
-                   amax_part, dev_status, static_cast<const __nv_bfloat16*>(x_bf16), (int64_t)H, amax)
+#define NVFP4MOE_ROUTE(NP)                                                                                         \
+  err = launch_pdl(route_kernel<NP>, C * subs, 1024 / subs, 0, st, logits, T, E, k, topk_ids, topk_w, offsets, perm, \
+                   inv, masks, amax_part, dev_status, static_cast<const __nv_bfloat16*>(x_bf16), (int64_t)H, amax)
   if (nper <= 1) NVFP4MOE_ROUTE(1);
   else if (nper <= 2) NVFP4MOE_ROUTE(2);
   else if (nper <= 4) NVFP4MOE_ROUTE(4);
@@ -347,11 +370,12 @@ cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t*
   if (smem <= kPlaceSmemMax) {
     err = ensure_dynamic_smem(reinterpret_cast<const void*>(route_place_kernel), (int)kPlaceSmemMax);
     if (err != cudaSuccess) return err;
-    return launch_pdl(route_place_kernel, 1, 1024, smem, st, T, E, k, static_cast<const int32_t*>(topk_ids),
+    return launch_pdl(route_place_kernel, 1, 1024, smem, st, T, E, k, subs, static_cast<const int32_t*>(topk_ids),
                       static_cast<const uint32_t*>(masks), static_cast<const uint32_t*>(amax_part),
                       x_bf16 != nullptr ? amax : nullptr, offsets, perm, inv, dev_status);
   }
-  return launch_pdl(route_place_serial_kernel, 1, 1024, 0, st, T, E, k, static_cast<const int32_t*>(topk_ids),
+  return launch_pdl(route_place_serial_kernel, 1, 1024, 0, st, T, E, k, subs,
+                    static_cast<const int32_t*>(topk_ids),
                     static_cast<const uint32_t*>(masks), static_cast<const uint32_t*>(amax_part),
                     x_bf16 != nullptr ? amax : nullptr, offsets, perm, inv, dev_status);
 }
