@@ -100,7 +100,7 @@ struct Params {
   int32_t* dev_status;
   int E, N, K, R;
   int drop_stage;  // fault injection for tests: producer stage index never armed (-1: none)
-  int splits;      // K splits per work item: 1, or 2 (the halves add into a zeroed output)
+  int splits;      // K parts per work item, 1 to 8 (more than one: they add into a zeroed output)
 };
 
 
@@ -219,8 +219,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   pdl_trigger();  // after this CTA's TMEM allocation
   const uint32_t tmem = tmem_base_s;
-  // work unit = (item, K split); splits is 1, or 2 when the items alone
-  // cannot fill the GPU (the two K halves then add into a zeroed output)
+  // work unit = (item, K part); more than one part when the items alone
+  // cannot fill the GPU (the parts then add into a zeroed output)
   const int units = tab.base[p.E] * p.splits;
   // unit number j of this CTA (u = blockIdx.x + j * gridDim.x)
   auto unit_j = [&](int j, int u) -> Unit {
@@ -465,8 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (tb + i < m1) p.out[(size_t)(tb + i) * p.N + n] = __fmul_rn(__uint_as_float(r[i]), alpha);
             continue;
           }
-          // a K half: the two halves add into a zeroed output (0 + a + b ==
-          // 0 + b + a, so the sum does not depend on their order)
+          // a K part: the parts add into a zeroed output
           if constexpr (G == 4) {
             if (tb + TG <= m1) {
               // a full group: stage it as [token][row] and let TMA add it into
@@ -562,13 +561,17 @@ static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, c
   p.drop_stage = fault_injection_drop_stage();
   // the number of work items depends on the routing, which lives on the
   // device: launch one persistent CTA per SM and let each find its items
-  // Split K in two when even the largest possible number of work items,
-  // tiles x (experts + R/128) passes, cannot fill every SM once.  Exactly two
-  // partial sums keep the result independent of their arrival order.
+  // Split K when even the largest possible number of work items -- N/128
+  // tiles times sum_e ceil(m_e / TOK) <= (R + E (TOK - 1)) / TOK passes --
+  // cannot fill every SM once: into as many parts (up to 8, at least one K
+  // stage each) as keep every unit in one wave.  Two parts added onto zero
+  // give the same sum in either order; with more, the fp32 summation order
+  // (and so the last bits) follows their arrival.
   constexpr int TOK = Geo<G>::TOK_PER_PASS;
-  const long long max_items = (long long)(N / BM) * ((long long)E + (R + TOK - 1) / TOK);
-  p.splits = (max_items < num_sms() && (K / KC) >= 2) ? 2 : 1;
-  if (p.splits == 2) {
+  const long long max_items = (long long)(N / BM) * (((long long)R + (long long)E * (TOK - 1)) / TOK);
+  p.splits = 1;
+  while (p.splits < 8 && max_items * (p.splits + 1) <= num_sms() && (K / KC) >= p.splits + 1) ++p.splits;
+  if (p.splits > 1) {
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }

@@ -19,8 +19,8 @@
 //    its N side; one pair tile = (expert, 256-row weight tile, pass of BN
 //    tokens), numbered expert-major as in the decode kernel; persistent pairs
 //    (76 on 152 SMs) walk the tiles round-robin;
-//  * a K split in two halves when the tiles cannot occupy every pair: both
-//    add into a zeroed output (0 + a + b == 0 + b + a: order-independent);
+//  * a K split (2 to 4 parts) when the tiles cannot occupy every pair: the
+//    parts add into a zeroed output;
 //  * epilogue: full 32-token groups are staged in shared memory and written
 //    by TMA (store, or reduce-add for a K half), asynchronously to the warp;
 //    an expert's ragged last group is written (or added) element-wise.
@@ -30,10 +30,13 @@
 //              all BN tokens), own weight scales
 //    warp 1    leader CTA: tcgen05.cp of the block scales and tcgen05.mma for
 //              the pair; peer CTA: tensor-memory allocation only
-//    warps 2-5 epilogue of the CTA's own 128 rows x BN tokens
+//    warps 2-5, 7-10  epilogue of the CTA's own 128 rows x BN tokens: two
+//              warps per tensor-memory lane quarter, each draining every
+//              other 32-token group
 //    warp 6    token-scale transpose (and MXFP4 widening) in shared memory;
-//              arrives on the leader's "scales ready" barrier, so the leader's
-//              MMA waits for both CTAs' stages
+//              arrives on the leader's "scales ready" barrier once its own
+//              stage has landed, so that barrier alone tells the leader's MMA
+//              that both CTAs' stages are complete
 // Cross-CTA signals: the leader's tcgen05.commit arrives on both CTAs'
 // "stage empty" and "accumulator full" barriers (multicast); both CTAs'
 // epilogue warps arrive on the leader's "accumulator empty" barrier.  Every
@@ -61,7 +64,7 @@ constexpr int KC = 256;                        // K elements per stage (one 128-
 constexpr int TG = 32;                         // tokens per group
 constexpr uint32_t W_BYTES = BM * KC / 2;      // 16384
 constexpr uint32_t WS_BYTES = BM * KC / 16;    // 2048: weight scale cells
-constexpr int NUM_THREADS = 224;
+constexpr int NUM_THREADS = 352;
 
 template <int BN>
 struct Geo {
@@ -82,8 +85,8 @@ struct Geo {
   static constexpr uint32_t SF_STAGE = 16 + 4 * G;
   static constexpr uint32_t TMEM_USED = SF_BASE + STAGES * SF_STAGE;
   static constexpr uint32_t TMEM_ALLOC = TMEM_USED <= 256 ? 256 : 512;
-  // epilogue staging: per epilogue warp two [32 tokens][32 rows] fp32 boxes
-  static constexpr uint32_t RED_BYTES = 4 * 2 * TG * 32 * 4;
+  // epilogue staging: per epilogue warp one [32 tokens][32 rows] fp32 box
+  static constexpr uint32_t RED_BYTES = 8 * TG * 32 * 4;
   static constexpr uint32_t OFF_RED = STAGES * STAGE_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_RED + RED_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
@@ -108,7 +111,7 @@ struct Params {
   int32_t* dev_status;
   int E, N, K, R;
   int drop_stage;  // fault injection for tests: producer stage index never armed (-1: none)
-  int splits;      // 1, or 2 (the halves add into a zeroed output)
+  int splits;      // K parts, 1 to 4 (more than one: they add into a zeroed output)
 };
 
 struct Unit {
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t sf_ready[STAGES];   // leader: both CTAs' stage prepared (count 2)
   __shared__ __align__(8) uint64_t empty_bar[STAGES];  // the pair's MMAs of the stage completed
   __shared__ __align__(8) uint64_t acc_full[ACC_BUFS];
-  __shared__ __align__(8) uint64_t acc_empty[ACC_BUFS];  // leader: 8 epilogue warps (both CTAs) drained
+  __shared__ __align__(8) uint64_t acc_empty[ACC_BUFS];  // leader: 16 epilogue warps (both CTAs) drained
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < ACC_BUFS; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 8);
+      mbar_init(&acc_empty[a], 16);
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -361,8 +364,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d_col = tmem + acc * BN;
         for (int kc = cur.kc0; kc < cur.kc1; ++kc) {
-          if (!pair::warp_wait_cluster(&sf_ready[stage], phase, &abort_flag, p.dev_status) ||
-              !warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
+          // both CTAs' scale warps arrive only after their own stage landed
+          if (!pair::warp_wait_cluster(&sf_ready[stage], phase, &abort_flag, p.dev_status)) {
             ok = false;
             break;
           }
@@ -403,13 +406,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2-5, both CTAs)
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ epilogue (warps 2-5, 7-10, both CTAs)
+    const int q = warp & 3;     // TMEM lane quarter this warp may access
+    const int eh = warp >= 7;   // the groups it drains: eh, eh + 2, ...
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    float* red = reinterpret_cast<float*>(smem + GE::OFF_RED) + q * 2 * (TG * 32);
-    int red_box = 0;
+    float* box = reinterpret_cast<float*>(smem + GE::OFF_RED) + (q + 4 * eh) * (TG * 32);
     for (int u = pair_id, j = 0; ok && u < units; u += npairs, ++j) {
       const WorkItem it = unit_j(j, u).it;
       const float alpha = MX ? 1.0f : __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e));
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after();
       if (lane == 0 && q == 0) PAIR_TRACE(5, j);
-      for (int g = 0; g < it.ng; ++g) {
+      for (int g = eh; g < it.ng; g += 2) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + g * TG, r);
         tmem_ld_wait();
@@ -429,8 +432,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (tb + TG <= it.m1) {
           // a full group: stage it as [token][row] and let TMA store it (or,
           // for a K half, add it in L2), asynchronously to this warp
-          float* box = red + red_box * (TG * 32);
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // box's last use read
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // box's last use read
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < 32; ++i) box[i * 32 + lane] = __fmul_rn(__uint_as_float(r[i]), alpha);
@@ -441,7 +443,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else tma_reduce_add_2d(&tm_out, box, nrow0, tb);
             bulk_commit_group();
           }
-          red_box ^= 1;
           continue;
         }
         // the expert's last, ragged group: rows past its end belong to the
@@ -523,11 +524,13 @@ static cudaError_t launch_pair_geo(const uint8_t* a_codes, const uint8_t* a_scal
   p.R = R;
   p.drop_stage = fault_injection_drop_stage();
   const int npairs = num_sms() / 2;
-  // split K in two when even the largest possible number of pair tiles,
-  // (N/256) x (experts + R/BN) passes, cannot occupy every pair once
-  const long long max_items = (long long)(N / (2 * BM)) * ((long long)E + (R + BN - 1) / BN);
-  p.splits = (max_items < npairs && (K / KC) >= 2) ? 2 : 1;
-  if (p.splits == 2) {
+  // split K into as many parts (up to 4) as still fit every unit in one
+  // wave of pairs, counting the largest possible number of pair tiles: N/256
+  // weight tiles times sum_e ceil(m_e / BN) <= (R + E (BN - 1)) / BN passes
+  const long long max_items = (long long)(N / (2 * BM)) * (((long long)R + (long long)E * (BN - 1)) / BN);
+  p.splits = 1;
+  while (p.splits < 4 && max_items * (p.splits + 1) <= npairs && (K / KC) >= 2 * (p.splits + 1)) ++p.splits;
+  if (p.splits > 1) {
     const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
@@ -550,10 +553,12 @@ static cudaError_t launch_pair_geo(const uint8_t* a_codes, const uint8_t* a_scal
 
 // The pair kernel for problems whose experts see many tokens: on average at
 // least 1024 rows per expert (passes of 256 tokens).  Measured on GB300 for
-// the single-expert GEMM N = 2048, K = 6144: at M = 4096 34.2 us against 44 us
-// for the one-CTA kernel; at M = 512 (a 128-token geometry of this kernel)
-// 13.6 us against 12.7 us, so below 1024 rows per expert the one-CTA kernel
-// runs.  Needs N % 256 == 0 and an even SM count.
+// the single-expert GEMM N = 2048, K = 6144 (CUDA-graph replays, operands
+// rotating through more than twice the L2): 33.1 us at M = 4096 against 44 us
+// for the one-CTA kernel, 18.9 us at M = 2048, 17.2 us at M = 1024; at M = 512
+// (a 4-way K split) 14.1 us against the one-CTA kernel's 12.8 us, so below
+// 1024 rows per expert the one-CTA kernel runs.  Needs N % 256 == 0 and an
+// even SM count.
 bool gemm_w4a4_pair_eligible(int E, int N, int R) {
   return N % 256 == 0 && (long long)R >= 1024LL * E && num_sms() >= 2;
 }

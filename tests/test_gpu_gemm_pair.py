@@ -1,8 +1,8 @@
 """GPU parity of the CTA-pair grouped GEMM (the .cta_group::2 kernel that
 moe_grouped_gemm_nvfp4 runs when the experts see at least 1024 rows on
 average and N % 256 == 0) against the oracle's fp64 grouped GEMM, NVFP4 and
-MXFP4: one K stage, ragged last passes, an empty expert, the two-way K split
-and the unsplit many-tiles-per-pair schedule; and routing errors reported
+MXFP4: one K stage, ragged last passes, an empty expert, K splits in two,
+three and four parts and the unsplit many-tiles-per-pair schedule; and routing errors reported
 through the status word."""
 import numpy as np
 import pytest
@@ -21,6 +21,8 @@ CASES = [
     ([1100], 512, 1024),             # ragged last pass (1100 = 4 x 256 + 76), K split in two
     ([1100, 0, 2000], 512, 768),     # an empty expert; K halves of 1 and 2 stages
     ([2100, 2200], 4096, 512),       # 304 pair tiles, several per pair, no split
+    ([2048], 512, 2048),             # 16 pair tiles: K in four parts of 2 stages
+    ([1500, 700], 256, 1536),        # ragged passes of two experts: K in three parts
 ]
 
 
@@ -51,7 +53,7 @@ def test_pair_gemm_nvfp4(orc, case):
     assert_close(out.cpu().numpy(), ref, "pair nvfp4 case %d" % case)
 
 
-@pytest.mark.parametrize("case", [1, 3])
+@pytest.mark.parametrize("case", [1, 3, 5])
 def test_pair_gemm_mxfp4(orc, case):
     dev = cuda_or_skip()
     counts, N, K = CASES[case]
