@@ -559,6 +559,32 @@ cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const 
                     h_codes, h_scales, static_cast<__nv_bfloat16*>(h_bf16));
 }
 
+// Zero fill of a GEMM's fp32 output before its K parts add into it.  An
+// ordinary launch (it starts once the stream's previous work is complete)
+// that lets the GEMM -- a programmatic dependent -- launch as soon as every
+// block has started, so the GEMM's prologue overlaps the fill where a memset
+// node would serialise the two launches.  (Launched as a programmatic
+// dependent itself, its blocks would sit resident beside the previous kernel
+// until that one completed; on GB300 that measured slower than a memset at
+// 4-8 MB.)
+__global__ void __launch_bounds__(256) zero_f32_kernel(float* __restrict__ p, size_t n) {
+  pdl_trigger();
+  const size_t n4 = n / 4, stride = (size_t)gridDim.x * blockDim.x;
+  float4* p4 = reinterpret_cast<float4*>(p);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
+    p4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (size_t i = n4 * 4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.0f;
+}
+
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return cudaMemsetAsync(p, 0, n * sizeof(float), st);
+  const size_t blocks = (n / 4 + 255) / 256;
+  const int grid = (int)(blocks < (size_t)(2 * num_sms()) ? (blocks > 0 ? blocks : 1) : 2 * num_sms());
+  zero_f32_kernel<<<grid, 256, 0, st>>>(p, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H, int out_dtype,
                            void* out, int32_t* dev_status, cudaStream_t st) {
   const int64_t total = (int64_t)T * (H / 4);

@@ -572,7 +572,7 @@ static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, c
   p.splits = 1;
   while (p.splits < 8 && max_items * (p.splits + 1) <= num_sms() && (K / KC) >= p.splits + 1) ++p.splits;
   if (p.splits > 1) {
-    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
+    cudaError_t e = launch_zero_f32(out, (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(gemm_w4a4_kernel<MX, G>, num_sms(), NUM_THREADS, Geo<G>::SMEM_BYTES, st, tm_w, tm_a, tm_as, tm_a4,

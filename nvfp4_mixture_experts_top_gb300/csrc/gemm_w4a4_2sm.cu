@@ -531,7 +531,7 @@ static cudaError_t launch_pair_geo(const uint8_t* a_codes, const uint8_t* a_scal
   p.splits = 1;
   while (p.splits < 4 && max_items * (p.splits + 1) <= npairs && (K / KC) >= 2 * (p.splits + 1)) ++p.splits;
   if (p.splits > 1) {
-    const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)R * N, st);
+    const cudaError_t e = launch_zero_f32(out, (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};

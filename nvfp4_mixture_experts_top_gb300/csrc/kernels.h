@@ -48,6 +48,9 @@ cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t co
 cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st);
 cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
                                   uint8_t* h_scales, void* h_bf16, cudaStream_t st);
+// out[0, n) = 0 before a GEMM's K parts add into it; the GEMM launched next
+// (a programmatic dependent) may start its prologue during the fill.
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, int T, int k, int H,
                            int out_dtype, void* out, int32_t* dev_status, cudaStream_t st);
 // Copy bytes16 (a multiple of 16) from src16 to dst16 and bytes4 (a multiple

@@ -114,10 +114,10 @@ def router(dev, mode):
 def layer(dev, mode):
     """The whole layer, its kernels chained as programmatic dependents: the
     injected gate_up GEMM times out, the kernels after it still run and
-    return, and the next layer call is correct.  H = 2048 gives four K stages
-    per gate_up work unit after the split, so stage 3 lies inside the first
-    ring lap."""
-    cfg = wl.MoEConfig("fail_layer", T=8, H=2048, I=512, E=4, k=2, routing="uniform")
+    return, and the next layer call is correct.  H = 4096 gives at least four
+    K stages per gate_up work unit after the K split (16 stages in up to four
+    parts), so stage 3 lies inside the first ring lap."""
+    cfg = wl.MoEConfig("fail_layer", T=8, H=4096, I=512, E=4, k=2, routing="uniform")
     m = {"w4a4": B.MOE_W4A4, "w4a16": B.MOE_W4A16}[mode]
     xt = wl.activations_bf16(cfg.T, cfg.H, seed=5)
     logits = wl.router_logits(cfg, seed=5)
