@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t d_col = tmem + acc * ACC_COLS;
       for (int kc = 0; kc < KCH; ++kc) {
-        if (!warp_wait(&a_full[slot], slot_phase, &abort_flag, p.dev_status) ||
-            !warp_wait(&raw_full[stage], phase, &abort_flag, p.dev_status)) {
+        // the dequantisation warps arrive on a_full only after they saw the
+        // raw stage (weights and tokens) land, so a_full alone orders it
+        // before the MMAs
+        if (!warp_wait(&a_full[slot], slot_phase, &abort_flag, p.dev_status)) {
           ok = false;
           break;
         }

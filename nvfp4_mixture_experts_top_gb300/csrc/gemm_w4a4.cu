@@ -389,10 +389,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d_col = tmem + acc * ACC_COLS;
         for (int kc = kc0; kc < kc1; ++kc) {
-          // sf_ready is arrived after the scale warp saw full_bar; waiting on
-          // both keeps the TMA completion directly observed by this warp
+          // sf_ready is arrived by the scale warp after it saw full_bar, so it
+          // alone orders the stage's TMA data before the MMAs.  Passes of 128
+          // tokens skip the second wait (about 150 cycles of a stage the MMA
+          // issue limits: decode_b512 gate_up and the M = 512 GEMM 3-5% faster
+          // on GB300); at 32 tokens, where HBM sets the stage rate, waiting on
+          // full_bar as well measured faster (decode_c16 gate_up 156 against
+          // 159-162 us) and stays.
           if (!warp_wait(&sf_ready[stage], phase, &abort_flag, p.dev_status) ||
-              !warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status)) {
+              (G == 1 && !warp_wait(&full_bar[stage], phase, &abort_flag, p.dev_status))) {
             ok = false;
             break;
           }
