@@ -503,6 +503,8 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
     h_c = torch.empty(R, I if mode == B.MOE_W4A8 else I // 2, dtype=torch.uint8, device=dev)
     h_s = torch.empty(R, B.mxfp4_scale_pitch(I) if mx else I // 16, dtype=torch.uint8, device=dev)
     h_b = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
+    a_rs = torch.empty(R, dtype=torch.float32, device=dev)  # W4A16: F16 row carriers' multipliers
+    h_rs = torch.empty(R, dtype=torch.float32, device=dev)
     Y = torch.empty(R, H, dtype=torch.float32, device=dev)
     out = torch.empty(T, H, dtype=torch.float32, device=dev)
     L = B.load()
@@ -556,16 +558,19 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
             chk(L.moe_grouped_gemm_nvfp4(0, P(h_c), P(h_s), P(S_h), P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
                                          cfg.E, H, I, R, P(Y), P(status), st))
         else:
-            chk(L.moe_align_permute(P(logits), T, cfg.E, k, P(ids), P(tw), P(offs), P(perm), P(inv), 2, P(x), None,
-                                    H, P(a_b), None, P(status), P(ws_route), ws_route.numel(), st))
+            # W4A16 as moe_layer_forward runs it: the bf16 operands carried as
+            # F16 rows with per-row powers of two (GEMM mode MOE_W4A16F)
+            chk(L.moe_align_permute(P(logits), T, cfg.E, k, P(ids), P(tw), P(offs), P(perm), P(inv), 0, None, None,
+                                    0, None, None, P(status), P(ws_route), ws_route.numel(), st))
+            chk(L.moe_gather_f16(P(x), T, H, P(perm), R, P(a_b), P(a_rs), st))
             if ev_pair:
                 ev_pair[0].record()
-            chk(L.moe_grouped_gemm_nvfp4(1, P(a_b), None, None, P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
+            chk(L.moe_grouped_gemm_nvfp4(4, P(a_b), None, P(a_rs), P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
                                          cfg.E, 2 * I, H, R, P(G), P(status), st))
             if ev_pair:
                 ev_pair[1].record()
-            chk(L.moe_swiglu_requant(P(G), R, I, 1, None, None, None, P(h_b), st))
-            chk(L.moe_grouped_gemm_nvfp4(1, P(h_b), None, None, P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
+            chk(L.moe_swiglu_f16(P(G), R, I, P(h_b), P(h_rs), st))
+            chk(L.moe_grouped_gemm_nvfp4(4, P(h_b), None, P(h_rs), P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
                                          cfg.E, H, I, R, P(Y), P(status), st))
         chk(L.moe_combine(P(Y), P(inv), P(tw), T, k, H, 1, P(out), P(status), st))
 
@@ -702,7 +707,7 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
     result = {
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {B.MOE_W4A4: "fp4(e2m1)xfp4, fp32 accumulate", B.MOE_W4A16: "fp4(e2m1)xbf16, fp32 accumulate",
+        "dtype": {B.MOE_W4A4: "fp4(e2m1)xfp4, fp32 accumulate", B.MOE_W4A16: "fp4(e2m1)xbf16 (carried as f16 rows), fp32 accumulate",
                   B.MOE_MXW4A4: "fp4(e2m1)xfp4 (UE8M0 scales), fp32 accumulate",
                   B.MOE_W4A8: "fp4(e2m1)xfp8(e4m3) on f16 operands, fp32 accumulate"}[mode],
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised on the GPU)",

@@ -67,7 +67,7 @@ typedef enum nvfp4_status {
 
 enum { NVFP4_DT_BF16 = 0, NVFP4_DT_F32 = 1 };
 enum { NVFP4_SCALE_STATIC = 0, NVFP4_SCALE_DYNAMIC = 1 };
-enum { MOE_W4A4 = 0, MOE_W4A16 = 1, MOE_MXW4A4 = 2, MOE_W4A8 = 3 };
+enum { MOE_W4A4 = 0, MOE_W4A16 = 1, MOE_MXW4A4 = 2, MOE_W4A8 = 3, MOE_W4A16F = 4 };
 enum { MOE_ACT_NONE = 0, MOE_ACT_NVFP4 = 1, MOE_ACT_BF16 = 2 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -295,6 +295,7 @@ int moe_route_quantize_fp8(const void* x, const float* logits, int T, int H, int
  *   W4A16: out[r, n] =        w_S[e] * sum_k a[r,k]      * dec(w[e,n,k])
  *   MXW4A4: out[r, n] =              sum_k dec(a[r,k]) * dec(w[e,n,k])
  *   W4A8 : out[r, n] = a_S * w_S[e] * sum_k e4m3(a[r,k]) * dec(w[e,n,k])
+ *   W4A16F: out[r, n] = a_S[r] * w_S[e] * sum_k a[r,k] * dec(w[e,n,k])
  * with dec(.) = e2m1(code) * e4m3(block scale) (MXFP4: * 2^(scale-127) per
  * 32 elements), fp32 accumulation.
  *   W4A4 : a = codes [R, K/2], a_scales = [R, K/16], a_S = device fp32 scalar
@@ -304,6 +305,12 @@ int moe_route_quantize_fp8(const void* x, const float* logits, int T, int H, int
  *   W4A8 : a = FP8 E4M3 codes [R, K] (fp8_quantize), a_scales = NULL, a_S =
  *          device fp32 scalar; runs on F16 operands (e2m1 * e4m3 weights and
  *          E4M3 activations are both exact in f16), fp32 accumulation
+ *   W4A16F: the W4A16 product on bf16 rows carried as F16 (moe_gather_f16,
+ *          moe_swiglu_f16): a = f16 [R, K] holding a_bf16[r] * 2^e_r, a_S =
+ *          fp32 [R] holding 2^-e_r (a power of two, so the rescale is exact),
+ *          a_scales = NULL; runs on F16 operands.  The weight dequantisation
+ *          then needs no f16 -> bf16 widening, which made the W4A16 stage
+ *          1.3x longer on GB300.
  *   w_codes        [E, N, K/2]
  *   w_scales_packed  from nvfp4_pack_weight_scales (mxfp4_pack_weight_scales)
  *   w_S            fp32 [E]
@@ -318,6 +325,33 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
                            const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                            const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
                            int32_t* dev_status, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_gather_f16 -- bf16 activation rows carried as F16 for MOE_W4A16F.
+ * The pages define no such step: it is an exact carrier of the W4A16
+ * operand for F16 tensor-core operands.  For r < R with src = perm[r] (or r
+ * when perm is NULL):
+ *   e_r       = 14 - floor(log2(max_k |x[src, k]|)), capped at 126 (0 for a
+ *               row of zeros), so the row's largest magnitude maps into
+ *               [2^14, 2^15) and nothing overflows f16;
+ *   a_f16[r]  = f16(x[src] * 2^e_r) -- exact for every element within a
+ *               factor 2^28 of the row's max (an f16 normal then), rounded to
+ *               the f16 subnormal grid below that (absolute error <= 2^-39 of
+ *               the row's max);
+ *   a_rs[r]   = 2^-e_r (fp32).
+ *   x bf16 [T, H]; perm int32 [R] (values in [0, T)) or NULL with R <= T;
+ *   a_f16 f16 [R, H]; a_rs fp32 [R]
+ * Constraints: H % 8 == 0; x and a_f16 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+int moe_gather_f16(const void* x, int T, int H, const int32_t* perm, int R, void* a_f16, float* a_rs,
+                   nvfp4_stream_t stream);
+
+/* moe_swiglu_f16 -- the W4A16 SwiGLU (as moe_swiglu_requant with MOE_W4A16:
+ * h = bf16(silu(g) * u)) written as F16 rows for MOE_W4A16F, with the
+ * per-row powers of two of moe_gather_f16: h_f16[r] = f16(h[r] * 2^e_r),
+ * h_rs[r] = 2^-e_r.  G fp32 [R, 2I]; h_f16 f16 [R, I]; h_rs fp32 [R].
+ * Constraints: I % 16 == 0; G and h_f16 16-byte aligned. */
+int moe_swiglu_f16(const float* G, int R, int I, void* h_f16, float* h_rs, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_swiglu_requant -- SwiGLU on the gate_up output and requantisation.
@@ -366,7 +400,9 @@ int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, 
  * moe_layer_forward -- the whole layer in one call: every step above,
  * enqueued in order on `stream` with no host synchronisation, so the call
  * can be captured in a CUDA graph.
- *   mode        MOE_W4A4, MOE_W4A16, MOE_MXW4A4 or MOE_W4A8
+ *   mode        MOE_W4A4, MOE_W4A16, MOE_MXW4A4 or MOE_W4A8 (MOE_W4A16 runs
+ *               moe_gather_f16, MOE_W4A16F GEMMs and moe_swiglu_f16: the
+ *               W4A16 products, with the bf16 operands carried as F16 rows)
  *   x           bf16 [T, H]; logits fp32 [T, E]
  *   w13_*       gate_up weights: codes [E, 2I, H/2], packed scales, S [E]
  *   w2_*        down weights:    codes [E, H, I/2],  packed scales, S [E]

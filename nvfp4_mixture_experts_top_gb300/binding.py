@@ -17,7 +17,7 @@ from . import build as _build
 NVFP4_OK = 0
 NVFP4_DT_BF16, NVFP4_DT_F32 = 0, 1
 NVFP4_SCALE_STATIC, NVFP4_SCALE_DYNAMIC = 0, 1
-MOE_W4A4, MOE_W4A16, MOE_MXW4A4, MOE_W4A8 = 0, 1, 2, 3
+MOE_W4A4, MOE_W4A16, MOE_MXW4A4, MOE_W4A8, MOE_W4A16F = 0, 1, 2, 3, 4
 MOE_ACT_NONE, MOE_ACT_NVFP4, MOE_ACT_BF16 = 0, 1, 2
 STATUS_NAMES = {0: "NVFP4_OK", 1: "NVFP4_E_INVAL", 2: "NVFP4_E_SHAPE", 3: "NVFP4_E_ALIGN", 4: "NVFP4_E_WORKSPACE",
                 5: "NVFP4_E_ARCH", 6: "NVFP4_E_CUDA", 7: "NVFP4_E_DEVICE_TIMEOUT", 8: "NVFP4_E_BAD_ROUTING"}
@@ -30,7 +30,7 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspac
            "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4",
            "moe_router_logits_workspace_bytes", "moe_router_logits", "moe_layer_host_workspace_bytes",
            "moe_layer_forward_host", "fp8_quantize", "moe_route_quantize_fp8", "moe_router_route_workspace_bytes",
-           "moe_router_route")
+           "moe_router_route", "moe_gather_f16", "moe_swiglu_f16")
 
 
 class Nvfp4Error(RuntimeError):
@@ -108,6 +108,10 @@ def load(build_if_missing: bool = True):
     L.moe_router_route_workspace_bytes.argtypes = [_I, _I, _I, _I]
     L.moe_router_route.restype = _I
     L.moe_router_route.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_gather_f16.restype = _I
+    L.moe_gather_f16.argtypes = [_P, _I, _I, _P, _I, _P, _P, _P]
+    L.moe_swiglu_f16.restype = _I
+    L.moe_swiglu_f16.argtypes = [_P, _I, _I, _P, _P, _P]
     L.fp8_quantize.restype = _I
     L.fp8_quantize.argtypes = [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _SZ, _P]
     L.moe_route_quantize_fp8.restype = _I
@@ -414,6 +418,30 @@ def moe_swiglu_requant(G, mode, S_h=None):
     hb = _empty((max(R, 1), I), torch.bfloat16, dev)
     _check("moe_swiglu_requant", L.moe_swiglu_requant(_ptr(G), R, I, mode, None, None, None, _ptr(hb), _stream()))
     return hb[:R]
+
+
+def moe_gather_f16(x, perm=None, R=None):
+    """bf16 rows x[perm[r]] (or x[r]) carried as F16: returns (a_f16 [R, H]
+    float16 holding x * 2^e_r, a_rs [R] fp32 = 2^-e_r)."""
+    L = load()
+    T, H = x.shape
+    R = (perm.numel() if perm is not None else T) if R is None else R
+    a = _empty((max(R, 1), H), torch.float16, x.device)
+    rs = _empty((max(R, 1),), torch.float32, x.device)
+    _check("moe_gather_f16", L.moe_gather_f16(_ptr(x), T, H, _ptr(perm), R, _ptr(a), _ptr(rs), _stream()))
+    return a[:R], rs[:R]
+
+
+def moe_swiglu_f16(G):
+    """The W4A16 SwiGLU (h rounded to bf16) carried as F16 rows: returns
+    (h_f16 [R, I] float16 = h * 2^e_r, h_rs [R] fp32 = 2^-e_r)."""
+    L = load()
+    R, I2 = G.shape
+    I = I2 // 2
+    h = _empty((max(R, 1), I), torch.float16, G.device)
+    rs = _empty((max(R, 1),), torch.float32, G.device)
+    _check("moe_swiglu_f16", L.moe_swiglu_f16(_ptr(G), R, I, _ptr(h), _ptr(rs), _stream()))
+    return h[:R], rs[:R]
 
 
 def moe_combine(Y, inv, topk_w, out_dtype=torch.float32, dev_status=None):

@@ -397,7 +397,8 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
                            const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                            const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
                            int32_t* dev_status, nvfp4_stream_t stream) {
-  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8) return NVFP4_E_INVAL;
+  if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8 && mode != MOE_W4A16F)
+    return NVFP4_E_INVAL;
   if (E <= 0 || N < 0 || K < 0 || R < 0) return NVFP4_E_INVAL;
   if (N % 128 != 0 || K % 256 != 0) return NVFP4_E_SHAPE;
   if (R == 0 || N == 0 || K == 0) return NVFP4_OK;
@@ -406,7 +407,7 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
     return NVFP4_E_INVAL;
   if (mode != MOE_MXW4A4 && w_S == nullptr) return NVFP4_E_INVAL;
   if (mode == MOE_W4A4 && (a_scales == nullptr || a_S == nullptr)) return NVFP4_E_INVAL;
-  if (mode == MOE_W4A8 && a_S == nullptr) return NVFP4_E_INVAL;
+  if ((mode == MOE_W4A8 || mode == MOE_W4A16F) && a_S == nullptr) return NVFP4_E_INVAL;
   if (mode == MOE_MXW4A4 && a_scales == nullptr) return NVFP4_E_INVAL;
   if (!aligned16(a) || !aligned16(w_codes) || !aligned16(w_scales_packed) || !aligned16(out))
     return NVFP4_E_ALIGN;
@@ -416,6 +417,9 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
   if (mode == MOE_W4A8)
     return cuda_status(launch_gemm_w4a8(static_cast<const uint8_t*>(a), a_S, w_codes, w_scales_packed, w_S,
                                         expert_offsets, E, N, K, R, out, dev_status, st));
+  if (mode == MOE_W4A16F)
+    return cuda_status(launch_gemm_w4a16_f16(a, a_S, w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out,
+                                             dev_status, st));
   // many tokens per expert (prefill, large-M GEMMs): CTA pairs on one MMA
   if ((mode == MOE_W4A4 || mode == MOE_MXW4A4) && gemm_w4a4_pair_eligible(E, N, R))
     return cuda_status(launch_gemm_w4a4_pair(mode == MOE_MXW4A4, static_cast<const uint8_t*>(a), a_scales, a_S,
@@ -429,6 +433,28 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
                                         expert_offsets, E, N, K, R, out, dev_status, st));
   return cuda_status(
       launch_gemm_w4a16(a, w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out, dev_status, st));
+}
+
+int moe_gather_f16(const void* x, int T, int H, const int32_t* perm, int R, void* a_f16, float* a_rs,
+                   nvfp4_stream_t stream) {
+  if (T < 0 || H < 0 || R < 0) return NVFP4_E_INVAL;
+  if (H % 8 != 0) return NVFP4_E_SHAPE;
+  if ((int64_t)R * H == 0) return NVFP4_OK;
+  if (x == nullptr || a_f16 == nullptr || a_rs == nullptr) return NVFP4_E_INVAL;
+  if (perm == nullptr && R > T) return NVFP4_E_INVAL;
+  if (!aligned16(x) || !aligned16(a_f16)) return NVFP4_E_ALIGN;
+  CHECK_ARCH();
+  return cuda_status(launch_gather_f16(x, H, perm, R, a_f16, a_rs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_swiglu_f16(const float* G, int R, int I, void* h_f16, float* h_rs, nvfp4_stream_t stream) {
+  if (R < 0 || I < 0) return NVFP4_E_INVAL;
+  if (I % 16 != 0) return NVFP4_E_SHAPE;
+  if ((int64_t)R * I == 0) return NVFP4_OK;
+  if (G == nullptr || h_f16 == nullptr || h_rs == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(G) || !aligned16(h_f16)) return NVFP4_E_ALIGN;
+  CHECK_ARCH();
+  return cuda_status(launch_swiglu_f16(G, R, I, h_f16, h_rs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
@@ -475,7 +501,8 @@ struct LayerWs {
   uint32_t* amax;
   void* route;
   uint8_t *xq_codes, *xq_scales, *a_codes, *a_scales, *h_codes, *h_scales;
-  void *a_bf16, *h_bf16;
+  void *a_bf16, *h_bf16;  // W4A16: the F16-carried rows (same size)
+  float *a_rs, *h_rs;     // W4A16: their per-row multipliers
   size_t total;
 };
 
@@ -516,6 +543,8 @@ static LayerWs carve(void* base, int mode, int T, int H, int I, int E, int k) {
   } else {
     w.a_bf16 = take(R * H * 2);
     w.h_bf16 = take(R * I * 2);
+    w.a_rs = reinterpret_cast<float*>(take(R * 4));
+    w.h_rs = reinterpret_cast<float*>(take(R * 4));
   }
   w.total = off;
   return w;
@@ -584,15 +613,20 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
                                E, H, I, R, w.Y, dev_status, stream);
     if (s != NVFP4_OK) return s;
   } else {
-    s = moe_align_permute(logits, T, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, MOE_ACT_BF16, x, nullptr, H,
-                          w.a_bf16, nullptr, dev_status, w.route, route_workspace_bytes(T, E), stream);
+    // W4A16: the bf16 activations (x, and h rounded to bf16) travel as F16
+    // rows with per-row powers of two, which the F16 form of the dequantising
+    // GEMM takes (the same products; see moe_gather_f16)
+    s = moe_align_permute(logits, T, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, MOE_ACT_NONE, nullptr, nullptr, 0,
+                          nullptr, nullptr, dev_status, w.route, route_workspace_bytes(T, E), stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_W4A16, w.a_bf16, nullptr, nullptr, w13_codes, w13_scales_packed, w13_S,
+    s = moe_gather_f16(x, T, H, w.perm, R, w.a_bf16, w.a_rs, stream);
+    if (s != NVFP4_OK) return s;
+    s = moe_grouped_gemm_nvfp4(MOE_W4A16F, w.a_bf16, nullptr, w.a_rs, w13_codes, w13_scales_packed, w13_S,
                                w.offsets, E, 2 * I, H, R, w.G, dev_status, stream);
     if (s != NVFP4_OK) return s;
-    s = moe_swiglu_requant(w.G, R, I, MOE_W4A16, nullptr, nullptr, nullptr, w.h_bf16, stream);
+    s = moe_swiglu_f16(w.G, R, I, w.h_bf16, w.h_rs, stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_W4A16, w.h_bf16, nullptr, nullptr, w2_codes, w2_scales_packed, w2_S, w.offsets,
+    s = moe_grouped_gemm_nvfp4(MOE_W4A16F, w.h_bf16, nullptr, w.h_rs, w2_codes, w2_scales_packed, w2_S, w.offsets,
                                E, H, I, R, w.Y, dev_status, stream);
     if (s != NVFP4_OK) return s;
   }

@@ -559,6 +559,122 @@ cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const 
                     h_codes, h_scales, static_cast<__nv_bfloat16*>(h_bf16));
 }
 
+// ---------------------------------------------------------------------------
+// F16 carrier of BF16 rows (the W4A16 product on F16 tensor-core operands).
+// A bf16 value has 8 significant bits, an f16 11, but f16 spans only
+// [2^-24, 65504].  Row r is carried as f16(x * 2^e_r) with the power of two
+// chosen so that the row's max |x| lands in [2^14, 2^15): every element of
+// the row within a factor 2^28 of that max stays an f16 normal and is exact;
+// smaller ones round to the f16 subnormal grid, an absolute error of at most
+// 2^-39 times the row's max.  rs[r] = 2^-e_r undoes the scaling (exactly:
+// a power of two) in the GEMM's epilogue.
+// ---------------------------------------------------------------------------
+
+// e_r for a row whose largest magnitude is amax (0: an all-zero row), kept
+// within [-113, 126] so that 2^e and 2^-e are fp32 normals.
+__device__ __forceinline__ int f16_row_exponent(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  const int e = 14 - ilogbf(amax);
+  return e > 126 ? 126 : e;
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// One warp per output row: a_f16[r] = x[src] * 2^e_r, rs[r] = 2^-e_r, with
+// src = perm[r] (or r).  Two passes over the row (max, then convert); the
+// second reads it from L1/L2.
+__global__ void __launch_bounds__(256) gather_f16_kernel(const __nv_bfloat16* __restrict__ x, int64_t H,
+                                                         const int32_t* __restrict__ perm, int R,
+                                                         __half* __restrict__ a, float* __restrict__ rs) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
+    const int64_t t = perm != nullptr ? (int64_t)__ldg(perm + r) : r;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    float m = 0.0f;
+    for (int64_t i = lane; i < H / 8; i += 32) {
+      const uint4 u = __ldg(src + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const int e = f16_row_exponent(m);
+    const float sc = pow2f(e);
+    uint4* dst = reinterpret_cast<uint4*>(a + r * H);
+    for (int64_t i = lane; i < H / 8; i += 32) {
+      const uint4 u = __ldg(src + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 h2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[q] << 16), sc),
+                                             __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), sc));
+        o4[q] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      dst[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+    if (lane == 0) rs[r] = pow2f(-e);
+  }
+}
+
+// One warp per row r of G [R, 2I] (gate | up): h = bf16(silu(g) * u) -- the
+// W4A16 activation of the down GEMM -- carried as f16(h * 2^e_r), rs[r] =
+// 2^-e_r.  The bf16 values are written first (as 16-bit words into the f16
+// buffer) with the row's max taken on the way, then converted in place.
+__global__ void __launch_bounds__(256) swiglu_f16_kernel(const float* __restrict__ G, int64_t R, int64_t I,
+                                                         __half* __restrict__ h, float* __restrict__ rs) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
+    const float4* gp = reinterpret_cast<const float4*>(G + r * 2 * I);
+    const float4* up = reinterpret_cast<const float4*>(G + r * 2 * I + I);
+    uint2* hrow = reinterpret_cast<uint2*>(h + r * I);
+    float m = 0.0f;
+    for (int64_t i = lane; i < I / 4; i += 32) {
+      const float4 g = __ldg(gp + i), u = __ldg(up + i);
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
+      const __nv_bfloat162 b1 = __floats2bfloat162_rn(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(&b0), w1 = *reinterpret_cast<const uint32_t*>(&b1);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(w0 << 16)), fabsf(__uint_as_float(w0 & 0xFFFF0000u))),
+                         fmaxf(fabsf(__uint_as_float(w1 << 16)), fabsf(__uint_as_float(w1 & 0xFFFF0000u)))));
+      hrow[i] = make_uint2(w0, w1);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const int e = f16_row_exponent(m);
+    const float sc = pow2f(e);
+    __syncwarp();  // the row's bf16 words (written by all lanes) before they are read back
+    for (int64_t i = lane; i < I / 4; i += 32) {
+      const uint2 v = hrow[i];
+      const __half2 h0 = __floats2half2_rn(__fmul_rn(__uint_as_float(v.x << 16), sc),
+                                           __fmul_rn(__uint_as_float(v.x & 0xFFFF0000u), sc));
+      const __half2 h1 = __floats2half2_rn(__fmul_rn(__uint_as_float(v.y << 16), sc),
+                                           __fmul_rn(__uint_as_float(v.y & 0xFFFF0000u), sc));
+      hrow[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    }
+    if (lane == 0) rs[r] = pow2f(-e);
+  }
+}
+
+cudaError_t launch_gather_f16(const void* x_bf16, int64_t H, const int32_t* perm, int R, void* a_f16, float* rs,
+                              cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  return launch_pdl(gather_f16_kernel, grid_for((int64_t)R * 32, 256), 256, 0, st,
+                    static_cast<const __nv_bfloat16*>(x_bf16), H, perm, R, static_cast<__half*>(a_f16), rs);
+}
+
+cudaError_t launch_swiglu_f16(const float* G, int R, int I, void* h_f16, float* rs, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  return launch_pdl(swiglu_f16_kernel, grid_for((int64_t)R * 32, 256), 256, 0, st, G, (int64_t)R, (int64_t)I,
+                    static_cast<__half*>(h_f16), rs);
+}
+
 // Zero fill of a GEMM's fp32 output before its K parts add into it.  An
 // ordinary launch (it starts once the stream's previous work is complete)
 // that lets the GEMM -- a programmatic dependent -- launch as soon as every

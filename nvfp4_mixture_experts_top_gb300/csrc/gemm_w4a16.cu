@@ -1,8 +1,9 @@
 // gemm_w4a16.cu -- ragged grouped GEMM with BF16 activations and NVFP4
 // weights (W4A16): the FP4 weights are dequantised to BF16 inside the kernel
 // and multiplied on the tensor cores with tcgen05.mma kind::f16.  The same
-// kernel, instantiated with FP8 = true, runs the W4A8 mode (FP8 E4M3
-// activations with a per-tensor scale; F16 operands, see the template).
+// kernel runs the W4A8 mode (FP8 E4M3 activations with a per-tensor scale)
+// and the F16-carried W4A16 mode (BF16 rows carried as F16 with per-row
+// powers of two), both on F16 operands; see the template.
 //
 // e2m1 * e4m3 products need at most 6 significant bits and lie in
 // [2^-10, 2688], so the dequantised weight is exact in BF16 and the only
@@ -71,6 +72,7 @@ struct Params {
   const uint8_t* w_scales;
   const float* w_S;
   const uint8_t* a_fp8;  // W4A8: FP8 token codes [R, K] (read by the dequantisation warps)
+  const float* a_rs;     // F16 rows: per-row multipliers 2^-e_r [R]
   const float* a_S;      // W4A8: their per-tensor decode scale
   const int32_t* offsets;
   float* out;
@@ -134,13 +136,21 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);
 }
 
-// FP8 = false: W4A16 (BF16 tokens by TMA, weights dequantised to BF16).
-// FP8 = true: W4A8 -- FP8 E4M3 token codes with a per-tensor scale; weights
-// dequantised to F16 and the tokens converted to F16 (both exact) by the
-// dequantisation warps, which write them into the stage's B area in the
-// 128-byte-swizzled layout the TMA would have produced; MMA kind::f16 with
-// F16 operands; alpha = a_S * w_S[e].
-template <bool FP8>
+// Token operand kinds of the kernel.
+enum { kBF16 = 0, kFP8 = 1, kF16R = 2 };
+// kBF16: W4A16 -- BF16 tokens by TMA, weights dequantised to BF16.
+// kFP8: W4A8 -- FP8 E4M3 token codes with a per-tensor scale; weights
+//   dequantised to F16 and the tokens converted to F16 (both exact) by the
+//   dequantisation warps, which write them into the stage's B area in the
+//   128-byte-swizzled layout the TMA would have produced; alpha = a_S * w_S[e].
+// kF16R: W4A16 with the BF16 rows carried as F16 (row r holds x_r * 2^e_r,
+//   exact for every element within 2^28 of the row's max): F16 tokens by TMA,
+//   weights dequantised to F16 -- cvt + one multiply per pair, where BF16
+//   needs an f16 -> f32 -> bf16 widening as well, which on GB300 made the
+//   BF16 form's stage 1.3x longer -- and out = acc * w_S[e] * 2^-e_r, a power
+//   of two that restores the product exactly.
+// kFP8 and kF16R run MMA kind::f16 with F16 operands.
+template <int AK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                       const Params p) {
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w);
-    if (!FP8) prefetch_tmap(&tm_b);
+    if (AK != kFP8) prefetch_tmap(&tm_b);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, TMEM_COLS);
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       const WorkItem it = item_j(j, w);
       const uint8_t* wsc = p.w_scales + ((size_t)(it.e * NT + it.nt) * (p.K / 64)) * 512;
-      const uint32_t bytes = W_BYTES + WS_BYTES + (FP8 ? 0 : it.ng * NATOM * B_GROUP);
+      const uint32_t bytes = W_BYTES + WS_BYTES + (AK == kFP8 ? 0 : it.ng * NATOM * B_GROUP);
       for (int kc = 0; kc < KCH; ++kc) {
         if (!warp_wait(&raw_empty[stage], phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
@@ -244,7 +254,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ew_arrive_expect_tx(&raw_full[stage], bytes);
         ew_tma_load_2d(sb + OFF_W, &tm_w, &raw_full[stage], kc * (KC / 2), it.e * p.N + it.nt * BM, pol_w);
         ew_bulk_load(sb + OFF_WS, wsc + (size_t)kc * NATOM * 512, WS_BYTES, &raw_full[stage], pol_w);
-        if (!FP8)
+        if (AK != kFP8)
         for (int g = 0; g < it.ng; ++g)
 #pragma unroll
           for (int a = 0; a < NATOM; ++a)
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t smem_base = smem_u32(smem);
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       const int ng = item_j(j, w).ng;
-      const uint32_t idesc = FP8 ? idesc_f16(BM, TG * ng) : idesc_bf16(BM, TG * ng);
+      const uint32_t idesc = AK == kBF16 ? idesc_bf16(BM, TG * ng) : idesc_f16(BM, TG * ng);
       if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
         ok = false;
         break;
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       const WorkItem it = item_j(j, w);
-      const float alpha = FP8 ? __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e)) : __ldg(p.w_S + it.e);
+      const float alpha = AK == kFP8 ? __fmul_rn(__ldg(p.a_S), __ldg(p.w_S + it.e)) : __ldg(p.w_S + it.e);
       const int n = it.nt * BM + q * 32 + lane;
       if (!warp_wait(&acc_full[acc], acc_phase, &abort_flag, p.dev_status)) {
         ok = false;
@@ -344,7 +354,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int tb = it.r0 + g * TG;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (tb + j < it.m1) p.out[(size_t)(tb + j) * p.N + n] = __fmul_rn(__uint_as_float(r[j]), alpha);
+          if (tb + j < it.m1) {
+            // kF16R: alpha * 2^-e_r is exact (a power of two), and so is its product's rounding
+            const float a = AK == kF16R ? __fmul_rn(alpha, __ldg(p.a_rs + tb + j)) : alpha;
+            p.out[(size_t)(tb + j) * p.N + n] = __fmul_rn(__uint_as_float(r[j]), a);
+          }
       }
       tc_fence_before();
       __syncwarp();
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int tg = tt >> 7, tatom = (tt >> 5) & 3, trow = tt & 31;
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
       int t_src = -1;  // global token row this thread converts, or -1
-      if (FP8) {
+      if (AK == kFP8) {
         const WorkItem it = item_j(j, w);
         const int row = it.r0 + tg * TG + trow;
         if (tg < it.ng && row < p.R) t_src = row;
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         if (lane == 0 && warp == 6) W4A16_TRACE(1, it_d);
         uint4 tok[4];  // W4A8: this thread's 64 token codes of the stage, in flight during the dequantisation
-        if (FP8) {
+        if (AK == kFP8) {
           const uint4* src = reinterpret_cast<const uint4*>(p.a_fp8 + (size_t)(t_src < 0 ? 0 : t_src) * p.K +
                                                             kc * KC + tatom * 64);
 #pragma unroll
@@ -409,7 +423,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 4; ++j) {  // 16-element block j
             const __half sh = __float2half_rn(f32_from_e4m3((s4 >> (8 * j)) & 0xFFu));
             const __half2 s2 = __halves2half2(sh, sh);
-            if (FP8) {
+            if (AK != kBF16) {
               dequant8_f16(words[2 * j], s2, outw + 8 * j);
               dequant8_f16(words[2 * j + 1], s2, outw + 8 * j + 4);
             } else {
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tmem_st_32x32b_x32(a_col + 32 * part, outw);
         }
-        if (FP8) {
+        if (AK == kFP8) {
           // the tokens: 64 codes -> 64 f16 = 8 chunks of 16 bytes at chunk
           // c ^ (row & 7) of the row's 128-byte line (128-byte swizzle)
           if (t_src >= 0) {  // other rows of the B area are not read (N = 32 * ng) or not stored
@@ -463,7 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace w4a16
 
-template <bool FP8>
+template <int AK>
 static cudaError_t launch_dequant_gemm(const void* a, const float* a_S, const uint8_t* w_codes,
                                        const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E,
                                        int N, int K, int R, float* out, int32_t* dev_status, cudaStream_t st) {
@@ -471,7 +485,7 @@ static cudaError_t launch_dequant_gemm(const void* a, const float* a_S, const ui
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   {
-    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a16_kernel<FP8>), SMEM_BYTES);
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(gemm_w4a16_kernel<AK>), SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tm_w, tm_b;
@@ -479,18 +493,19 @@ static cudaError_t launch_dequant_gemm(const void* a, const float* a_S, const ui
   cudaError_t err =
       make_tmap_2d_u8(&tm_w, w_codes, (uint64_t)K / 2, (uint64_t)E * N, (uint64_t)K / 2, KC / 2, BM, 128);
   if (err != cudaSuccess) return err;
-  if (FP8) {
+  if (AK == kFP8) {
     tm_b = tm_w;  // not used: the dequantisation warps read the FP8 tokens
   } else {
-    // bf16 tokens viewed as bytes: [R rows, 2K bytes], box 128 B x 32 rows, 128-byte swizzle
+    // bf16 (or f16) tokens viewed as bytes: [R rows, 2K bytes], box 128 B x 32 rows, 128-byte swizzle
     err = make_tmap_2d_u8(&tm_b, a, (uint64_t)K * 2, (uint64_t)R, (uint64_t)K * 2, 128, TG, 128);
     if (err != cudaSuccess) return err;
   }
   Params p;
   p.w_scales = w_scales_packed;
   p.w_S = w_S;
-  p.a_fp8 = FP8 ? static_cast<const uint8_t*>(a) : nullptr;
-  p.a_S = a_S;
+  p.a_fp8 = AK == kFP8 ? static_cast<const uint8_t*>(a) : nullptr;
+  p.a_S = AK == kFP8 ? a_S : nullptr;
+  p.a_rs = AK == kF16R ? a_S : nullptr;
   p.offsets = offsets;
   p.out = out;
   p.dev_status = dev_status;
@@ -499,21 +514,28 @@ static cudaError_t launch_dequant_gemm(const void* a, const float* a_S, const ui
   p.K = K;
   p.R = R;
   p.drop_stage = fault_injection_drop_stage();
-  return launch_pdl(gemm_w4a16_kernel<FP8>, num_sms(), NUM_THREADS, SMEM_BYTES, st, tm_w, tm_b, p);
+  return launch_pdl(gemm_w4a16_kernel<AK>, num_sms(), NUM_THREADS, SMEM_BYTES, st, tm_w, tm_b, p);
 }
 
 cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const uint8_t* w_scales_packed,
                               const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
                               int32_t* dev_status, cudaStream_t st) {
-  return launch_dequant_gemm<false>(a_bf16, nullptr, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
-                                    dev_status, st);
+  return launch_dequant_gemm<w4a16::kBF16>(a_bf16, nullptr, w_codes, w_scales_packed, w_S, offsets, E, N, K, R,
+                                           out, dev_status, st);
 }
 
 cudaError_t launch_gemm_w4a8(const uint8_t* a_fp8, const float* a_S, const uint8_t* w_codes,
                              const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E, int N,
                              int K, int R, float* out, int32_t* dev_status, cudaStream_t st) {
-  return launch_dequant_gemm<true>(a_fp8, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out, dev_status,
-                                   st);
+  return launch_dequant_gemm<w4a16::kFP8>(a_fp8, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                                          dev_status, st);
+}
+
+cudaError_t launch_gemm_w4a16_f16(const void* a_f16, const float* a_rs, const uint8_t* w_codes,
+                                  const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E,
+                                  int N, int K, int R, float* out, int32_t* dev_status, cudaStream_t st) {
+  return launch_dequant_gemm<w4a16::kF16R>(a_f16, a_rs, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
+                                           dev_status, st);
 }
 
 }  // namespace nvfp4moe

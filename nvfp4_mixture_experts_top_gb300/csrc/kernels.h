@@ -48,6 +48,12 @@ cudaError_t launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t co
 cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st);
 cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h, uint8_t* h_codes,
                                   uint8_t* h_scales, void* h_bf16, cudaStream_t st);
+// F16 carrier of BF16 rows: a_f16[r] = x[perm[r] or r] * 2^e_r, rs[r] = 2^-e_r
+// (H % 8 == 0, 16-byte aligned rows); the SwiGLU of W4A16 (h rounded to bf16)
+// carried the same way (I % 4 == 0).
+cudaError_t launch_gather_f16(const void* x_bf16, int64_t H, const int32_t* perm, int R, void* a_f16, float* rs,
+                              cudaStream_t st);
+cudaError_t launch_swiglu_f16(const float* G, int R, int I, void* h_f16, float* rs, cudaStream_t st);
 // out[0, n) = 0 before a GEMM's K parts add into it; the GEMM launched next
 // (a programmatic dependent) may start its prologue during the fill.
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t st);
@@ -97,6 +103,10 @@ cudaError_t launch_gemm_w4a16(const void* a_bf16, const uint8_t* w_codes, const 
                               const float* w_S, const int32_t* offsets, int E, int N, int K, int R, float* out,
                               int32_t* dev_status, cudaStream_t st);
 // W4A8: FP8 E4M3 token codes [R, K] with the per-tensor decode scale *a_S.
+// W4A16 on F16-carried rows: a_f16 [R, K] holds x_r * 2^e_r, a_rs [R] = 2^-e_r.
+cudaError_t launch_gemm_w4a16_f16(const void* a_f16, const float* a_rs, const uint8_t* w_codes,
+                                  const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E,
+                                  int N, int K, int R, float* out, int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_gemm_w4a8(const uint8_t* a_fp8, const float* a_S, const uint8_t* w_codes,
                              const uint8_t* w_scales_packed, const float* w_S, const int32_t* offsets, int E, int N,
                              int K, int R, float* out, int32_t* dev_status, cudaStream_t st);

@@ -62,11 +62,14 @@ def staged(mode, x, logits, cfg, w13, w2, S_h):
         Y = B.moe_grouped_gemm_nvfp4(mode, hc, hs, S_h, *w2, rt["offsets"], H, I)
         d.update(S_x=S_x, hc=hc, hs=hs)
     else:
-        rt = B.moe_align_permute(logits, k, act=x, act_kind=B.MOE_ACT_BF16)
-        G = B.moe_grouped_gemm_nvfp4(mode, rt["act_bf16"], None, None, *w13, rt["offsets"], 2 * I, H)
-        hb = B.moe_swiglu_requant(G, mode)
-        Y = B.moe_grouped_gemm_nvfp4(mode, hb, None, None, *w2, rt["offsets"], H, I)
-        d.update(hb=hb)
+        # W4A16 as moe_layer_forward runs it: the bf16 operands carried as F16
+        # rows (moe_gather_f16, moe_swiglu_f16) into the MOE_W4A16F GEMMs
+        rt = B.moe_align_permute(logits, k)
+        a, a_rs = B.moe_gather_f16(x, rt["perm"])
+        G = B.moe_grouped_gemm_nvfp4(B.MOE_W4A16F, a, None, a_rs, *w13, rt["offsets"], 2 * I, H)
+        hf, h_rs = B.moe_swiglu_f16(G)
+        Y = B.moe_grouped_gemm_nvfp4(B.MOE_W4A16F, hf, None, h_rs, *w2, rt["offsets"], H, I)
+        d.update(hb=(hf.float() * h_rs[:, None]).to(torch.bfloat16))
     out = B.moe_combine(Y, rt["inv"], rt["w"])
     d.update(rt=rt, G=G, Y=Y, out=out)
     return d
