@@ -15,7 +15,8 @@
 //               packed scales (2 KB), token tiles [32 rows][64 bf16] per group
 //               and 64-element atom (128-byte swizzle)
 //  warps 6-13   dequantise: warp (quarter q, half h) turns rows 32q..32q+31,
-//               K elements 128h..128h+127 of the stage into BF16 and writes them
+//               K elements 128h..128h+127 of the stage into BF16 (F16 for the
+//               F16-operand forms) and writes them
 //               straight into tensor memory (tcgen05.st), where the MMA reads
 //               its A operand -- no shared-memory round trip for the 4x larger
 //               BF16 tile
@@ -41,8 +42,12 @@ constexpr int BM = 128;
 constexpr int KC = 256;     // K elements per stage
 constexpr int TG = 32;
 constexpr int MAXG = 2;     // token groups per pass
-constexpr int RSTAGES = 4;  // raw stages
+// Raw stages and dequantised-operand slots in TMEM pair up one to one, so
+// that one commit of the MMAs of a stage frees both the raw stage and its
+// slot (a second commit per stage cost ~15% of the stage time on GB300).
+constexpr int RSTAGES = 3;  // raw stages
 constexpr int ASLOTS = 3;   // dequantised operand slots in TMEM (dequantisation runs ahead of the MMAs)
+static_assert(RSTAGES == ASLOTS, "stage s uses slot s");
 constexpr int TOK_PER_PASS = TG * MAXG;
 
 constexpr uint32_t B_GROUP = TG * 128;              // 4096: one group's 64-element atom
@@ -156,9 +161,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[RSTAGES];
-  __shared__ __align__(8) uint64_t raw_empty[RSTAGES];
+  __shared__ __align__(8) uint64_t consumed[RSTAGES];  // the MMAs of stage s completed: raw stage and slot free
   __shared__ __align__(8) uint64_t a_full[ASLOTS];
-  __shared__ __align__(8) uint64_t a_empty[ASLOTS];
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -176,11 +180,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RSTAGES; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], NUM_DEQ_WARPS + 1);  // dequant warps + MMA commit
-    }
-    for (int s = 0; s < ASLOTS; ++s) {
+      mbar_init(&consumed[s], 1);  // the MMA warp's commit
       mbar_init(&a_full[s], NUM_DEQ_WARPS);
-      mbar_init(&a_empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint8_t* wsc = p.w_scales + ((size_t)(it.e * NT + it.nt) * (p.K / 64)) * 512;
       const uint32_t bytes = W_BYTES + WS_BYTES + (AK == kFP8 ? 0 : it.ng * NATOM * B_GROUP);
       for (int kc = 0; kc < KCH; ++kc) {
-        if (!warp_wait(&raw_empty[stage], phase ^ 1, &abort_flag, p.dev_status)) {
+        if (!warp_wait(&consumed[stage], phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
@@ -310,8 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ew_mma_bf16_ts(d_col, a_col + 8 * kk, bdesc, idesc, (kc | kk) != 0);
         }
         if (lane == 0) W4A16_TRACE(4, it_m);
-        ew_commit(&a_empty[slot]);
-        ew_commit(&raw_empty[stage]);
+        ew_commit(&consumed[stage]);
         ++it_m;
         if (++slot == ASLOTS) {
           slot = 0;
@@ -390,8 +390,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (tg < it.ng && row < p.R) t_src = row;
       }
       for (int kc = 0; kc < KCH; ++kc) {
-        if (!warp_wait(&raw_full[stage], phase, &abort_flag, p.dev_status) ||
-            !warp_wait(&a_empty[slot], slot_phase ^ 1, &abort_flag, p.dev_status)) {
+        // raw_full of this fill implies the slot is free: the producer refills
+        // stage s only after the MMAs that read slot s have completed
+        if (!warp_wait(&raw_full[stage], phase, &abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
@@ -454,7 +455,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         ew_arrive(&a_full[slot]);
-        ew_arrive(&raw_empty[stage]);
         ++it_d;
         if (++slot == ASLOTS) {
           slot = 0;
