@@ -579,33 +579,45 @@ __device__ __forceinline__ int f16_row_exponent(float amax) {
 }
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 
-// One warp per output row: a_f16[r] = x[src] * 2^e_r, rs[r] = 2^-e_r, with
-// src = perm[r] (or r).  Two passes over the row (max, then convert); the
-// second reads it from L1/L2.
+// The largest value of v over the block (256 threads), in every thread.
+__device__ __forceinline__ float block_max256(float v) {
+  __shared__ float red[8];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  __syncthreads();  // red[] of a previous call has been read
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) v = fmaxf(v, red[i]);
+  return v;
+}
+
+// One 256-thread block per output row: a_f16[r] = x[src] * 2^e_r, rs[r] =
+// 2^-e_r, with src = perm[r] (or r).  Two passes over the row (max, then
+// convert); the second reads it from L1/L2.  (A warp per row left most SMs
+// idle at decode sizes: 128 rows.)
 __global__ void __launch_bounds__(256) gather_f16_kernel(const __nv_bfloat16* __restrict__ x, int64_t H,
                                                          const int32_t* __restrict__ perm, int R,
                                                          __half* __restrict__ a, float* __restrict__ rs) {
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
+  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
     const int64_t t = perm != nullptr ? (int64_t)__ldg(perm + r) : r;
     const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
     float m = 0.0f;
-    for (int64_t i = lane; i < H / 8; i += 32) {
+    for (int64_t i = threadIdx.x; i < H / 8; i += blockDim.x) {
       const uint4 u = __ldg(src + i);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    m = block_max256(m);
     const int e = f16_row_exponent(m);
     const float sc = pow2f(e);
     uint4* dst = reinterpret_cast<uint4*>(a + r * H);
-    for (int64_t i = lane; i < H / 8; i += 32) {
+    for (int64_t i = threadIdx.x; i < H / 8; i += blockDim.x) {
       const uint4 u = __ldg(src + i);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
       uint32_t o4[4];
@@ -617,26 +629,25 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(const __nv_bfloat16* __
       }
       dst[i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
     }
-    if (lane == 0) rs[r] = pow2f(-e);
+    if (threadIdx.x == 0) rs[r] = pow2f(-e);
   }
 }
 
-// One warp per row r of G [R, 2I] (gate | up): h = bf16(silu(g) * u) -- the
-// W4A16 activation of the down GEMM -- carried as f16(h * 2^e_r), rs[r] =
-// 2^-e_r.  The bf16 values are written first (as 16-bit words into the f16
-// buffer) with the row's max taken on the way, then converted in place.
+// One 256-thread block per row r of G [R, 2I] (gate | up): h = bf16(silu(g)
+// * u) -- the W4A16 activation of the down GEMM -- carried as f16(h * 2^e_r),
+// rs[r] = 2^-e_r.  The bf16 values are written first (as 16-bit words into
+// the f16 buffer) with the row's max taken on the way, then converted in
+// place by the thread that wrote them.
 __global__ void __launch_bounds__(256) swiglu_f16_kernel(const float* __restrict__ G, int64_t R, int64_t I,
                                                          __half* __restrict__ h, float* __restrict__ rs) {
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
+  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
     const float4* gp = reinterpret_cast<const float4*>(G + r * 2 * I);
     const float4* up = reinterpret_cast<const float4*>(G + r * 2 * I + I);
     uint2* hrow = reinterpret_cast<uint2*>(h + r * I);
     float m = 0.0f;
-    for (int64_t i = lane; i < I / 4; i += 32) {
+    for (int64_t i = threadIdx.x; i < I / 4; i += blockDim.x) {
       const float4 g = __ldg(gp + i), u = __ldg(up + i);
       const __nv_bfloat162 b0 = __floats2bfloat162_rn(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
       const __nv_bfloat162 b1 = __floats2bfloat162_rn(silu_mul(g.z, u.z), silu_mul(g.w, u.w));
@@ -645,12 +656,10 @@ __global__ void __launch_bounds__(256) swiglu_f16_kernel(const float* __restrict
                          fmaxf(fabsf(__uint_as_float(w1 << 16)), fabsf(__uint_as_float(w1 & 0xFFFF0000u)))));
       hrow[i] = make_uint2(w0, w1);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    m = block_max256(m);  // then each thread converts the words it wrote
     const int e = f16_row_exponent(m);
     const float sc = pow2f(e);
-    __syncwarp();  // the row's bf16 words (written by all lanes) before they are read back
-    for (int64_t i = lane; i < I / 4; i += 32) {
+    for (int64_t i = threadIdx.x; i < I / 4; i += blockDim.x) {
       const uint2 v = hrow[i];
       const __half2 h0 = __floats2half2_rn(__fmul_rn(__uint_as_float(v.x << 16), sc),
                                            __fmul_rn(__uint_as_float(v.x & 0xFFFF0000u), sc));
@@ -658,20 +667,20 @@ __global__ void __launch_bounds__(256) swiglu_f16_kernel(const float* __restrict
                                            __fmul_rn(__uint_as_float(v.y & 0xFFFF0000u), sc));
       hrow[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
     }
-    if (lane == 0) rs[r] = pow2f(-e);
+    if (threadIdx.x == 0) rs[r] = pow2f(-e);
   }
 }
 
 cudaError_t launch_gather_f16(const void* x_bf16, int64_t H, const int32_t* perm, int R, void* a_f16, float* rs,
                               cudaStream_t st) {
   if (R == 0) return cudaSuccess;
-  return launch_pdl(gather_f16_kernel, grid_for((int64_t)R * 32, 256), 256, 0, st,
+  return launch_pdl(gather_f16_kernel, R < 8 * num_sms() ? R : 8 * num_sms(), 256, 0, st,
                     static_cast<const __nv_bfloat16*>(x_bf16), H, perm, R, static_cast<__half*>(a_f16), rs);
 }
 
 cudaError_t launch_swiglu_f16(const float* G, int R, int I, void* h_f16, float* rs, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
-  return launch_pdl(swiglu_f16_kernel, grid_for((int64_t)R * 32, 256), 256, 0, st, G, (int64_t)R, (int64_t)I,
+  return launch_pdl(swiglu_f16_kernel, R < 8 * num_sms() ? R : 8 * num_sms(), 256, 0, st, G, (int64_t)R, (int64_t)I,
                     static_cast<__half*>(h_f16), rs);
 }
 
