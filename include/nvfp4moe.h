@@ -463,11 +463,12 @@ int moe_layer_forward_host(int mode, const void* x_host, const float* logits_hos
  * library's own device memory: it allocates nothing and calls no allocating
  * routine.
  *   - Limit: a call needs 256 + 4 * B * E + 4 * B bytes of scratch (each
- *     term after the first rounded up to 256), B = ceil(T / 32) thread
- *     blocks of routing, times 4 for 33 <= T <= 256 (eight tokens per block
- *     there); a larger problem (e.g. T > 4064 tokens at E = 1024 experts,
- *     T > 32480 at E = 128) is refused with NVFP4_E_WORKSPACE before
- *     anything is launched.
+ *     term after the first rounded up to 256), B = ceil(T / 32); a larger
+ *     problem (e.g. T > 4064 tokens at E = 1024 experts, T > 32480 at
+ *     E = 128) is refused with NVFP4_E_WORKSPACE before anything is
+ *     launched.  (Where the array holds four times that, routing runs in
+ *     blocks of eight tokens as moe_align_permute does from 33 tokens;
+ *     otherwise in blocks of 32: the results are the same.)
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current), and so does the first call
  *     after a device reset (cudaDeviceReset destroys the context, and the

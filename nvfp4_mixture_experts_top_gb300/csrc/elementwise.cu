@@ -278,55 +278,78 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
 // inv comes from the caller: a row outside [0, T*k) contributes nothing and
 // is reported as NVFP4_E_BAD_ROUTING (never read).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ Y, const int32_t* __restrict__ inv,
-                                                      const float* __restrict__ w, int T, int k, int64_t H,
+                                                      const float* __restrict__ w, int T, int k, int64_t H, int cs,
                                                       int out_dtype, void* __restrict__ out, int32_t* dev_status) {
+  // block b: token b / cs, the (b % cs)-th of cs column ranges of its row.
+  // The token's k row indices and weights are read once per block into
+  // shared memory (a row outside [0, T*k) is marked -1); each thread then
+  // keeps the k row loads of two float4 columns in flight.
+  __shared__ int64_t s_r[32];
+  __shared__ float s_w[32];
   pdl_wait();
   pdl_trigger();
   const int64_t q_per_row = H / 4;
-  const int64_t total = (int64_t)T * q_per_row;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / q_per_row, c = (i % q_per_row) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // the k rows in chunks of 8: the row indices, then the 8 row loads, are
-    // issued together (one or two dependent round trips instead of k); the
-    // sum still runs in j order
-    constexpr int kU = 8;
-    const uint32_t R = (uint32_t)T * (uint32_t)k;
-    for (int j0 = 0; j0 < k; j0 += kU) {
-      int64_t r[kU];
-      float wj[kU];
-      float4 y[kU];
-      bool ok[kU];
+  const int64_t chunk = (q_per_row + cs - 1) / cs;
+  const uint32_t R = (uint32_t)T * (uint32_t)k;
+  for (int64_t b = blockIdx.x; b < (int64_t)T * cs; b += gridDim.x) {
+    const int64_t t = b / cs;
+    const int64_t q0 = (b % cs) * chunk, q1 = min(q_per_row, q0 + chunk);
+    __syncthreads();  // the previous token's s_r / s_w have been read
+    if (threadIdx.x < k) {
+      const int32_t rr = __ldg(inv + t * k + threadIdx.x);
+      const bool ok = (uint32_t)rr < R;
+      if (!ok) report_status(dev_status, NVFP4_E_BAD_ROUTING);
+      s_r[threadIdx.x] = ok ? (int64_t)rr * H : -1;
+      s_w[threadIdx.x] = __ldg(w + t * k + threadIdx.x);
+    }
+    __syncthreads();
+    for (int64_t q = q0 + threadIdx.x; q < q1; q += 2 * (int64_t)blockDim.x) {
+      const int64_t c0 = q * 4, c1 = (q + blockDim.x) * 4;
+      const bool two = q + blockDim.x < q1;
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+      // rows in chunks of 8 (loads issued together; the sum runs in j order)
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        float4 y0[8], y1[8];
 #pragma unroll
-      for (int j = 0; j < kU; ++j) {
-        const int32_t rr = (j0 + j < k) ? __ldg(inv + t * k + j0 + j) : 0;
-        ok[j] = (j0 + j < k) && (uint32_t)rr < R;
-        if (j0 + j < k && !ok[j]) report_status(dev_status, NVFP4_E_BAD_ROUTING);
-        r[j] = ok[j] ? rr : 0;
-        wj[j] = (j0 + j < k) ? __ldg(w + t * k + j0 + j) : 0.0f;
-      }
+        for (int j = 0; j < 8; ++j) {
+          const int64_t r = (j0 + j < k) ? s_r[j0 + j] : -1;
+          if (r >= 0) {
+            y0[j] = __ldg(reinterpret_cast<const float4*>(Y + r + c0));
+            if (two) y1[j] = __ldg(reinterpret_cast<const float4*>(Y + r + c1));
+          }
+        }
 #pragma unroll
-      for (int j = 0; j < kU; ++j)
-        if (ok[j]) y[j] = __ldg(reinterpret_cast<const float4*>(Y + r[j] * H + c));
-#pragma unroll
-      for (int j = 0; j < kU; ++j) {
-        if (ok[j]) {
-          acc.x = __fadd_rn(acc.x, __fmul_rn(wj[j], y[j].x));
-          acc.y = __fadd_rn(acc.y, __fmul_rn(wj[j], y[j].y));
-          acc.z = __fadd_rn(acc.z, __fmul_rn(wj[j], y[j].z));
-          acc.w = __fadd_rn(acc.w, __fmul_rn(wj[j], y[j].w));
+        for (int j = 0; j < 8; ++j) {
+          const int64_t r = (j0 + j < k) ? s_r[j0 + j] : -1;
+          if (r >= 0) {
+            const float wj = s_w[j0 + j];
+            a0.x = __fadd_rn(a0.x, __fmul_rn(wj, y0[j].x));
+            a0.y = __fadd_rn(a0.y, __fmul_rn(wj, y0[j].y));
+            a0.z = __fadd_rn(a0.z, __fmul_rn(wj, y0[j].z));
+            a0.w = __fadd_rn(a0.w, __fmul_rn(wj, y0[j].w));
+            if (two) {
+              a1.x = __fadd_rn(a1.x, __fmul_rn(wj, y1[j].x));
+              a1.y = __fadd_rn(a1.y, __fmul_rn(wj, y1[j].y));
+              a1.z = __fadd_rn(a1.z, __fmul_rn(wj, y1[j].z));
+              a1.w = __fadd_rn(a1.w, __fmul_rn(wj, y1[j].w));
+            }
+          }
         }
       }
-    }
-    if (out_dtype == NVFP4_DT_F32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c) = acc;
-    } else {
-      const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 v;
-      v.x = *reinterpret_cast<const uint32_t*>(&a);
-      v.y = *reinterpret_cast<const uint32_t*>(&b);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + t * H + c) = v;
+      for (int u = 0; u < (two ? 2 : 1); ++u) {
+        const float4 acc = u ? a1 : a0;
+        const int64_t c = u ? c1 : c0;
+        if (out_dtype == NVFP4_DT_F32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c) = acc;
+        } else {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 v;
+          v.x = *reinterpret_cast<const uint32_t*>(&lo);
+          v.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + t * H + c) = v;
+        }
+      }
     }
   }
 }
@@ -714,7 +737,15 @@ cudaError_t launch_combine(const float* Y, const int32_t* inv, const float* w, i
                            void* out, int32_t* dev_status, cudaStream_t st) {
   const int64_t total = (int64_t)T * (H / 4);
   if (total == 0) return cudaSuccess;
-  return launch_pdl(combine_kernel, grid_for(total, 256), 256, 0, st, Y, inv, w, T, k, (int64_t)H, out_dtype, out,
+  // column ranges per token so that small batches still cover the SMs twice
+  // over, each range at least one float4 column per thread (256)
+  const int64_t q_per_row = H / 4;
+  const int64_t cs_max = q_per_row / 256 > 0 ? q_per_row / 256 : 1;
+  int64_t cs = (2 * (int64_t)num_sms() + T - 1) / T;
+  cs = cs < 1 ? 1 : (cs > cs_max ? cs_max : cs);
+  const int64_t blocks = (int64_t)T * cs;
+  const int grid = (int)(blocks < 8 * (int64_t)num_sms() ? blocks : 8 * (int64_t)num_sms());
+  return launch_pdl(combine_kernel, grid, 256, 0, st, Y, inv, w, T, k, (int64_t)H, (int)cs, out_dtype, out,
                     dev_status);
 }
 

@@ -66,13 +66,16 @@ cudaError_t launch_stage_in(const void* src16, void* dst16, int64_t bytes16, con
                             int64_t bytes4, cudaStream_t st);
 
 // Routing: top-k + stable counting sort + optional gather.  ws must hold
-// route_workspace_bytes(T, E).
+// route_workspace_bytes(T, E) -- or, when ws_bytes says it holds less, at
+// least route_workspace_min_bytes(T, E) (routing then runs in blocks of 32
+// tokens, the layout with the smallest scratch).
 size_t route_workspace_bytes(int T, int E);
+size_t route_workspace_min_bytes(int T, int E);
 // Routing alone; with x_bf16 != NULL it also leaves amax(|x|) ([T, H] bf16)
 // as fp32 bits in the second word of ws (for nvfp4 quantisation).
 cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dev_status, void* ws,
-                              cudaStream_t st, const void* x_bf16, int64_t H);
+                              cudaStream_t st, const void* x_bf16, int64_t H, size_t ws_bytes = (size_t)-1);
 cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* act_in, const uint8_t* act_in_scales,
                           int64_t act_cols, void* act_out, uint8_t* act_out_scales, cudaStream_t st);
 // Quantise x [T, H] bf16 with S = amax/2688 (amax bits from the routing
@@ -84,7 +87,7 @@ cudaError_t launch_quantize_scatter(const void* x_bf16, int T, int H, int k, con
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
                          const uint8_t* act_in_scales, int64_t act_cols, void* act_out, uint8_t* act_out_scales,
-                         int32_t* dev_status, void* ws, cudaStream_t st);
+                         int32_t* dev_status, void* ws, cudaStream_t st, size_t ws_bytes = (size_t)-1);
 
 // Grouped GEMMs.  Return cudaSuccess or the launch/setup error; host-side
 // argument checks happen before these are called.

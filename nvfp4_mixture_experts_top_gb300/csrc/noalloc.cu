@@ -109,7 +109,7 @@ extern "C" int moe_align_permute_noalloc(const float* logits, int T, int E, int 
   if (expert_offsets == nullptr) return NVFP4_E_INVAL;
   if (act_kind != MOE_ACT_NONE && act_kind != MOE_ACT_NVFP4 && act_kind != MOE_ACT_BF16) return NVFP4_E_INVAL;
   // the fixed scratch must hold this problem, otherwise refuse before any work
-  if (route_workspace_bytes(T, E) > (size_t)NVFP4MOE_NOALLOC_SCRATCH_BYTES) return NVFP4_E_WORKSPACE;
+  if (route_workspace_min_bytes(T, E) > (size_t)NVFP4MOE_NOALLOC_SCRATCH_BYTES) return NVFP4_E_WORKSPACE;
   if (T > 0) {
     if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr || perm == nullptr || inv == nullptr)
       return NVFP4_E_INVAL;
@@ -134,6 +134,6 @@ extern "C" int moe_align_permute_noalloc(const float* logits, int T, int E, int 
   if (s != NVFP4_OK) return s;
   const cudaError_t e = launch_route(logits, T, E, k, topk_ids, topk_w, expert_offsets, perm, inv, act_kind,
                                      act_in, act_in_scales, act_cols, act_out, act_out_scales, dev_status, scratch,
-                                     reinterpret_cast<cudaStream_t>(stream));
+                                     reinterpret_cast<cudaStream_t>(stream), (size_t)NVFP4MOE_NOALLOC_SCRATCH_BYTES);
   return e == cudaSuccess ? NVFP4_OK : NVFP4_E_CUDA;
 }

@@ -2,7 +2,7 @@
 // plus the gather of activation rows into permuted order.
 //
 // route_kernel: one warp per token; one CTA per chunk of 32 tokens, or, for
-// up to 8 chunks, four CTAs of 8 tokens per chunk (see route_subs).
+// up to 76 chunks, four CTAs of 8 tokens per chunk (see route_subs).
 //  1. top-k: the token's logits sit in registers (E/32 per lane, a
 //     compile-time count); k rounds of a warp-shuffle arg-max (ties to the
 //     lower expert id) give the experts in descending logit order; the weights
@@ -35,18 +35,24 @@ constexpr int kChunk = 32;
 constexpr size_t kPlaceSmemMax = 192 * 1024;
 
 // CTAs per 32-token chunk in the multi-chunk launch: four CTAs of eight
-// tokens while there are at most 8 chunks (T <= 256), so that the top-k --
-// k shuffle rounds per token, up to 22 rounds over 512 experts at the wide
-// workload -- runs on four times as many SMs; one CTA of 32 tokens beyond.
-static int route_subs(int C) { return C > 1 && C <= 8 ? 4 : 1; }
+// tokens while that stays within two per SM (up to 76 chunks, T <= 2432), so
+// that the top-k -- k shuffle rounds per token, up to 22 rounds over 512
+// experts at the wide workload -- and the activation amax (a 12 KB row per
+// token at H = 6144) run on four times as many SMs; one CTA of 32 tokens
+// beyond.
+static int route_subs(int C) { return C > 1 && C <= 76 ? 4 : 1; }
 
 // Scratch layout: [0, 256) the activation amax in word 1; then one mask per
 // (CTA, expert) [C * subs][E] u32; then per-CTA activation amax [C * subs].
-size_t route_workspace_bytes(int T, int E) {
-  const size_t C = (size_t)(T + kChunk - 1) / kChunk;
-  const size_t CS = C * (size_t)route_subs((int)C);
+static size_t route_ws_for(int C, int E, int subs) {
+  const size_t CS = (size_t)C * (size_t)subs;
   return 256 + ((CS * (size_t)E * 4 + 255) & ~(size_t)255) + ((CS * 4 + 255) & ~(size_t)255);
 }
+size_t route_workspace_bytes(int T, int E) {
+  const int C = (T + kChunk - 1) / kChunk;
+  return route_ws_for(C, E, route_subs(C));
+}
+size_t route_workspace_min_bytes(int T, int E) { return route_ws_for((T + kChunk - 1) / kChunk, E, 1); }
 
 // Chunk cc's mask of expert e: the OR of its `subs` CTAs' masks.
 __device__ __forceinline__ uint32_t chunk_mask(const uint32_t* masks, int subs, int cc, int E, int e) {
@@ -345,10 +351,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
 
 cudaError_t launch_route_only(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dev_status, void* ws,
-                              cudaStream_t st, const void* x_bf16, int64_t H) {
+                              cudaStream_t st, const void* x_bf16, int64_t H, size_t ws_bytes) {
   if (T == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st);
   const int C = (T + kChunk - 1) / kChunk;
-  const int subs = route_subs(C);
+  // four blocks per chunk where the scratch holds their masks, else one
+  int subs = route_subs(C);
+  if (subs > 1 && route_ws_for(C, E, subs) > ws_bytes) subs = 1;
   uint32_t* amax = static_cast<uint32_t*>(ws) + 1;  // word 1: activation amax
   uint32_t* masks = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256);
   uint32_t* amax_part = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 256 +
@@ -395,9 +403,9 @@ cudaError_t launch_gather(const int32_t* perm, int R, int act_kind, const void* 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int act_kind, const void* act_in,
                          const uint8_t* act_in_scales, int64_t act_cols, void* act_out, uint8_t* act_out_scales,
-                         int32_t* dev_status, void* ws, cudaStream_t st) {
-  cudaError_t e =
-      launch_route_only(logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, dev_status, ws, st, nullptr, 0);
+                         int32_t* dev_status, void* ws, cudaStream_t st, size_t ws_bytes) {
+  cudaError_t e = launch_route_only(logits, T, E, k, topk_ids, topk_w, offsets, perm, inv, dev_status, ws, st,
+                                    nullptr, 0, ws_bytes);
   if (e != cudaSuccess) return e;
   return launch_gather(perm, T * k, act_kind, act_in, act_in_scales, act_cols, act_out, act_out_scales, st);
 }

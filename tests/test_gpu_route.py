@@ -35,10 +35,10 @@ def test_route_workloads(orc, name):
     _check(orc, wl.router_logits(cfg).numpy(), cfg.k, dev)
 
 
-# 33..256 tokens route in blocks of eight tokens (four per 32-token chunk);
-# 256 and 257 sit on either side of that switch
+# 33..2432 tokens route in blocks of eight tokens (four per 32-token chunk);
+# 2432 and 2433 sit on either side of that switch
 @pytest.mark.parametrize("T,E,k", [(1, 8, 1), (33, 64, 8), (65, 1024, 32), (100, 7, 7), (31, 40, 3),
-                                   (256, 128, 8), (257, 96, 4)])
+                                   (2432, 128, 8), (2433, 96, 4)])
 def test_route_ragged_shapes(orc, T, E, k):
     dev = cuda_or_skip()
     logits = wl.random_fp32((T, E), seed=T * 1000 + E, tag="logits").numpy()

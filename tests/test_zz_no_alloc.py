@@ -9,7 +9,9 @@ a row, each over the previous call's leftovers in the shared fixed scratch
 (which is never cleared between calls): decode_b512 twice (16 routing chunks
 of 32 tokens), then wide (2 chunks, 512 experts: its masks land on top of the
 previous call's), then decode_c16 (one chunk).  decode_b512 is also compared
-with the oracle directly.  The file is named so that pytest collects it last.
+with the oracle directly.  A problem whose eight-token routing blocks would
+not fit the fixed scratch (1500 tokens, 1024 experts) routes in blocks of 32
+there and still matches.  The file is named so that pytest collects it last.
 """
 import ctypes as C
 
@@ -97,3 +99,30 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     xc = torch.zeros(T, 128, dtype=torch.uint8, device=dev)
     xs = torch.zeros(T, 16, dtype=torch.uint8, device=dev)
     assert _call(True, logits, k, xc, xs, out) == 4  # NVFP4_E_WORKSPACE, nothing launched
+
+
+def test_noalloc_routes_in_32_token_blocks_when_the_scratch_is_short(orc):
+    """T = 1500, E = 1024: moe_align_permute routes in blocks of eight tokens,
+    whose masks (4 * 47 blocks * 1024 experts * 4 B) would not fit the fixed
+    scratch; the no-allocation entry point falls back to blocks of 32 tokens
+    (47 * 1024 * 4 B) and must give the same routing and rows."""
+    dev = cuda_or_skip()
+    T, E, k, H = 1500, 1024, 8, 256
+    nb = (T + 31) // 32
+    assert 256 + 4 * 4 * nb * E > SCRATCH_LIMIT and 256 + 4 * nb * E + 4 * nb + 512 <= SCRATCH_LIMIT
+    cfg = wl.MoEConfig("noalloc_fallback", T=T, H=H, I=256, E=E, k=k, routing="uniform")
+    logits = wl.router_logits(cfg, seed=9, device=dev)
+    x = wl.activations_bf16(T, H, seed=9, device=dev)
+    xc, xs, _ = B.nvfp4_quantize(x)
+    ref = _outputs(T, E, k, H, dev)
+    got = _outputs(T, E, k, H, dev)
+    assert _call(False, logits, k, xc, xs, ref) == 0
+    assert _call(True, logits, k, xc, xs, got) == 0
+    torch.cuda.synchronize()
+    for key in ("ids", "offsets", "perm", "inv", "codes", "scales", "status"):
+        assert torch.equal(got[key], ref[key]), key
+    assert torch.allclose(got["w"], ref["w"], rtol=1e-6, atol=0)
+    ids, w = orc.route(logits.cpu().numpy(), k)
+    offsets, perm, inv = orc.permute(ids, E)
+    assert np.array_equal(got["perm"].cpu().numpy(), perm)
+    assert np.array_equal(got["offsets"].cpu().numpy(), offsets)
