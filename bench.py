@@ -530,17 +530,20 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
             chk(L.moe_grouped_gemm_nvfp4(2, P(h_c), P(h_s), None, P(w2[0]), P(w2[1]), None, P(offs),
                                          cfg.E, H, I, R, P(Y), P(status), st))
         elif mode == B.MOE_W4A8:
-            # routing + FP8 quantisation straight into permuted rows
-            chk(L.moe_route_quantize_fp8(P(x), P(logits), T, H, cfg.E, k, P(ids), P(tw), P(offs), P(perm),
-                                         P(inv), P(S_x), P(a_c), P(status), P(ws_route), ws_route.numel(), st))
+            # as moe_layer_forward runs it: routing + FP8 quantisation straight
+            # into permuted rows, the codes carried as their f16 values into
+            # the F16-operand GEMM (MOE_W4A16F)
+            chk(L.moe_route_quantize_fp8_f16(P(x), P(logits), T, H, cfg.E, k, P(ids), P(tw), P(offs), P(perm),
+                                             P(inv), P(S_x), P(a_b), P(a_rs), P(status), P(ws_route),
+                                             ws_route.numel(), st))
             if ev_pair:
                 ev_pair[0].record()
-            chk(L.moe_grouped_gemm_nvfp4(3, P(a_c), None, P(S_x), P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
+            chk(L.moe_grouped_gemm_nvfp4(4, P(a_b), None, P(a_rs), P(w13[0]), P(w13[1]), P(w13[2]), P(offs),
                                          cfg.E, 2 * I, H, R, P(G), P(status), st))
             if ev_pair:
                 ev_pair[1].record()
-            chk(L.moe_swiglu_requant(P(G), R, I, 3, P(S_h), P(h_c), None, None, st))
-            chk(L.moe_grouped_gemm_nvfp4(3, P(h_c), None, P(S_h), P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
+            chk(L.moe_swiglu_fp8_f16(P(G), R, I, P(S_h), P(h_b), P(h_rs), st))
+            chk(L.moe_grouped_gemm_nvfp4(4, P(h_b), None, P(h_rs), P(w2[0]), P(w2[1]), P(w2[2]), P(offs),
                                          cfg.E, H, I, R, P(Y), P(status), st))
         elif mode == B.MOE_W4A4:
             # routing + activation quantisation straight into permuted rows
@@ -602,7 +605,7 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
     touched = int((counts > 0).sum())
     w13_bytes = touched * 2 * I * H * bpe
     w2_bytes = touched * H * I * bpe
-    act_in = R * H * {B.MOE_W4A16: 2.0, B.MOE_W4A8: 1.0}.get(mode, bpe)
+    act_in = R * H * {B.MOE_W4A16: 2.0, B.MOE_W4A8: 2.0}.get(mode, bpe)  # both carried as f16 rows
     gemm1_bytes = w13_bytes + act_in + R * 2 * I * 4
     layer_weight_bytes = w13_bytes + w2_bytes
 
@@ -709,7 +712,7 @@ def measure_layer(args, cfg, mode_name, metric, world, rank, local, full=True, n
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {B.MOE_W4A4: "fp4(e2m1)xfp4, fp32 accumulate", B.MOE_W4A16: "fp4(e2m1)xbf16 (carried as f16 rows), fp32 accumulate",
                   B.MOE_MXW4A4: "fp4(e2m1)xfp4 (UE8M0 scales), fp32 accumulate",
-                  B.MOE_W4A8: "fp4(e2m1)xfp8(e4m3) on f16 operands, fp32 accumulate"}[mode],
+                  B.MOE_W4A8: "fp4(e2m1)xfp8(e4m3) (codes carried as f16 values), fp32 accumulate"}[mode],
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised on the GPU)",
         "config": {"workload": cfg.name, "mode": mode_name, "T": T, "hidden": H, "intermediate": I,
                    "experts": cfg.E, "top_k": k, "routing": cfg.routing, "touched_experts": touched,

@@ -284,6 +284,17 @@ int moe_route_quantize_fp8(const void* x, const float* logits, int T, int H, int
                            uint8_t* a_codes, int32_t* dev_status, void* workspace, size_t workspace_bytes,
                            nvfp4_stream_t stream);
 
+/* moe_route_quantize_fp8_f16 -- moe_route_quantize_fp8 with every FP8 code
+ * written as its value in f16 (E4M3 values are f16 values: exact) for the
+ * MOE_W4A16F GEMM: a_f16 [T*k, H] holds e4m3(code), a_rs [T*k] holds S_x for
+ * every row, so that GEMM forms exactly the MOE_W4A8 products.  The layer's
+ * W4A8 path runs this form.  S_x, routing outputs and constraints as
+ * moe_route_quantize_fp8. */
+int moe_route_quantize_fp8_f16(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                               float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, float* S_x,
+                               void* a_f16, float* a_rs, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                               nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * moe_grouped_gemm_nvfp4 -- ragged grouped GEMM over experts.
  * "The 2x Gap", sections "The Investigation So Far" and "Discovering the
@@ -353,6 +364,13 @@ int moe_gather_f16(const void* x, int T, int H, const int32_t* perm, int R, void
  * Constraints: I % 16 == 0; G and h_f16 16-byte aligned. */
 int moe_swiglu_f16(const float* G, int R, int I, void* h_f16, float* h_rs, nvfp4_stream_t stream);
 
+/* moe_swiglu_fp8_f16 -- the W4A8 SwiGLU (as moe_swiglu_requant with MOE_W4A8:
+ * FP8 codes of h with the static decode scale *S_h) with every code written
+ * as its f16 value for the MOE_W4A16F GEMM: h_f16 [R, I], h_rs[r] = *S_h.
+ * Constraints: I % 16 == 0; G and h_f16 16-byte aligned. */
+int moe_swiglu_fp8_f16(const float* G, int R, int I, const float* S_h, void* h_f16, float* h_rs,
+                       nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * moe_swiglu_requant -- SwiGLU on the gate_up output and requantisation.
  * Defined by the layer this library implements -- gate_up, then SwiGLU,
@@ -402,7 +420,9 @@ int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, 
  * can be captured in a CUDA graph.
  *   mode        MOE_W4A4, MOE_W4A16, MOE_MXW4A4 or MOE_W4A8 (MOE_W4A16 runs
  *               moe_gather_f16, MOE_W4A16F GEMMs and moe_swiglu_f16: the
- *               W4A16 products, with the bf16 operands carried as F16 rows)
+ *               W4A16 products, with the bf16 operands carried as F16 rows;
+ *               MOE_W4A8 runs moe_route_quantize_fp8_f16, MOE_W4A16F GEMMs
+ *               and moe_swiglu_fp8_f16: the W4A8 products)
  *   x           bf16 [T, H]; logits fp32 [T, E]
  *   w13_*       gate_up weights: codes [E, 2I, H/2], packed scales, S [E]
  *   w2_*        down weights:    codes [E, H, I/2],  packed scales, S [E]

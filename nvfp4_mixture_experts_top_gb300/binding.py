@@ -30,7 +30,8 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_device_check", "nvfp4_quantize_workspac
            "mxfp4_quantize", "mxfp4_pack_weight_scales", "moe_route_quantize_mxfp4",
            "moe_router_logits_workspace_bytes", "moe_router_logits", "moe_layer_host_workspace_bytes",
            "moe_layer_forward_host", "fp8_quantize", "moe_route_quantize_fp8", "moe_router_route_workspace_bytes",
-           "moe_router_route", "moe_gather_f16", "moe_swiglu_f16")
+           "moe_router_route", "moe_gather_f16", "moe_swiglu_f16", "moe_route_quantize_fp8_f16",
+           "moe_swiglu_fp8_f16")
 
 
 class Nvfp4Error(RuntimeError):
@@ -112,6 +113,10 @@ def load(build_if_missing: bool = True):
     L.moe_gather_f16.argtypes = [_P, _I, _I, _P, _I, _P, _P, _P]
     L.moe_swiglu_f16.restype = _I
     L.moe_swiglu_f16.argtypes = [_P, _I, _I, _P, _P, _P]
+    L.moe_route_quantize_fp8_f16.restype = _I
+    L.moe_route_quantize_fp8_f16.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.moe_swiglu_fp8_f16.restype = _I
+    L.moe_swiglu_fp8_f16.argtypes = [_P, _I, _I, _P, _P, _P, _P]
     L.fp8_quantize.restype = _I
     L.fp8_quantize.argtypes = [_P, _I, _I64, _I64, _I64, _P, _I, _P, _P, _SZ, _P]
     L.moe_route_quantize_fp8.restype = _I
@@ -441,6 +446,44 @@ def moe_swiglu_f16(G):
     h = _empty((max(R, 1), I), torch.float16, G.device)
     rs = _empty((max(R, 1),), torch.float32, G.device)
     _check("moe_swiglu_f16", L.moe_swiglu_f16(_ptr(G), R, I, _ptr(h), _ptr(rs), _stream()))
+    return h[:R], rs[:R]
+
+
+def moe_route_quantize_fp8_f16(x, logits, k, dev_status=None):
+    """moe_route_quantize_fp8 with the codes as their f16 values: returns
+    dict(ids, w, offsets, perm, inv, S_x, act_f16 [T*k, H] float16, act_rs [T*k])."""
+    L = load()
+    T, H = x.shape
+    E = logits.shape[1]
+    dev = x.device
+    R = T * k
+    out = dict(ids=_empty((max(T, 1), k), torch.int32, dev), w=_empty((max(T, 1), k), torch.float32, dev),
+               offsets=_empty((E + 1,), torch.int32, dev), perm=_empty((max(R, 1),), torch.int32, dev),
+               inv=_empty((max(R, 1),), torch.int32, dev), S_x=_empty((4,), torch.float32, dev),
+               act_f16=_empty((max(R, 1), H), torch.float16, dev), act_rs=_empty((max(R, 1),), torch.float32, dev))
+    ws = _empty((max(int(L.moe_align_permute_workspace_bytes(T, E, k)), 256),), torch.uint8, dev)
+    _check("moe_route_quantize_fp8_f16",
+           L.moe_route_quantize_fp8_f16(_ptr(x), _ptr(logits), T, H, E, k, _ptr(out["ids"]), _ptr(out["w"]),
+                                        _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv"]), _ptr(out["S_x"]),
+                                        _ptr(out["act_f16"]), _ptr(out["act_rs"]), _ptr(dev_status), _ptr(ws),
+                                        ws.numel(), _stream()))
+    for key in ("ids", "w"):
+        out[key] = out[key][:T]
+    for key in ("perm", "inv", "act_f16", "act_rs"):
+        out[key] = out[key][:R]
+    out["S_x"] = out["S_x"][:1]
+    return out
+
+
+def moe_swiglu_fp8_f16(G, S_h):
+    """The W4A8 SwiGLU's FP8 codes as their f16 values: returns (h_f16 [R, I]
+    float16, h_rs [R] fp32 = S_h)."""
+    L = load()
+    R, I2 = G.shape
+    I = I2 // 2
+    h = _empty((max(R, 1), I), torch.float16, G.device)
+    rs = _empty((max(R, 1),), torch.float32, G.device)
+    _check("moe_swiglu_fp8_f16", L.moe_swiglu_fp8_f16(_ptr(G), R, I, _ptr(S_h), _ptr(h), _ptr(rs), _stream()))
     return h[:R], rs[:R]
 
 

@@ -435,6 +435,48 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
       launch_gemm_w4a16(a, w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out, dev_status, st));
 }
 
+int moe_route_quantize_fp8_f16(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
+                               float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv, float* S_x,
+                               void* a_f16, float* a_rs, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                               nvfp4_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return NVFP4_E_INVAL;
+  if (k > E || k > 32 || E > 1024 || H % 256 != 0) return NVFP4_E_SHAPE;
+  if (expert_offsets == nullptr || S_x == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(expert_offsets) || !aligned16(S_x)) return NVFP4_E_ALIGN;
+  if (T > 0) {
+    if (x == nullptr || logits == nullptr || topk_ids == nullptr || topk_w == nullptr || perm == nullptr ||
+        inv == nullptr || a_f16 == nullptr || a_rs == nullptr)
+      return NVFP4_E_INVAL;
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(perm) ||
+        !aligned16(inv) || !aligned16(a_f16))
+      return NVFP4_E_ALIGN;
+    if (workspace == nullptr || workspace_bytes < route_workspace_bytes(T, E)) return NVFP4_E_WORKSPACE;
+    if (!aligned16(workspace)) return NVFP4_E_ALIGN;
+  }
+  CHECK_ARCH();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (cudaMemsetAsync(S_x, 0, sizeof(float), st) != cudaSuccess) return NVFP4_E_CUDA;
+    return cuda_status(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (size_t)(E + 1), st));
+  }
+  if (launch_route_only(logits, T, E, k, topk_ids, topk_w, expert_offsets, perm, inv, dev_status, workspace, st, x,
+                        H) != cudaSuccess)
+    return NVFP4_E_CUDA;
+  return cuda_status(launch_fp8_quantize_scatter(x, T, H, k, inv, static_cast<const uint32_t*>(workspace) + 1, S_x,
+                                                 nullptr, st, a_f16, a_rs));
+}
+
+int moe_swiglu_fp8_f16(const float* G, int R, int I, const float* S_h, void* h_f16, float* h_rs,
+                       nvfp4_stream_t stream) {
+  if (R < 0 || I < 0) return NVFP4_E_INVAL;
+  if (I % 16 != 0) return NVFP4_E_SHAPE;
+  if ((int64_t)R * I == 0) return NVFP4_OK;
+  if (G == nullptr || S_h == nullptr || h_f16 == nullptr || h_rs == nullptr) return NVFP4_E_INVAL;
+  if (!aligned16(G) || !aligned16(h_f16)) return NVFP4_E_ALIGN;
+  CHECK_ARCH();
+  return cuda_status(launch_swiglu_fp8_f16(G, R, I, S_h, h_f16, h_rs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_gather_f16(const void* x, int T, int H, const int32_t* perm, int R, void* a_f16, float* a_rs,
                    nvfp4_stream_t stream) {
   if (T < 0 || H < 0 || R < 0) return NVFP4_E_INVAL;
@@ -531,9 +573,12 @@ static LayerWs carve(void* base, int mode, int T, int H, int I, int E, int k) {
     w.h_codes = take(R * I / 2);
     w.h_scales = take(R * (size_t)mx_scale_pitch(I));
   } else if (mode == MOE_W4A8) {
+    // the FP8 activations travel as their f16 values (MOE_W4A16F GEMMs)
     w.S_x = reinterpret_cast<float*>(take(16));
-    w.a_codes = take(R * H);
-    w.h_codes = take(R * I);
+    w.a_bf16 = take(R * H * 2);
+    w.h_bf16 = take(R * I * 2);
+    w.a_rs = reinterpret_cast<float*>(take(R * 4));
+    w.h_rs = reinterpret_cast<float*>(take(R * 4));
   } else if (mode == MOE_W4A4) {
     w.S_x = reinterpret_cast<float*>(take(16));
     w.a_codes = take(R * H / 2);
@@ -589,16 +634,19 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
                                w.offsets, E, H, I, R, w.Y, dev_status, stream);
     if (s != NVFP4_OK) return s;
   } else if (mode == MOE_W4A8) {
-    s = moe_route_quantize_fp8(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_codes,
-                               dev_status, w.route, route_workspace_bytes(T, E), stream);
+    // FP8 quantisation as moe_route_quantize_fp8 / moe_swiglu_requant, with
+    // the codes carried as their f16 values into the F16-operand GEMM (the
+    // same products as the MOE_W4A8 GEMM, whose codes it converts itself)
+    s = moe_route_quantize_fp8_f16(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_bf16,
+                                   w.a_rs, dev_status, w.route, route_workspace_bytes(T, E), stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_W4A8, w.a_codes, nullptr, w.S_x, w13_codes, w13_scales_packed, w13_S, w.offsets,
-                               E, 2 * I, H, R, w.G, dev_status, stream);
+    s = moe_grouped_gemm_nvfp4(MOE_W4A16F, w.a_bf16, nullptr, w.a_rs, w13_codes, w13_scales_packed, w13_S,
+                               w.offsets, E, 2 * I, H, R, w.G, dev_status, stream);
     if (s != NVFP4_OK) return s;
-    s = moe_swiglu_requant(w.G, R, I, MOE_W4A8, S_h, w.h_codes, nullptr, nullptr, stream);
+    s = moe_swiglu_fp8_f16(w.G, R, I, S_h, w.h_bf16, w.h_rs, stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_W4A8, w.h_codes, nullptr, S_h, w2_codes, w2_scales_packed, w2_S, w.offsets, E,
-                               H, I, R, w.Y, dev_status, stream);
+    s = moe_grouped_gemm_nvfp4(MOE_W4A16F, w.h_bf16, nullptr, w.h_rs, w2_codes, w2_scales_packed, w2_S, w.offsets,
+                               E, H, I, R, w.Y, dev_status, stream);
     if (s != NVFP4_OK) return s;
   } else if (mode == MOE_W4A4) {
     s = moe_route_quantize_nvfp4(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_codes,

@@ -138,6 +138,19 @@ __device__ __forceinline__ uint32_t fp8_code(float x, float s) {
   return e4m3_from_f32(fabsf(q)) | ((__float_as_uint(q) >> 31) << 7);
 }
 
+// Two FP8 codes (low byte: the lower element) -> their values as f16x2 (exact:
+// every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t two) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)two));
+  return d;
+}
+// Eight FP8 codes (two words) -> their eight f16 values (four words).
+__device__ __forceinline__ uint4 f16x8_of_e4m3x8(uint2 c) {
+  return make_uint4(f16x2_of_e4m3x2(c.x & 0xFFFFu), f16x2_of_e4m3x2(c.x >> 16), f16x2_of_e4m3x2(c.y & 0xFFFFu),
+                    f16x2_of_e4m3x2(c.y >> 16));
+}
+
 // Eight inputs -> eight FP8 codes (two little-endian words), decode scale s.
 __device__ __forceinline__ uint2 fp8_codes8(const float (&v)[8], float s) {
   uint32_t w[2];
@@ -180,7 +193,9 @@ __global__ void __launch_bounds__(256) fp8_quantize_scatter_kernel(const __nv_bf
                                                                    int64_t H, int k, const int32_t* __restrict__ inv,
                                                                    const uint32_t* __restrict__ amax_bits,
                                                                    float* __restrict__ S,
-                                                                   uint8_t* __restrict__ codes) {
+                                                                   uint8_t* __restrict__ codes,
+                                                                   __half* __restrict__ f16_out,
+                                                                   float* __restrict__ rs) {
   pdl_wait();
   pdl_trigger();
   const float s = __fdiv_rn(__uint_as_float(*amax_bits), 448.0f);
@@ -192,7 +207,17 @@ __global__ void __launch_bounds__(256) fp8_quantize_scatter_kernel(const __nv_bf
     float v[8];
     load8<__nv_bfloat16>(x + t * H + c, v);
     const uint2 w = fp8_codes8(v, s);
-    for (int j = 0; j < k; ++j) *reinterpret_cast<uint2*>(codes + (int64_t)__ldg(inv + t * k + j) * H + c) = w;
+    if (f16_out == nullptr) {
+      for (int j = 0; j < k; ++j) *reinterpret_cast<uint2*>(codes + (int64_t)__ldg(inv + t * k + j) * H + c) = w;
+    } else {
+      // the F16 carrier: each code's value (exact), the scale per row
+      const uint4 f = f16x8_of_e4m3x8(w);
+      for (int j = 0; j < k; ++j) {
+        const int64_t r = __ldg(inv + t * k + j);
+        *reinterpret_cast<uint4*>(f16_out + r * H + c) = f;
+        if (c == 0) rs[r] = s;
+      }
+    }
   }
 }
 
@@ -226,7 +251,8 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
                                                              int mode, const float* __restrict__ S_h,
                                                              uint8_t* __restrict__ h_codes,
                                                              uint8_t* __restrict__ h_scales,
-                                                             __nv_bfloat16* __restrict__ h_bf16) {
+                                                             __nv_bfloat16* __restrict__ h_bf16,
+                                                             __half* __restrict__ h_f16, float* __restrict__ h_rs) {
   pdl_wait();
   pdl_trigger();
   const int64_t nb_row = I / 16;
@@ -256,7 +282,15 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
       for (int q = 0; q < 4; ++q)
         w[q] = fp8_code(h[4 * q], s) | (fp8_code(h[4 * q + 1], s) << 8) | (fp8_code(h[4 * q + 2], s) << 16) |
                (fp8_code(h[4 * q + 3], s) << 24);
-      *reinterpret_cast<uint4*>(h_codes + r * I + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (h_f16 == nullptr) {
+        *reinterpret_cast<uint4*>(h_codes + r * I + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        // the F16 carrier of the FP8 codes: their values (exact), the scale per row
+        uint4* dst = reinterpret_cast<uint4*>(h_f16 + r * I + b * 16);
+        dst[0] = f16x8_of_e4m3x8(make_uint2(w[0], w[1]));
+        dst[1] = f16x8_of_e4m3x8(make_uint2(w[2], w[3]));
+        if (b == 0) h_rs[r] = s;
+      }
     } else {
       uint32_t w[8];
 #pragma unroll
@@ -560,11 +594,13 @@ cudaError_t launch_fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_
 }
 
 cudaError_t launch_fp8_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
-                                        const uint32_t* amax_bits, float* S, uint8_t* codes, cudaStream_t st) {
+                                        const uint32_t* amax_bits, float* S, uint8_t* codes, cudaStream_t st,
+                                        void* f16_out, float* rs) {
   const int64_t nv = (int64_t)T * (H / 8);
   if (nv == 0) return cudaSuccess;
   return launch_pdl(fp8_quantize_scatter_kernel, grid_for(nv, 256), 256, 0, st,
-                    static_cast<const __nv_bfloat16*>(x_bf16), T, (int64_t)H, k, inv, amax_bits, S, codes);
+                    static_cast<const __nv_bfloat16*>(x_bf16), T, (int64_t)H, k, inv, amax_bits, S, codes,
+                    static_cast<__half*>(f16_out), rs);
 }
 
 cudaError_t launch_pack_scales(const uint8_t* in, int E, int N, int K, uint8_t* out, cudaStream_t st) {
@@ -579,7 +615,17 @@ cudaError_t launch_swiglu_requant(const float* G, int R, int I, int mode, const 
   const int64_t nblk = (int64_t)R * (I / 16);
   if (nblk == 0) return cudaSuccess;
   return launch_pdl(swiglu_requant_kernel, grid_for(nblk, 256), 256, 0, st, G, (int64_t)R, (int64_t)I, mode, S_h,
-                    h_codes, h_scales, static_cast<__nv_bfloat16*>(h_bf16));
+                    h_codes, h_scales, static_cast<__nv_bfloat16*>(h_bf16), static_cast<__half*>(nullptr),
+                    static_cast<float*>(nullptr));
+}
+
+cudaError_t launch_swiglu_fp8_f16(const float* G, int R, int I, const float* S_h, void* h_f16, float* h_rs,
+                                  cudaStream_t st) {
+  const int64_t nblk = (int64_t)R * (I / 16);
+  if (nblk == 0) return cudaSuccess;
+  return launch_pdl(swiglu_requant_kernel, grid_for(nblk, 256), 256, 0, st, G, (int64_t)R, (int64_t)I,
+                    (int)MOE_W4A8, S_h, static_cast<uint8_t*>(nullptr), static_cast<uint8_t*>(nullptr),
+                    static_cast<__nv_bfloat16*>(nullptr), static_cast<__half*>(h_f16), h_rs);
 }
 
 // ---------------------------------------------------------------------------

@@ -119,8 +119,14 @@ cudaError_t launch_fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_
                                 int dynamic, uint32_t* amax_ws, uint8_t* codes, cudaStream_t st);
 // x [T, H] bf16 -> FP8 codes of each token in its k permuted rows (amax bits
 // from the routing pass; S written to *S).
+// With f16_out != NULL the codes are written as their f16 values (the F16
+// carrier of MOE_W4A16F) and rs[r] = S for every written row r.
 cudaError_t launch_fp8_quantize_scatter(const void* x_bf16, int T, int H, int k, const int32_t* inv,
-                                        const uint32_t* amax_bits, float* S, uint8_t* codes, cudaStream_t st);
+                                        const uint32_t* amax_bits, float* S, uint8_t* codes, cudaStream_t st,
+                                        void* f16_out = nullptr, float* rs = nullptr);
+// The W4A8 SwiGLU's FP8 codes written as their f16 values, h_rs[r] = *S_h.
+cudaError_t launch_swiglu_fp8_f16(const float* G, int R, int I, const float* S_h, void* h_f16, float* h_rs,
+                                  cudaStream_t st);
 
 // Router logits [T, E] = x [T, H] . W [E, H]^T (bf16 in, fp32 out) on the
 // tensor cores, K split over the SMs; workspace holds the fp32 partials

@@ -66,6 +66,41 @@ def test_route_quantize_fp8_matches_staged(orc, name):
     assert float(S.item()) == float(orc.fp8_tensor_scale(x.float().cpu().numpy()))
 
 
+def _codes_as_f16(codes):
+    """FP8 E4M3 codes -> their values as float16 (every E4M3 value is one)."""
+    return codes.view(torch.float8_e4m3fn).to(torch.float16)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_c16", "wide"])
+def test_route_quantize_fp8_f16_carries_the_codes(orc, name):
+    """The F16 carrier of the FP8 front half (what the W4A8 layer runs): the
+    same routing and scale as moe_route_quantize_fp8, every code replaced by
+    its value in f16, and the scale beside every row."""
+    dev = cuda_or_skip()
+    cfg = wl.CONFIGS[name]
+    x = wl.activations_bf16(cfg.T, cfg.H, device=dev)
+    logits = wl.router_logits(cfg, device=dev)
+    rt = B.moe_route_quantize_fp8(x, logits, cfg.k)
+    rf = B.moe_route_quantize_fp8_f16(x, logits, cfg.k)
+    torch.cuda.synchronize()
+    for key in ("ids", "offsets", "perm", "inv", "S_x"):
+        assert torch.equal(rf[key], rt[key]), key
+    assert torch.equal(rf["act_f16"].view(torch.int16), _codes_as_f16(rt["act_codes"]).view(torch.int16))
+    assert torch.equal(rf["act_rs"], rt["S_x"].expand(rf["act_rs"].shape[0]))
+
+
+@pytest.mark.parametrize("R,I", [(1, 16), (37, 512)])
+def test_swiglu_fp8_f16_carries_the_codes(R, I):
+    dev = cuda_or_skip()
+    G = (wl.random_fp32((R, 2 * I), seed=R + I, tag="g8f") * 2).to(dev)
+    S_h = torch.tensor([0.01], dtype=torch.float32, device=dev)
+    hc = B.moe_swiglu_requant(G, B.MOE_W4A8, S_h=S_h)
+    hf, rs = B.moe_swiglu_fp8_f16(G, S_h)
+    torch.cuda.synchronize()
+    assert torch.equal(hf.view(torch.int16), _codes_as_f16(hc).view(torch.int16))
+    assert torch.equal(rs, S_h.expand(R))
+
+
 def _fp8_acts(orc, R, K, seed):
     a = wl.random_fp32((R, K), seed=seed, tag="acts8").to(torch.bfloat16).float().numpy()
     return orc.fp8_quantize(a)
