@@ -25,6 +25,8 @@
 // All warps run converged; single operations go through elect.sync.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -284,8 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int it_m = 0;
     const uint32_t smem_base = smem_u32(smem);
     for (int w = blockIdx.x, j = 0; ok && w < items; w += gridDim.x, ++j) {
-      const int ng = item_j(j, w).ng;
-      const uint32_t idesc = AK == kBF16 ? idesc_bf16(BM, TG * ng) : idesc_f16(BM, TG * ng);
+      const int ng = item_j(j, w).ng;  // 1 or 2 token groups
       if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
         ok = false;
         break;
@@ -304,12 +305,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) W4A16_TRACE(3, it_m);
         const uint32_t a_col = tmem + A_COL0 + slot * A_SLOT_COLS;
         const uint32_t sb = smem_base + stage * RSTAGE_BYTES + OFF_B;
+        // 16 values of K per step: 8 TMEM columns of A, 32 bytes along B's
+        // swizzled row.  The instruction descriptor is a compile-time constant
+        // per token-group count: with it in a register the 16 MMAs of a stage
+        // took ~9 cycles longer each to issue (GB300), and the MMA issue sets
+        // this kernel's stage period.
+        auto issue = [&](auto ngc) {
+          constexpr uint32_t kIdesc = AK == kBF16 ? idesc_bf16(BM, TG * decltype(ngc)::value)
+                                                  : idesc_f16(BM, TG * decltype(ngc)::value);
 #pragma unroll
-        for (int kk = 0; kk < KC / 16; ++kk) {
-          // 16 bf16 of K per step: 8 TMEM columns of A, 32 bytes along B's swizzled row
-          const uint64_t bdesc = desc_sw128(sb + (kk >> 2) * B_ATOM) + 2 * (kk & 3);
-          ew_mma_bf16_ts(d_col, a_col + 8 * kk, bdesc, idesc, (kc | kk) != 0);
-        }
+          for (int kk = 0; kk < KC / 16; ++kk) {
+            const uint64_t bdesc = desc_sw128(sb + (kk >> 2) * B_ATOM) + 2 * (kk & 3);
+            ew_mma_bf16_ts(d_col, a_col + 8 * kk, bdesc, kIdesc, (kc | kk) != 0);
+          }
+        };
+        static_assert(MAXG == 2, "a pass holds one or two token groups");
+        if (ng == 1)
+          issue(std::integral_constant<int, 1>{});
+        else
+          issue(std::integral_constant<int, 2>{});
         if (lane == 0) W4A16_TRACE(4, it_m);
         ew_commit(&consumed[stage]);
         ++it_m;

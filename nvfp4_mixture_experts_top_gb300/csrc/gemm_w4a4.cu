@@ -381,7 +381,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kc0 = cur.kc0, kc1 = cur.kc1;
       const int ng = cur.it.ng;
       {
-        const uint32_t idesc = MX ? idesc_mxf4_ue8m0(BM, TG * ng) : idesc_mxf4nvf4(BM, TG * ng);
         if (!warp_wait(&acc_empty[acc], acc_phase ^ 1, &abort_flag, p.dev_status)) {
           ok = false;
           break;
@@ -408,17 +407,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sfb = sfa + 16;
           const uint64_t adesc = desc_sw128(sb);
           const uint64_t bdesc = desc_sw128(sb + OFF_A);
+          // K step kk = 64 FP4 elements = 32 bytes along the swizzled row.
+          // Passes of one token group issue with a compile-time instruction
+          // descriptor (decode_c16 gate_up 155 -> 152 us on GB300); for passes
+          // of up to four groups a switch over the four constants measured
+          // 3% slower than the descriptor in a register, which stays.
+          auto issue = [&](uint32_t idesc) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            ew_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
-            ew_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
-            // K step kk = 64 FP4 elements = 32 bytes along the swizzled row
-            if constexpr (MX)
-              ew_mma_mxf4_2x(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
-                             (kc != kc0 || kk != 0));
-            else
-              ew_mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
-                            (kc != kc0 || kk != 0));
+            for (int kk = 0; kk < 4; ++kk) {
+              ew_cp_32x128b_x4(sfa + 4 * kk, desc_sf(sb + OFF_WS + kk * 512));
+              ew_cp_32x128b_x4(sfb + 4 * kk, desc_sf(sb + OFF_AS + kk * AS_BYTES));
+              if constexpr (MX)
+                ew_mma_mxf4_2x(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
+                               (kc != kc0 || kk != 0));
+              else
+                ew_mma_mxf4nvf4(d_col, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + 4 * kk,
+                                (kc != kc0 || kk != 0));
+            }
+          };
+          if constexpr (G == 1) {
+            constexpr uint32_t kIdesc1 = MX ? idesc_mxf4_ue8m0(BM, TG) : idesc_mxf4nvf4(BM, TG);
+            issue(kIdesc1);
+          } else {
+            issue(MX ? idesc_mxf4_ue8m0(BM, TG * ng) : idesc_mxf4nvf4(BM, TG * ng));
           }
           ew_commit(&empty_bar[stage]);
           if (lane == 0) W4A4_TRACE(2, it_c);
