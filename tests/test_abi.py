@@ -130,3 +130,31 @@ def test_layer_entries_validate_on_the_host_without_gpu():
                                L.moe_layer_workspace_bytes(0, 16, 4000, 2048, 256, 8), None) == 2
     assert L.moe_layer_forward(0, ok, ok, 16, 4096, 2048, 256, 8, ok, ok, ok, ok, ok, ok, ok, ok, None, ok,
                                L.moe_layer_workspace_bytes(0, 16, 4096, 2048, 256, 8) - 1, None) == 4
+
+
+def test_carrier_entries_validate_on_the_host_without_gpu():
+    """The F16-carrier entry points and GEMM mode MOE_W4A16F reject bad
+    arguments on the host: shapes, missing pointers and misalignment."""
+    from nvfp4_mixture_experts_top_gb300 import binding
+    L = binding.load()
+    p16, p8 = ctypes.c_void_p(16), ctypes.c_void_p(8)
+    # W4A16F needs its row multipliers (a_S) -> E_INVAL
+    assert L.moe_grouped_gemm_nvfp4(binding.MOE_W4A16F, p16, None, None, p16, p16, p16, p16, 4, 128, 256, 8, p16,
+                                    None, None) == 1
+    # moe_gather_f16: H % 8 != 0 -> E_SHAPE; no row-multiplier output -> E_INVAL; misaligned rows -> E_ALIGN;
+    # no permutation and more output rows than tokens -> E_INVAL; nothing to do -> OK
+    assert L.moe_gather_f16(p16, 4, 12, None, 4, p16, p16, None) == 2
+    assert L.moe_gather_f16(p16, 4, 16, None, 4, p16, None, None) == 1
+    assert L.moe_gather_f16(p8, 4, 16, None, 4, p16, p16, None) == 3
+    assert L.moe_gather_f16(p16, 4, 16, None, 8, p16, p16, None) == 1
+    assert L.moe_gather_f16(None, 0, 16, None, 0, None, None, None) == 0
+    # moe_swiglu_f16 / moe_swiglu_fp8_f16: I % 16 != 0 -> E_SHAPE; missing S_h -> E_INVAL
+    assert L.moe_swiglu_f16(p16, 4, 24, p16, p16, None) == 2
+    assert L.moe_swiglu_f16(p16, 4, 32, p16, None, None) == 1
+    assert L.moe_swiglu_fp8_f16(p16, 4, 32, None, p16, p16, None) == 1
+    assert L.moe_swiglu_fp8_f16(p16, 4, 24, p16, p16, p16, None) == 2
+    # moe_route_quantize_fp8_f16: H % 256 != 0 -> E_SHAPE; no carrier output -> E_INVAL
+    assert L.moe_route_quantize_fp8_f16(p16, p16, 4, 200, 64, 8, p16, p16, p16, p16, p16, p16, p16, p16, None, p16,
+                                        1 << 20, None) == 2
+    assert L.moe_route_quantize_fp8_f16(p16, p16, 4, 256, 64, 8, p16, p16, p16, p16, p16, p16, None, p16, None, p16,
+                                        1 << 20, None) == 1
