@@ -151,16 +151,22 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   // 1-2: top-k of this chunk's tokens, chunk mask (and, when x is given, the
   // amax of the token's activation row for the per-tensor NVFP4 scale)
   const int t = blockIdx.x * tpc + warp;  // token; its bit in the chunk mask is t % 32
-  if (t < T && x != nullptr) {
-    const uint4* row = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+  if (x != nullptr) {
+    // the amax of this CTA's token rows, spread over all its threads (16 KB
+    // of loads in flight per warp), not one warp per row: at T = 16 half of
+    // the warps would otherwise idle
+    const int64_t t0 = (int64_t)blockIdx.x * tpc;
+    const int64_t rows = min((int64_t)tpc, (int64_t)T - t0);
+    const int64_t vec_per_row = H / 8;
+    const int64_t nvec = rows > 0 ? rows * vec_per_row : 0;
+    const uint4* base = reinterpret_cast<const uint4*>(x + t0 * H);
     float m = 0.0f;
-    // 8 independent 16-byte loads in flight per lane: one warp reads a whole
-    // row (12 KB at H = 6144), which one load at a time took ~24 round trips
     constexpr int kU = 8;
-    for (int64_t i0 = lane; i0 < H / 8; i0 += 32 * kU) {
+    for (int64_t i0 = threadIdx.x; i0 < nvec; i0 += (int64_t)blockDim.x * kU) {
       uint4 u[kU];
 #pragma unroll
-      for (int j = 0; j < kU; ++j) u[j] = (i0 + 32 * j < H / 8) ? __ldg(row + i0 + 32 * j) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kU; ++j)
+        u[j] = (i0 + (int64_t)blockDim.x * j < nvec) ? __ldg(base + i0 + (int64_t)blockDim.x * j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const uint32_t wv[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
