@@ -409,7 +409,7 @@ int moe_swiglu_requant(const float* G, int R, int I, int mode, const float* S_h,
  *   checked on the device: an entry outside [0, T*k) contributes nothing,
  *   and sets NVFP4_E_BAD_ROUTING in dev_status (optional, may be NULL);
  *   no out-of-range row is ever read.
- * Constraints: H % 4 == 0.
+ * Constraints: H % 4 == 0, 1 <= k <= 32 (as routing).
  * ------------------------------------------------------------------------ */
 int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, int k, int H, int out_dtype,
                 void* out, int32_t* dev_status, nvfp4_stream_t stream);

@@ -527,7 +527,7 @@ int moe_combine(const float* Y, const int32_t* inv, const float* topk_w, int T, 
                 void* out, int32_t* dev_status, nvfp4_stream_t stream) {
   if (T < 0 || k <= 0 || H < 0) return NVFP4_E_INVAL;
   if (out_dtype != NVFP4_DT_F32 && out_dtype != NVFP4_DT_BF16) return NVFP4_E_INVAL;
-  if (H % 4 != 0) return NVFP4_E_SHAPE;
+  if (H % 4 != 0 || k > 32) return NVFP4_E_SHAPE;
   if ((int64_t)T * H == 0) return NVFP4_OK;
   if (Y == nullptr || inv == nullptr || topk_w == nullptr || out == nullptr) return NVFP4_E_INVAL;
   if (!aligned16(Y) || !aligned16(out)) return NVFP4_E_ALIGN;

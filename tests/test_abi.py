@@ -158,3 +158,11 @@ def test_carrier_entries_validate_on_the_host_without_gpu():
                                         1 << 20, None) == 2
     assert L.moe_route_quantize_fp8_f16(p16, p16, 4, 256, 64, 8, p16, p16, p16, p16, p16, p16, None, p16, None, p16,
                                         1 << 20, None) == 1
+
+
+def test_combine_rejects_more_than_32_slots_without_gpu():
+    """k > 32 (more slots than routing produces) is refused on the host."""
+    from nvfp4_mixture_experts_top_gb300 import binding
+    L = binding.load()
+    p16 = ctypes.c_void_p(16)
+    assert L.moe_combine(p16, p16, p16, 4, 33, 64, 1, p16, None, None) == 2
