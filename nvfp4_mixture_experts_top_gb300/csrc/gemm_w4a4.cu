@@ -75,8 +75,8 @@ struct Geo {
   static constexpr uint32_t STAGE_BYTES = OFF_AS + 4 * AS_BYTES;
   static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
   // split-K epilogue staging (G = 4 only): per epilogue warp a [32 tokens][32
-  // rows] fp32 box in which a K half of a full token group is staged for the
-  // TMA reduce-add; G = 1 adds its K halves with atomics
+  // rows] fp32 box in which a K part of a full token group is staged for the
+  // TMA reduce-add; G = 1 adds its K parts with atomics
   static constexpr int RED_FLOATS = G == 4 ? 4 * 32 * 32 : 4;
   // TMEM columns: two accumulators of 32*G fp32 columns, then per stage 16
   // columns of weight scales and 16 of token scales (4 per K step each)

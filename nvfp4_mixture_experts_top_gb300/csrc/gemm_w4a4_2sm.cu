@@ -22,7 +22,7 @@
 //  * a K split (2 to 4 parts) when the tiles cannot occupy every pair: the
 //    parts add into a zeroed output;
 //  * epilogue: full 32-token groups are staged in shared memory and written
-//    by TMA (store, or reduce-add for a K half), asynchronously to the warp;
+//    by TMA (store, or reduce-add for a K part), asynchronously to the warp;
 //    an expert's ragged last group is written (or added) element-wise.
 // Warp roles in each CTA (all converged; single operations via elect.sync):
 //    warp 0    TMA producer: own weight rows, own token rows, both token
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int tb = it.r0 + g * TG;
         if (tb + TG <= it.m1) {
           // a full group: stage it as [token][row] and let TMA store it (or,
-          // for a K half, add it in L2), asynchronously to this warp
+          // for a K part, add it in L2), asynchronously to this warp
           if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // box's last use read
           __syncwarp();
 #pragma unroll
