@@ -19,7 +19,7 @@ CASES = [
     # (counts per expert, N, K): all with >= 1024 rows per expert on average
     ([1024], 256, 256),              # four full passes, one K stage (no split)
     ([1100], 512, 1024),             # ragged last pass (1100 = 4 x 256 + 76), K in two parts
-    ([1100, 0, 2000], 512, 768),     # an empty expert; K parts of 1 and 2 stages
+    ([1100, 0, 2000], 512, 1280),    # an empty expert; K in two parts of 2 and 3 stages
     ([2100, 2200], 4096, 512),       # 304 pair tiles, several per pair, no split
     ([2048], 512, 2048),             # 16 pair tiles: K in four parts of 2 stages
     ([1500, 700], 256, 1536),        # ragged passes of two experts: K in three parts
