@@ -15,6 +15,8 @@
 //      warp 0    TMA producer (weights evict-first, activations evict-last)
 //      warp 1    tcgen05.cp of block scales into TMEM + tcgen05.mma
 //      warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32 stores
+//                (passes of 128 tokens add warps 7-10: warps 2-5 take token
+//                groups 0 and 2, warps 7-10 groups 1 and 3)
 //      warp 6    token-scale preparation (shared-memory transpose, below)
 //  * a shared-memory ring (8 x 24 KB for passes of 32 tokens, 5 x 36 KB for
 //    passes of 128; see Geo) and two TMEM accumulator buffers, so loads, MMAs
@@ -74,22 +76,30 @@ struct Geo {
   static constexpr uint32_t OFF_AS = OFF_WS + WS_BYTES;
   static constexpr uint32_t STAGE_BYTES = OFF_AS + 4 * AS_BYTES;
   static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  // epilogue warps: two per TMEM lane quarter when a pass holds 4 groups, so
+  // that the last unit's epilogue (not overlapped by anything) takes half as long
+  static constexpr int EPI_WARPS = G == 4 ? 8 : 4;
+  static constexpr int THREADS = (3 + EPI_WARPS) * 32;
   // split-K epilogue staging (G = 4 only): per epilogue warp a [32 tokens][32
   // rows] fp32 box in which a K part of a full token group is staged for the
   // TMA reduce-add; G = 1 adds its K parts with atomics
-  static constexpr int RED_FLOATS = G == 4 ? 4 * 32 * 32 : 4;
+  static constexpr int RED_FLOATS = G == 4 ? EPI_WARPS * 32 * 32 : 4;
   // TMEM columns: two accumulators of 32*G fp32 columns, then per stage 16
   // columns of weight scales and 16 of token scales (4 per K step each)
   static constexpr uint32_t ACC_COLS = TOK_PER_PASS;
   static constexpr uint32_t SF_BASE = 2 * ACC_COLS;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(SF_BASE + STAGES * 32 <= 512, "TMEM budget");
-  static_assert(SMEM_BYTES + RED_FLOATS * 4 + 17 * 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
+  // work units decoded in the prologue (later ones are decoded on the fly):
+  // fewer with 4 groups, where the staging boxes take the shared memory and a
+  // CTA rarely has more than a few dozen units
+  static constexpr int UNIT_SLOTS = G == 4 ? 64 : 256;
+  static_assert(SMEM_BYTES + RED_FLOATS * 4 + sizeof(ItemTable) + UNIT_SLOTS * 16 + 512 <= 227 * 1024,
+                "shared memory budget (dynamic + static)");
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_STAGE = 32;
 
-constexpr int NUM_THREADS = 224;  // 7 warps, roles above
 
 struct Params {
   const uint8_t* w_scales;  // packed atoms
@@ -122,8 +132,8 @@ __device__ __forceinline__ Unit unit_at(int u, int splits, int kch, const ItemTa
 // A CTA's units, decoded once in the prologue (32 at a time, one per lane):
 // decoding costs ~1000 cycles of dependent latency (binary search, integer
 // divisions), which at a unit boundary stalled the producer and the MMA
-// issuer for a whole stage.  Units beyond the table are decoded on the fly.
-constexpr int kUnitTable = 256;
+// issuer for a whole stage.  The table holds Geo::UNIT_SLOTS units; later
+// ones are decoded on the fly.
 __device__ __forceinline__ int4 pack_unit(const Unit& u) {
   return make_int4(u.it.e | (u.it.nt << 16), u.it.r0, u.it.m1, u.kc0 | (u.kc1 << 12) | (u.it.ng << 24));
 }
@@ -146,7 +156,7 @@ __device__ __forceinline__ Unit unpack_unit(int4 v) {
 // rows of mx_scale_pitch(K) bytes, and warp 6 widens both into the 4-byte
 // per-row cells that tcgen05.cp copies to TMEM (bytes 2-3 zero).
 template <bool MX, int G>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Geo<G>::THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_as, const __grid_constant__ CUtensorMap tm_a4,
                      const __grid_constant__ CUtensorMap tm_as4, const __grid_constant__ CUtensorMap tm_out,
@@ -169,7 +179,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_flag;
   __shared__ ItemTable tab;
-  __shared__ int4 s_units[kUnitTable];
+  __shared__ int4 s_units[GE::UNIT_SLOTS];
   __shared__ __align__(128) float s_red[GE::RED_FLOATS];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -185,7 +195,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], GE::EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
     __syncwarp();
     const int n_units = tab.base[p.E] * p.splits;
-    for (int j = lane; j < kUnitTable; j += 32) {
+    for (int j = lane; j < GE::UNIT_SLOTS; j += 32) {
       const int u = blockIdx.x + j * gridDim.x;
       if (u >= n_units) break;
       s_units[j] = pack_unit(unit_at<TOK_PER_PASS>(u, p.splits, KCH, tab, NT, p.E));
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int units = tab.base[p.E] * p.splits;
   // unit number j of this CTA (u = blockIdx.x + j * gridDim.x)
   auto unit_j = [&](int j, int u) -> Unit {
-    return j < kUnitTable ? unpack_unit(s_units[j]) : unit_at<TOK_PER_PASS>(u, p.splits, KCH, tab, NT, p.E);
+    return j < GE::UNIT_SLOTS ? unpack_unit(s_units[j]) : unit_at<TOK_PER_PASS>(u, p.splits, KCH, tab, NT, p.E);
   };
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -452,8 +462,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) mbar_wait(&drain_bar, 0);
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2-5)
+    // ------------------------------------------------------------ epilogue (warps 2-5, 7-10)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int eh = warp >= 7 ? 1 : 0;  // which of the two warps on quarter q (G = 4)
+    constexpr int GSTEP = GE::EPI_WARPS / 4;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -469,8 +481,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        if (lane == 0 && q == 0) W4A4_TRACE(3, it_e);
-        for (int g = 0; g < ng; ++g) {
+        if (lane == 0 && q == 0 && eh == 0) W4A4_TRACE(3, it_e);
+        for (int g = eh; g < ng; g += GSTEP) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS + g * TG, r);
           tmem_ld_wait();
@@ -486,7 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (tb + TG <= m1) {
               // a full group: stage it as [token][row] and let TMA add it into
               // the output in L2
-              float* box = s_red + q * (TG * 32);
+              float* box = s_red + (eh * 4 + q) * (TG * 32);
               if (lane == 0) bulk_wait_read_all();  // the previous box has been read
               __syncwarp();
 #pragma unroll
@@ -507,7 +519,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         ew_arrive(&acc_empty[acc]);
-        if (lane == 0 && q == 0) W4A4_TRACE(4, it_e);
+        if (lane == 0 && q == 0 && eh == 0) W4A4_TRACE(4, it_e);
         ++it_e;
         if (++acc == 2) {
           acc = 0;
@@ -591,7 +603,7 @@ static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, c
     cudaError_t e = launch_zero_f32(out, (size_t)R * N, st);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(gemm_w4a4_kernel<MX, G>, num_sms(), NUM_THREADS, Geo<G>::SMEM_BYTES, st, tm_w, tm_a, tm_as, tm_a4,
+  return launch_pdl(gemm_w4a4_kernel<MX, G>, num_sms(), Geo<G>::THREADS, Geo<G>::SMEM_BYTES, st, tm_w, tm_a, tm_as, tm_a4,
                     tm_as4, tm_out, p);
 }
 
