@@ -27,6 +27,10 @@
  *    on the stream: a kernel's prologue (barrier setup, TMEM allocation) may
  *    overlap that kernel's end, but it reads and writes memory only after
  *    that kernel has completed, so stream order holds as with plain launches.
+ *    Inside moe_layer_forward the W4A4 and MXFP4 grouped GEMMs also read the
+ *    routing and start their first weight copies during that overlap: both
+ *    were final before the preceding kernel started, so the order is the
+ *    same.
  *  - Arguments are validated on the host before anything is launched, so a
  *    failing call launches nothing.  The return value is an nvfp4_status.
  *  - Kernels that consume routing data check it and report problems through

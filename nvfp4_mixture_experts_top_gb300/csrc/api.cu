@@ -393,10 +393,10 @@ int moe_route_quantize_fp8(const void* x, const float* logits, int T, int H, int
                                                  a_codes, st));
 }
 
-int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, const float* a_S,
-                           const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
-                           const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
-                           int32_t* dev_status, nvfp4_stream_t stream) {
+// early: see launch_gemm_w4a4 (true only from moe_layer_forward's chain)
+static int grouped_gemm(int mode, const void* a, const uint8_t* a_scales, const float* a_S, const uint8_t* w_codes,
+                        const uint8_t* w_scales_packed, const float* w_S, const int32_t* expert_offsets, int E,
+                        int N, int K, int R, float* out, int32_t* dev_status, nvfp4_stream_t stream, bool early) {
   if (mode != MOE_W4A4 && mode != MOE_W4A16 && mode != MOE_MXW4A4 && mode != MOE_W4A8 && mode != MOE_W4A16F)
     return NVFP4_E_INVAL;
   if (E <= 0 || N < 0 || K < 0 || R < 0) return NVFP4_E_INVAL;
@@ -427,12 +427,20 @@ int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, con
                                              dev_status, st));
   if (mode == MOE_MXW4A4)
     return cuda_status(launch_gemm_mxw4a4(static_cast<const uint8_t*>(a), a_scales, w_codes, w_scales_packed,
-                                          expert_offsets, E, N, K, R, out, dev_status, st));
+                                          expert_offsets, E, N, K, R, out, dev_status, st, early));
   if (mode == MOE_W4A4)
     return cuda_status(launch_gemm_w4a4(static_cast<const uint8_t*>(a), a_scales, a_S, w_codes, w_scales_packed, w_S,
-                                        expert_offsets, E, N, K, R, out, dev_status, st));
+                                        expert_offsets, E, N, K, R, out, dev_status, st, early));
   return cuda_status(
       launch_gemm_w4a16(a, w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out, dev_status, st));
+}
+
+int moe_grouped_gemm_nvfp4(int mode, const void* a, const uint8_t* a_scales, const float* a_S,
+                           const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
+                           const int32_t* expert_offsets, int E, int N, int K, int R, float* out,
+                           int32_t* dev_status, nvfp4_stream_t stream) {
+  return grouped_gemm(mode, a, a_scales, a_S, w_codes, w_scales_packed, w_S, expert_offsets, E, N, K, R, out,
+                      dev_status, stream, false);
 }
 
 int moe_route_quantize_fp8_f16(const void* x, const float* logits, int T, int H, int E, int k, int32_t* topk_ids,
@@ -625,13 +633,13 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
     s = moe_route_quantize_mxfp4(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.a_codes, w.a_scales,
                                  dev_status, w.route, route_workspace_bytes(T, E), stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_MXW4A4, w.a_codes, w.a_scales, nullptr, w13_codes, w13_scales_packed, nullptr,
-                               w.offsets, E, 2 * I, H, R, w.G, dev_status, stream);
+    s = grouped_gemm(MOE_MXW4A4, w.a_codes, w.a_scales, nullptr, w13_codes, w13_scales_packed, nullptr, w.offsets, E,
+                     2 * I, H, R, w.G, dev_status, stream, true);
     if (s != NVFP4_OK) return s;
     s = moe_swiglu_requant(w.G, R, I, MOE_MXW4A4, nullptr, w.h_codes, w.h_scales, nullptr, stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_MXW4A4, w.h_codes, w.h_scales, nullptr, w2_codes, w2_scales_packed, nullptr,
-                               w.offsets, E, H, I, R, w.Y, dev_status, stream);
+    s = grouped_gemm(MOE_MXW4A4, w.h_codes, w.h_scales, nullptr, w2_codes, w2_scales_packed, nullptr, w.offsets, E, H,
+                     I, R, w.Y, dev_status, stream, true);
     if (s != NVFP4_OK) return s;
   } else if (mode == MOE_W4A8) {
     // FP8 quantisation as moe_route_quantize_fp8 / moe_swiglu_requant, with
@@ -652,13 +660,13 @@ int moe_layer_forward(int mode, const void* x, const float* logits, int T, int H
     s = moe_route_quantize_nvfp4(x, logits, T, H, E, k, w.ids, w.w, w.offsets, w.perm, w.inv, w.S_x, w.a_codes,
                                  w.a_scales, dev_status, w.route, route_workspace_bytes(T, E), stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_W4A4, w.a_codes, w.a_scales, w.S_x, w13_codes, w13_scales_packed, w13_S,
-                               w.offsets, E, 2 * I, H, R, w.G, dev_status, stream);
+    s = grouped_gemm(MOE_W4A4, w.a_codes, w.a_scales, w.S_x, w13_codes, w13_scales_packed, w13_S, w.offsets, E,
+                     2 * I, H, R, w.G, dev_status, stream, true);
     if (s != NVFP4_OK) return s;
     s = moe_swiglu_requant(w.G, R, I, MOE_W4A4, S_h, w.h_codes, w.h_scales, nullptr, stream);
     if (s != NVFP4_OK) return s;
-    s = moe_grouped_gemm_nvfp4(MOE_W4A4, w.h_codes, w.h_scales, S_h, w2_codes, w2_scales_packed, w2_S, w.offsets,
-                               E, H, I, R, w.Y, dev_status, stream);
+    s = grouped_gemm(MOE_W4A4, w.h_codes, w.h_scales, S_h, w2_codes, w2_scales_packed, w2_S, w.offsets, E, H, I, R,
+                     w.Y, dev_status, stream, true);
     if (s != NVFP4_OK) return s;
   } else {
     // W4A16: the bf16 activations (x, and h rounded to bf16) travel as F16

@@ -116,9 +116,12 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 // the programmatic-serialization attribute.  pdl_trigger: let the next grid
 // on the stream begin launching once every CTA of this grid has triggered or
 // exited.  Kernels of this library touch no global memory before pdl_wait
-// and trigger only after it (and after their TMEM allocation), so at most two
-// grids of a chain are resident and a waiting grid never holds TMEM that its
-// predecessor still has to allocate.
+// and trigger only after it (and after their TMEM allocation), so a waiting
+// grid never holds TMEM that its predecessor still has to allocate.  The one
+// exception is a grouped GEMM inside a layer's chain ("early"): it reads the
+// routing and issues weight copies before its wait -- data written by grids
+// that completed before its predecessor passed its own wait -- and triggers
+// its successor (SwiGLU, which allocates no TMEM) before its wait too.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

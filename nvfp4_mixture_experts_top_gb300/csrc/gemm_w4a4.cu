@@ -111,6 +111,11 @@ struct Params {
   int E, N, K, R;
   int drop_stage;  // fault injection for tests: producer stage index never armed (-1: none)
   int splits;      // K parts per work item, 1 to 8 (more than one: they add into a zeroed output)
+  // 1 inside a layer's kernel chain, where the routing was final before the
+  // preceding kernel started (that kernel waited on its own predecessor
+  // before it let this grid launch): the routing is read, and the ring's
+  // first weight copies issued, before griddepcontrol.wait
+  int early;
 };
 
 
@@ -211,8 +216,10 @@ __global__ void __launch_bounds__(Geo<G>::THREADS, 1)
     tmem_relinquish();
   }
   // nothing above reads or writes global memory: launched as a programmatic
-  // dependent, this prologue overlaps the preceding kernel's tail
-  pdl_wait();
+  // dependent, this prologue overlaps the preceding kernel's tail.  In a
+  // layer's chain (p.early) the item table and the first weight copies
+  // overlap it too; then only the token copies and the epilogue wait.
+  if (!p.early) pdl_wait();
   const ExpertRows xr{p.offsets, p.E, p.R};
   if (warp == 2) {
     build_item_table<TOK_PER_PASS>(xr, NT, tab, lane);
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(Geo<G>::THREADS, 1)
   };
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    if (__ldg(p.offsets + p.E) != p.R || __ldg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
+    if (__ldcg(p.offsets + p.E) != p.R || __ldcg(p.offsets) != 0) report_status(p.dev_status, NVFP4_E_BAD_ROUTING);
   }
 
   if (warp == 0) {
@@ -250,13 +257,38 @@ __global__ void __launch_bounds__(Geo<G>::THREADS, 1)
     uint32_t issued_mask = 0, issued_par = 0;  // per stage: issued at least once / parity of last issue
     int it_p = 0;
     bool ok = true;
+    // arm stage s for all of its bytes and copy unit cur's weight codes and
+    // scales for K chunk kc into it (the token copies follow separately)
+    auto issue_weights = [&](int s, const Unit& cur, int kc) {
+      uint8_t* sb = smem + s * STAGE_BYTES;
+      const uint8_t* wsc = p.w_scales + ((size_t)(cur.it.e * NT + cur.it.nt) * (p.K / 64)) * (MX ? 256 : 512);
+      ew_arrive_expect_tx(&full_bar[s], W_BYTES + WS_SRC_BYTES + (cur.it.ng == 1 ? 1 : MAXG) * (A_BYTES + AS_BYTES));
+      ew_tma_load_2d(sb, &tm_w, &full_bar[s], kc * (KC / 2), cur.it.e * p.N + cur.it.nt * BM, pol_w);
+      // NVFP4: the 2 KB of packed scale cells; MXFP4: 1 KB of scale pairs,
+      // staged in the upper half and widened in place by warp 6
+      ew_bulk_load(sb + OFF_WS + (MX ? WS_BYTES - WS_SRC_BYTES : 0), wsc + (size_t)kc * WS_SRC_BYTES, WS_SRC_BYTES,
+                   &full_bar[s], pol_w);
+    };
+    // p.early: the weights of the first ring's worth of stages go out now,
+    // while the preceding kernel still runs; iteration it_p < pre then adds
+    // only its token copies
+    int pre = 0;
+    if (p.early) {
+      for (int u = blockIdx.x, j = 0; pre < STAGES && u < units; u += gridDim.x, ++j) {
+        const Unit cur = unit_j(j, u);
+        for (int kc = cur.kc0; kc < cur.kc1 && pre < STAGES; ++kc, ++pre) {
+          if (pre == p.drop_stage) continue;  // never armed (fault injection, below)
+          issue_weights(pre, cur, kc);
+          issued_mask |= 1u << pre;  // first pass over the ring: parity 0
+        }
+      }
+      pdl_wait();  // the token codes and scales come from the preceding kernel
+    }
     for (int u = blockIdx.x, j = 0; ok && u < units; u += gridDim.x, ++j) {
       const Unit cur = unit_j(j, u);
       const int kc0 = cur.kc0, kc1 = cur.kc1;
-      const int e = cur.it.e, nt = cur.it.nt, r0 = cur.it.r0, ng = cur.it.ng;
-      const uint8_t* wsc = p.w_scales + ((size_t)(e * NT + nt) * (p.K / 64)) * (MX ? 256 : 512);
+      const int r0 = cur.it.r0, ng = cur.it.ng;
       {
-        const uint32_t bytes = W_BYTES + WS_SRC_BYTES + (ng == 1 ? 1 : MAXG) * (A_BYTES + AS_BYTES);
         for (int kc = kc0; kc < kc1; ++kc) {
           if (!warp_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.dev_status)) {
             ok = false;
@@ -274,12 +306,7 @@ __global__ void __launch_bounds__(Geo<G>::THREADS, 1)
             }
             continue;
           }
-          ew_arrive_expect_tx(&full_bar[stage], bytes);
-          ew_tma_load_2d(sb, &tm_w, &full_bar[stage], kc * (KC / 2), e * p.N + nt * BM, pol_w);
-          // NVFP4: the 2 KB of packed scale cells; MXFP4: 1 KB of scale pairs,
-          // staged in the upper half and widened in place by warp 6
-          ew_bulk_load(sb + OFF_WS + (MX ? WS_BYTES - WS_SRC_BYTES : 0), wsc + (size_t)kc * WS_SRC_BYTES,
-                       WS_SRC_BYTES, &full_bar[stage], pol_w);
+          if (it_p >= pre) issue_weights(stage, cur, kc);
           // token scales: NVFP4 16 B per row per stage; MXFP4 8 B, so the
           // 16-byte box covers two stages and warp 6 picks its half
           const int as_x = MX ? (kc >> 1) * 16 : kc * (KC / 16);
@@ -463,6 +490,7 @@ __global__ void __launch_bounds__(Geo<G>::THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2-5, 7-10)
+    if (p.early) pdl_wait();  // a_S may come from the preceding kernel
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int eh = warp >= 7 ? 1 : 0;  // which of the two warps on quarter q (G = 4)
     constexpr int GSTEP = GE::EPI_WARPS / 4;
@@ -545,7 +573,7 @@ template <bool MX, int G>
 static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
                                const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                                const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool early) {
   using namespace w4a4;
   if (R == 0 || E == 0) return cudaSuccess;
   if (E > kMaxExperts) return cudaErrorInvalidValue;
@@ -587,6 +615,7 @@ static cudaError_t launch_geo(const uint8_t* a_codes, const uint8_t* a_scales, c
   p.K = K;
   p.R = R;
   p.drop_stage = fault_injection_drop_stage();
+  p.early = early ? 1 : 0;
   // the number of work items depends on the routing, which lives on the
   // device: launch one persistent CTA per SM and let each find its items
   // Split K when even the largest possible number of work items -- N/128
@@ -614,27 +643,27 @@ template <bool MX>
 static cudaError_t launch_impl(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
                                const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                                const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool early) {
   if ((long long)R <= 4LL * E)
     return launch_geo<MX, 1>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
-                             dev_status, st);
+                             dev_status, st, early);
   return launch_geo<MX, 4>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
-                           dev_status, st);
+                           dev_status, st, early);
 }
 
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
                              const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                              const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
-                             cudaStream_t st) {
+                             cudaStream_t st, bool early) {
   return launch_impl<false>(a_codes, a_scales, a_S, w_codes, w_scales_packed, w_S, offsets, E, N, K, R, out,
-                            dev_status, st);
+                            dev_status, st, early);
 }
 
 cudaError_t launch_gemm_mxw4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
                                const uint8_t* w_scales_packed, const int32_t* offsets, int E, int N, int K, int R,
-                               float* out, int32_t* dev_status, cudaStream_t st) {
+                               float* out, int32_t* dev_status, cudaStream_t st, bool early) {
   return launch_impl<true>(a_codes, a_scales, nullptr, w_codes, w_scales_packed, nullptr, offsets, E, N, K, R, out,
-                           dev_status, st);
+                           dev_status, st, early);
 }
 
 }  // namespace nvfp4moe

@@ -90,11 +90,15 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk
                          int32_t* dev_status, void* ws, cudaStream_t st, size_t ws_bytes = (size_t)-1);
 
 // Grouped GEMMs.  Return cudaSuccess or the launch/setup error; host-side
-// argument checks happen before these are called.
+// argument checks happen before these are called.  early = true only where
+// the offsets, the weights and a_S were written by grids that completed
+// before the kernel preceding the GEMM passed its griddepcontrol.wait (a
+// layer's chain of this library's kernels): the GEMM then reads the routing
+// and issues its first weight copies before its own wait.
 cudaError_t launch_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_S,
                              const uint8_t* w_codes, const uint8_t* w_scales_packed, const float* w_S,
                              const int32_t* offsets, int E, int N, int K, int R, float* out, int32_t* dev_status,
-                             cudaStream_t st);
+                             cudaStream_t st, bool early = false);
 // The CTA-pair (.cta_group::2) grouped GEMM for many tokens per expert:
 // eligible when N % 256 == 0 and the experts see >= 1024 rows on average.
 bool gemm_w4a4_pair_eligible(int E, int N, int R);
@@ -170,6 +174,6 @@ cudaError_t launch_swiglu_requant_mx(const float* G, int R, int I, uint8_t* h_co
                                      cudaStream_t st);
 cudaError_t launch_gemm_mxw4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
                                const uint8_t* w_scales_packed, const int32_t* offsets, int E, int N, int K, int R,
-                               float* out, int32_t* dev_status, cudaStream_t st);
+                               float* out, int32_t* dev_status, cudaStream_t st, bool early = false);
 
 }  // namespace nvfp4moe

@@ -21,9 +21,11 @@ struct ExpertRows {
 };
 
 // Rows [m0, m1) of expert e, or an empty range if the offsets are invalid.
+// Read from L2 (ld.global.cg): a kernel may read offsets written by an
+// earlier grid before its own griddepcontrol.wait (see the GEMMs' `early`).
 __device__ __forceinline__ void expert_rows(const ExpertRows& x, int e, int& m0, int& m1) {
-  m0 = __ldg(x.offsets + e);
-  m1 = __ldg(x.offsets + e + 1);
+  m0 = __ldcg(x.offsets + e);
+  m1 = __ldcg(x.offsets + e + 1);
   if (m0 < 0 || m1 < m0 || m1 > x.R) m0 = m1 = 0;
 }
 
