@@ -166,3 +166,35 @@ def test_combine_rejects_more_than_32_slots_without_gpu():
     L = binding.load()
     p16 = ctypes.c_void_p(16)
     assert L.moe_combine(p16, p16, p16, 4, 33, 64, 1, p16, None, None) == 2
+
+
+def test_early_gemms_only_inside_the_layer_chain():
+    """The grouped GEMMs' early mode reads the routing and issues weight
+    copies before the grid-dependency wait.  That is safe only where the
+    routing was written by a kernel that completed before the GEMM's
+    predecessor passed its own wait: inside moe_layer_forward's chain.  So
+    every internal GEMM call that passes early = true must sit in that
+    function, and the public entry point must pass false (source check)."""
+    src = open(os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc", "api.cu")).read()
+    lines = src.splitlines()
+    owner = None
+    early_calls, public_false = [], False
+    for i, line in enumerate(lines):
+        m = re.match(r"^(?:static\s+)?int\s+(\w+)\(", line)
+        if m:
+            owner = m.group(1)
+        if re.search(r"\bgrouped_gemm\(", line) and not line.lstrip().startswith("static"):
+            call = " ".join(lines[i:i + 4])
+            call = call[: call.index(";") + 1]
+            flag = call.rstrip(");").rsplit(",", 1)[1].strip()
+            if flag == "true":
+                early_calls.append(owner)
+            elif owner == "moe_grouped_gemm_nvfp4" and flag == "false":
+                public_false = True
+    assert early_calls and set(early_calls) == {"moe_layer_forward"}, early_calls
+    assert public_false
+    # no other file launches a GEMM in early mode
+    csrc = os.path.join(ROOT, "nvfp4_mixture_experts_top_gb300", "csrc")
+    for fn in os.listdir(csrc):
+        if fn.endswith(".cu") and fn not in ("api.cu", "gemm_w4a4.cu"):
+            assert not re.search(r"\bearly\b", open(os.path.join(csrc, fn)).read()), fn
