@@ -100,7 +100,6 @@ struct Geo {
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_STAGE = 32;
 
-
 struct Params {
   const uint8_t* w_scales;  // packed atoms
   const float* w_S;
